@@ -1,0 +1,227 @@
+// Device primitives for the sm_103a sampler: bulk-copy (TMA) loads with
+// mbarriers and bounded waits, order-preserving float keys, the Splitmix64
+// generator, fixed-point masses and warp/cluster reductions.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "arc_sample.h"
+
+namespace arc {
+namespace cg = cooperative_groups;
+
+constexpr int kThreads = 256;              // threads per CTA
+constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 1024;                // histogram bins per select pass
+constexpr int kBinBits = 10;
+constexpr int kMaxCluster = 16;
+constexpr int kPieces = 4;                 // bulk copies per slice
+constexpr unsigned long long kWaitNs = 200ull * 1000ull * 1000ull;  // 200 ms wait bound
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bulk global -> shared copy completing on `bar` (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar` to complete; gives up after kWaitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+        __nanosleep(128);
+    }
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ------------------------------------------------------------------ keys
+// Order-preserving u32 key of a non-NaN float, reading -0 as +0.
+__device__ __forceinline__ uint32_t fkey(float z) {
+    const uint32_t b = __float_as_uint(__fadd_rn(z, 0.0f));
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+    const uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(b);
+}
+
+// ------------------------------------------------------------------ generator
+// Splitmix64 (Steele, Lea, Flood 2014): one output for state x.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+    uint64_t z = x + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// floor(rbits * mass / 2^53) exactly (128-bit product).
+__device__ __forceinline__ uint64_t scale_by_u(uint64_t rbits, uint64_t mass) {
+    const uint64_t lo = rbits * mass;
+    const uint64_t hi = __umul64hi(rbits, mass);
+    return (hi << 11) | (lo >> 53);
+}
+
+// ------------------------------------------------------------------ element loads
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<ARC_F32> {
+    static constexpr int kVec = 4;    // elements per 16-byte vector
+    static constexpr int kBytes = 4;
+    __device__ __forceinline__ static void unpack(const uint4& v, float (&z)[4]) {
+        z[0] = __uint_as_float(v.x);
+        z[1] = __uint_as_float(v.y);
+        z[2] = __uint_as_float(v.z);
+        z[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static float load_scalar(const void* row, int64_t i) {
+        return __ldg(reinterpret_cast<const float*>(row) + i);
+    }
+    __device__ __forceinline__ static float from_smem(const void* base, int i) {
+        return reinterpret_cast<const float*>(base)[i];
+    }
+    __device__ __forceinline__ static void store_smem_raw(void* base, int i, const void* row, int64_t gi) {
+        reinterpret_cast<uint32_t*>(base)[i] = __ldg(reinterpret_cast<const uint32_t*>(row) + gi);
+    }
+};
+
+template <>
+struct Elem<ARC_BF16> {
+    static constexpr int kVec = 8;
+    static constexpr int kBytes = 2;
+    __device__ __forceinline__ static void unpack(const uint4& v, float (&z)[8]) {
+        z[0] = __uint_as_float(v.x << 16);
+        z[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        z[2] = __uint_as_float(v.y << 16);
+        z[3] = __uint_as_float(v.y & 0xFFFF0000u);
+        z[4] = __uint_as_float(v.z << 16);
+        z[5] = __uint_as_float(v.z & 0xFFFF0000u);
+        z[6] = __uint_as_float(v.w << 16);
+        z[7] = __uint_as_float(v.w & 0xFFFF0000u);
+    }
+    __device__ __forceinline__ static float load_scalar(const void* row, int64_t i) {
+        const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    }
+    __device__ __forceinline__ static float from_smem(const void* base, int i) {
+        const unsigned short h = reinterpret_cast<const unsigned short*>(base)[i];
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    }
+    __device__ __forceinline__ static void store_smem_raw(void* base, int i, const void* row, int64_t gi) {
+        reinterpret_cast<unsigned short*>(base)[i] =
+            __ldg(reinterpret_cast<const unsigned short*>(row) + gi);
+    }
+};
+
+// ------------------------------------------------------------------ warp helpers
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+    const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), src);
+    const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), src);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t shfl_up_u64(uint64_t v, int d) {
+    const uint32_t lo = __shfl_up_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), d);
+    const uint32_t hi = __shfl_up_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), d);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), d);
+        const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), d);
+        v += (static_cast<uint64_t>(hi) << 32) | lo;
+    }
+    return v;
+}
+
+__device__ __forceinline__ uint64_t warp_inclusive_u64(uint64_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint64_t o = shfl_up_u64(v, d);
+        if (lane >= d) v += o;
+    }
+    return v;
+}
+
+// (value, index) max with ties to the smaller index; -1 index means "none".
+__device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
+    if (i2 >= 0 && (i < 0 || v2 > v || (v2 == v && i2 < i))) {
+        v = v2;
+        i = i2;
+    }
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, d);
+        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, d);
+        better(v, i, v2, i2);
+    }
+}
+
+}  // namespace arc

@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header
+declares, and rejects bad arguments before touching CUDA (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+from device_logits_sampling_gb300 import sampler, workloads
+
+HEADER = os.path.join(ROOT, "include", "arc_sample.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(sampler.LIB_PATH):
+        from device_logits_sampling_gb300 import build
+
+        build.build()
+    return sampler.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s*(arc_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert names == sorted(["arc_sample_batch", "arc_sample_greedy", "arc_sample_plan",
+                            "arc_sample_strerror", "arc_sample_abi_version"]), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", sampler.LIB_PATH], capture_output=True, text=True)
+    exported = set(re.findall(r"\bT (arc_\w+)", out.stdout))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing else with the public prefix leaks out
+    assert exported == set(declared_functions())
+
+
+def test_abi_version_and_strerror(lib):
+    assert lib.arc_sample_abi_version() == 1
+    assert sampler.strerror(0) == "ok"
+    for rc in range(-1, -8, -1):
+        assert len(sampler.strerror(rc)) > 10 and "unknown" not in sampler.strerror(rc)
+    assert "unknown" in sampler.strerror(-99)
+
+
+def test_struct_layouts_match_header():
+    assert workloads.ROW_PARAMS_DTYPE.itemsize == 48
+    assert sampler.ROW_DEBUG_DTYPE.itemsize == 72
+    assert ctypes.sizeof(sampler.Options) == 24
+    assert ctypes.sizeof(sampler.Geometry) == 32
+    # field offsets of arc_row_params as laid out in the header
+    off = {n: workloads.ROW_PARAMS_DTYPE.fields[n][1] for n in workloads.ROW_PARAMS_DTYPE.names}
+    assert off["temperature"] == 0 and off["top_k"] == 4 and off["flags"] == 28
+    assert off["seed"] == 32 and off["step"] == 40
+
+
+FAKE = 0x1000  # a non-NULL, aligned pointer that is never dereferenced
+
+
+def call_batch(lib, logits=FAKE, B=2, V=8, ld=8, dtype=1, params=FAKE, hoff=None, hids=None, out=FAKE,
+               opts=None):
+    o = ctypes.byref(opts) if opts is not None else None
+    return lib.arc_sample_batch(logits, B, V, ld, dtype, params, hoff, hids, out, None, o, None)
+
+
+def test_bad_arguments_fail_before_any_cuda_call(lib):
+    assert call_batch(lib, logits=None) == sampler.ARC_E_NULL
+    assert call_batch(lib, out=None) == sampler.ARC_E_NULL
+    assert call_batch(lib, params=None) == sampler.ARC_E_NULL
+    assert call_batch(lib, hoff=FAKE, hids=None) == sampler.ARC_E_NULL
+    assert call_batch(lib, B=0) == sampler.ARC_E_SHAPE
+    assert call_batch(lib, B=-3) == sampler.ARC_E_SHAPE
+    assert call_batch(lib, V=0) == sampler.ARC_E_SHAPE
+    assert call_batch(lib, V=2**31) == sampler.ARC_E_SHAPE
+    assert call_batch(lib, ld=7) == sampler.ARC_E_SHAPE
+    assert call_batch(lib, dtype=2) == sampler.ARC_E_DTYPE
+    assert call_batch(lib, dtype=-1) == sampler.ARC_E_DTYPE
+    assert call_batch(lib, logits=FAKE + 1) == sampler.ARC_E_ALIGN
+    assert call_batch(lib, logits=FAKE + 2, dtype=0) == sampler.ARC_E_ALIGN
+    assert call_batch(lib, params=FAKE + 4) == sampler.ARC_E_ALIGN
+    assert call_batch(lib, opts=sampler.Options(0, 3, 0, 0, None)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, opts=sampler.Options(0x80, 0, 0, 0, None)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, opts=sampler.Options(0, 0, -1, 0, None)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, opts=sampler.Options(0, 0, 0, 5, None)) == sampler.ARC_E_OPTION
+    g = lib.arc_sample_greedy
+    assert g(None, 2, 8, 8, 1, FAKE, None, None) == sampler.ARC_E_NULL
+    assert g(FAKE, 2, 8, 4, 1, FAKE, None, None) == sampler.ARC_E_SHAPE
+    assert g(FAKE, 2, 8, 8, 7, FAKE, None, None) == sampler.ARC_E_DTYPE
+
+
+def test_plan_geometry(lib):
+    # the mixed B=256 bf16 batch: 8 CTAs per row, 16,160 logits (32,320 B) each
+    g = sampler.plan(256, workloads.VOCAB_V4, workloads.DTYPE_BF16)
+    assert (g.cluster_ctas, g.slice_elems, g.grid_ctas, g.threads) == (8, 16160, 2048, 256)
+    assert g.frac_bits == 62 - 17
+    # a single row is split over the largest cluster
+    assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16).cluster_ctas == 16
+    # fp32 rows need twice the CTAs per row
+    assert sampler.plan(64, workloads.VOCAB_V4, workloads.DTYPE_F32).cluster_ctas == 16
+    # small vocabularies stay on one CTA
+    assert sampler.plan(4, 1024, workloads.DTYPE_F32).cluster_ctas == 1
+    # a forced cluster that cannot hold the row on chip is refused
+    with pytest.raises(sampler.ArcError) as e:
+        sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16, cluster_ctas=1)
+    assert e.value.rc == sampler.ARC_E_UNSUPPORTED
+    # history support reserves bitmap + patch space
+    g2 = sampler.plan(512, workloads.VOCAB_V4, workloads.DTYPE_BF16, has_history=True, max_hist_len=256)
+    assert g2.smem_bytes > g.smem_bytes
+    # every slice covers the row: s * L >= V with L a multiple of the vector width
+    for B, V, dt in [(3, 1, 1), (7, 9, 0), (1, 12345, 1), (33, 4097, 0), (2, 200_000, 1)]:
+        gg = sampler.plan(B, V, dt)
+        assert gg.cluster_ctas * gg.slice_elems >= V
+        assert gg.slice_elems % (8 if dt == 1 else 4) == 0
+
+
+def test_workload_generators_are_deterministic():
+    a = workloads.mixed_batch(B=8, V=1000)
+    b = workloads.mixed_batch(B=8, V=1000)
+    assert a.logits.tobytes() == b.logits.tobytes()
+    assert a.params.tobytes() == b.params.tobytes()
+    # bf16 rounding is round-to-nearest-even
+    x = np.array([1.0, 1.00390625, 1.01171875, -2.5, 3.0e38], dtype=np.float32)
+    bits = workloads.f32_to_bf16_bits(x)
+    assert bits.tolist() == [0x3F80, 0x3F80, 0x3F82, 0xC020, 0x7F62]
+    assert np.array_equal(workloads.bf16_bits_to_f32(bits)[:4], np.array([1.0, 1.0, 1.015625, -2.5], np.float32))
