@@ -15,8 +15,9 @@ namespace cg = cooperative_groups;
 
 constexpr int kThreads = 256;              // threads per CTA
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins = 1024;                // histogram bins per select pass
-constexpr int kBinBits = 10;
+constexpr int kBins = 512;                 // histogram bins per select pass
+constexpr int kBinBits = 9;
+constexpr int kCand = 256;                 // crossing-bin candidates gathered per row
 constexpr int kMaxCluster = 16;
 constexpr int kPieces = 4;                 // bulk copies per slice
 constexpr unsigned long long kWaitNs = 200ull * 1000ull * 1000ull;  // 200 ms wait bound
@@ -50,14 +51,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// try_wait that lets the hardware suspend the thread for up to `ns` nanoseconds
+// while the phase is incomplete (no busy polling).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
         : "memory");
     return ok != 0;
 }
@@ -68,15 +71,30 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` to complete; gives up after kWaitNs.
+// Wait for phase `parity` of `bar`; gives up after kWaitNs of wall time.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, 1000000u)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, 1000000u)) return true;
         if (global_ns() - t0 > kWaitNs) return false;
-        __nanosleep(128);
     }
+}
+
+// Split cluster barrier: arrive after this CTA's last read of another CTA's
+// shared memory, wait before leaving.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// IEEE max that propagates NaN (max.NaN, sm_80+).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -135,6 +153,11 @@ struct Elem<ARC_F32> {
         z[2] = __uint_as_float(v.z);
         z[3] = __uint_as_float(v.w);
     }
+    // max of the vector, propagating NaN
+    __device__ __forceinline__ static float vmax_nan(const uint4& v) {
+        return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                        fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
     __device__ __forceinline__ static float load_scalar(const void* row, int64_t i) {
         return __ldg(reinterpret_cast<const float*>(row) + i);
     }
@@ -159,6 +182,15 @@ struct Elem<ARC_BF16> {
         z[5] = __uint_as_float(v.z & 0xFFFF0000u);
         z[6] = __uint_as_float(v.w << 16);
         z[7] = __uint_as_float(v.w & 0xFFFF0000u);
+    }
+    // max of the vector, propagating NaN (packed bf16x2 max, exact)
+    __device__ __forceinline__ static float vmax_nan(const uint4& v) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+        const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+        const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+        return fmax_nan(__low2float(m), __high2float(m));
     }
     __device__ __forceinline__ static float load_scalar(const void* row, int64_t i) {
         const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + i);

@@ -22,7 +22,9 @@ constexpr int kAssumedSMs = 152;
 struct Plan {
     int s = 1;
     int L = 0;
-    int data_bytes = 0;
+    int vmax_off = 0;
+    int wsum_off = 0;
+    int hist_off_b = 0;
     int rounds_max = 0;
     int hist_cap = 0;
     int smem = 0;
@@ -84,8 +86,12 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     const int64_t L = ((per + vec - 1) / vec) * vec;
     const int64_t nv_max = L / vec;
     const int64_t rounds_max = (nv_max + kThreads - 1) / kThreads;
-    int64_t data_bytes = ((nv_max * 16 + 127) / 128) * 128;
-    int64_t smem = data_bytes + rounds_max * kWarps * 8;
+    // dynamic shared memory: slice | per-vector max | per-(round, warp) masses | history tables
+    const int64_t data_bytes = ((nv_max * 16 + 127) / 128) * 128;
+    const int64_t vmax_off = data_bytes;
+    const int64_t wsum_off = vmax_off + ((nv_max * 4 + 15) / 16) * 16;
+    const int64_t hist_off_b = wsum_off + rounds_max * kWarps * 8;
+    int64_t smem = hist_off_b;
     int cap = 0;
     if (has_hist) {
         cap = (o != nullptr && o->max_hist_len > 0) ? o->max_hist_len : kDefaultHist;
@@ -96,7 +102,9 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     if (smem > limit) return ARC_E_UNSUPPORTED;
     p.s = s;
     p.L = static_cast<int>(L);
-    p.data_bytes = static_cast<int>(data_bytes);
+    p.vmax_off = static_cast<int>(vmax_off);
+    p.wsum_off = static_cast<int>(wsum_off);
+    p.hist_off_b = static_cast<int>(hist_off_b);
     p.rounds_max = static_cast<int>(rounds_max);
     p.hist_cap = cap;
     p.smem = static_cast<int>(smem);
@@ -222,7 +230,9 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     a.err_word = err_word;
     a.debug = opts ? opts->debug : nullptr;
     a.L = p.L;
-    a.data_bytes = p.data_bytes;
+    a.vmax_off = p.vmax_off;
+    a.wsum_off = p.wsum_off;
+    a.hist_off_b = p.hist_off_b;
     a.rounds_max = p.rounds_max;
     a.hist_cap = p.hist_cap;
     a.F = p.F;

@@ -3,14 +3,22 @@
 // Each CTA bulk-copies (TMA, cp.async.bulk) its contiguous slice of the row
 // into shared memory once; every later look at the row -- max, top-k select,
 // top-p select, masses, the inverse-CDF walk -- runs out of shared memory.
+// Pass 1 also caches each 16-byte vector's max, so later threshold passes
+// skip vectors that cannot hold a survivor without reading them.
+//
 // CTAs of a row combine partial results through distributed shared memory
-// (DSMEM) and cluster barriers; every decision is computed redundantly and
-// identically by all CTAs, so control flow stays uniform across the cluster.
+// (DSMEM).  Every decision is computed redundantly and identically by all
+// CTAs from the same exchanged data, so control flow, and with it the
+// sequence of cluster barriers, is uniform across the cluster.
 //
 // Thresholds are found by multi-way threshold bisection on the order-
-// preserving u32 key of the logit: a 1024-bin histogram over a key window
-// below the row max narrows the window by 10 bits per pass until the bin that
-// crosses the target count (top-k) or target mass (top-p) holds one key.
+// preserving u32 key of the logit: a 512-bin histogram of the keys in a window
+// below the row max (each CTA adds its non-zero bins into every CTA's cluster
+// histogram with DSMEM atomics; one cluster barrier) locates the bin that
+// crosses the target count (top-k) or mass (top-p); the few ids in that bin
+// are then gathered into every CTA and ranked exactly.  Bins that hold too
+// many ids are bisected further, 9 bits per pass.
+//
 // Masses are fixed-point integers (units of 2^-F of the max weight), so sums
 // are exact, associative and identical in every pass, CTA and cluster size.
 #pragma once
@@ -33,7 +41,9 @@ struct SampleArgs {
     uint32_t* err_word;
     arc_row_debug* debug;
     int L;           // slice elements per CTA (multiple of the vector width)
-    int data_bytes;  // bytes reserved for the slice in dynamic shared memory
+    int vmax_off;    // dynamic shared memory offsets: per-vector max,
+    int wsum_off;    //   per-(round, warp) masses,
+    int hist_off_b;  //   history patch tables
     int rounds_max;  // rounds of the largest slice
     int hist_cap;    // history entries per row (patch table capacity)
     int F;           // fixed-point fraction bits
@@ -43,19 +53,20 @@ struct SampleArgs {
 
 struct __align__(16) SampleShared {
     uint64_t bar[kPieces];
-    uint64_t hist[kBins];
-    uint64_t seg[kBins / 2];
-    uint64_t slot[2][8];
+    uint64_t lhist[kBins];  // this CTA's histogram
+    uint64_t ghist[kBins];  // the cluster's histogram (every CTA adds into it)
+    uint64_t cval[kCand];   // gathered candidates: id or mass
+    uint32_t ckey[kCand];   //   and key
+    uint64_t slot[2][8];    // exchange ring
     uint64_t wred[kWarps];
     uint64_t bcast_u[4];
     int bcast_i[4];
     uint32_t wred32[kWarps];
-    uint32_t mm[2];
+    uint32_t ccount;        // candidates pushed into this CTA
     uint32_t flags;
 };
 
-// internal error bit: a search that exact integer arithmetic guarantees failed
-constexpr uint32_t kErrInternal = 0x40u;
+constexpr uint32_t kErrInternal = ARC_ERR_INTERNAL;
 
 // Survivor predicate on the penalised logit z at id `idx`:
 // survive iff z > zt || (z == zt && idx < iota); iota == INT_MAX means z >= zt.
@@ -68,6 +79,15 @@ struct Surv {
     }
 };
 
+// How a mass pass tests its domain: every id (the row has no NaN), z >= zt,
+// or the full (z, id) predicate.
+enum MassMode { kAll = 0, kGe = 1, kTie = 2 };
+
+struct Window {
+    uint32_t klo, khi;
+    int sh;
+};
+
 template <int DT, bool HIST>
 struct RowCtx {
     using E = Elem<DT>;
@@ -78,21 +98,32 @@ struct RowCtx {
     int s, rank, row, tid, lane, warp;
     int a0, a1, n, nv, nvf, rounds;
     const unsigned char* data;
+    float* vmax;
     uint64_t* Wsum;
     // history patches
     const uint32_t* bm;
     const uint32_t* wp;
     const float* patch;
     bool has_patch;
+    bool row_nan;
     // weights: w = ex2((z - m) * c), or [z == m] when m = +inf
     float m, c, scale;
     bool infm;
-    int par;      // exchange ring parity
+    int par;           // exchange ring parity
     int passes;
+    int epoch;         // cluster barriers so far
+    int ghist_zeroed;  // epoch at which the cluster histogram was last cleared
+    int cand_zeroed;   // epoch at which the candidate count was last cleared
 
     __device__ RowCtx(SampleShared& S_, cg::cluster_group cl_) : S(S_), cl(cl_) {}
 
     // ---------------------------------------------------------------- loads
+    __device__ __forceinline__ bool vec_patched(int v) const {
+        if (!(HIST && has_patch)) return false;
+        const int l0 = v * VEC;
+        return ((bm[l0 >> 5] >> (l0 & 31)) & ((1u << VEC) - 1u)) != 0;
+    }
+
     __device__ __forceinline__ void load(int v, float (&z)[VEC]) const {
         const uint4 raw = reinterpret_cast<const uint4*>(data)[v];
         E::unpack(raw, z);
@@ -117,72 +148,56 @@ struct RowCtx {
 
     __device__ __forceinline__ uint64_t fix(float w) const { return __float2ull_rn(__fmul_rn(w, scale)); }
 
-    // fixed-point mass of the survivors of one vector (fp32 sum in id order, then rounded)
-    template <bool TIE>
-    __device__ __forceinline__ uint64_t vec_mass(const float (&z)[VEC], int g0, const Surv& d) const {
-        bool in[VEC];
-        bool any = false;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            in[e] = TIE ? d.test(z[e], g0 + e) : (z[e] >= d.zt);
-            any |= in[e];
-        }
-        if (!any) return 0;
+    __device__ __forceinline__ static bool in_domain(int mode, const Surv& d, float z, int idx) {
+        return mode == kAll ? true : (mode == kGe ? (z >= d.zt) : d.test(z, idx));
+    }
+
+    // fixed-point mass of the survivors of one vector: fp32 sum in id order,
+    // rounded once
+    __device__ __forceinline__ uint64_t vec_mass(int mode, const float (&z)[VEC], int g0, const Surv& d) const {
         float sum = 0.0f;
+        if (mode == kAll) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            if (in[e]) sum = __fadd_rn(sum, weight(z[e]));
+            for (int e = 0; e < VEC; ++e) sum = __fadd_rn(sum, weight(z[e]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                if (in_domain(mode, d, z[e], g0 + e)) sum = __fadd_rn(sum, weight(z[e]));
+        }
         return fix(sum);
     }
 
     // first element of the vector whose running fixed-point mass exceeds t
-    template <bool TIE>
-    __device__ __forceinline__ int vec_mass_walk(const float (&z)[VEC], int g0, const Surv& d,
+    __device__ __forceinline__ int vec_mass_walk(int mode, const float (&z)[VEC], int g0, const Surv& d,
                                                  uint64_t t) const {
         float sum = 0.0f;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-            const bool in = TIE ? d.test(z[e], g0 + e) : (z[e] >= d.zt);
-            if (in) sum = __fadd_rn(sum, weight(z[e]));
+            if (in_domain(mode, d, z[e], g0 + e)) sum = __fadd_rn(sum, weight(z[e]));
             if (fix(sum) > t) return e;
         }
         return -1;
     }
 
-    __device__ __forceinline__ static uint64_t vec_count_eq(const float (&z)[VEC], float zt) {
-        uint64_t c = 0;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) c += (z[e] == zt) ? 1u : 0u;
-        return c;
-    }
-
-    __device__ __forceinline__ static int vec_count_walk(const float (&z)[VEC], float zt, uint64_t t) {
-        uint64_t c = 0;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            c += (z[e] == zt) ? 1u : 0u;
-            if (c > t) return e;
-        }
-        return -1;
-    }
-
     // ---------------------------------------------------------------- cluster exchange
-    // Thread 0 wrote S.slot[par][*]; after sync every CTA reads every rank's slot.
-    __device__ __forceinline__ void xsync() { cl.sync(); }
+    __device__ __forceinline__ void xsync() {
+        cl.sync();
+        epoch++;
+    }
     __device__ __forceinline__ uint64_t xread(int r, int i) const {
         return cl.map_shared_rank(&S.slot[par][0], r)[i];
     }
     __device__ __forceinline__ void xnext() { par ^= 1; }
 
-    // Sum of a per-CTA value over the cluster plus the exclusive prefix of
-    // this CTA and the first rank whose inclusive prefix exceeds t (or -1).
     struct Scan {
         uint64_t total, before_me;
         int first;
         uint64_t before_first;
     };
+    // Sum over the cluster of slot value i, this CTA's exclusive prefix and the
+    // first rank whose inclusive prefix exceeds t (-1 if none).
     __device__ __forceinline__ Scan xscan(int i, uint64_t t) const {
-        uint64_t x = (lane < s) ? xread(lane, i) : 0;
+        const uint64_t x = (lane < s) ? xread(lane, i) : 0;
         const uint64_t inc = warp_inclusive_u64(x);
         Scan r;
         r.total = shfl_u64(inc, 31);
@@ -193,7 +208,7 @@ struct RowCtx {
         return r;
     }
 
-    // Total of Wsum[0 .. rounds*kWarps) of this CTA into slot i (thread 0 of warp 0).
+    // Total of this CTA's Wsum into S.slot[par][i].
     __device__ __forceinline__ void publish_wsum_total(int i) {
         __syncthreads();
         if (warp == 0) {
@@ -204,8 +219,7 @@ struct RowCtx {
         }
     }
 
-    // warp-level search of arr[0..n) (generic pointer, may be remote) for the
-    // first position whose inclusive prefix exceeds t.  All lanes get the result.
+    // First position of arr[0..n) whose inclusive prefix exceeds t (warp-wide).
     __device__ __forceinline__ static void warp_find(const uint64_t* arr, int n, uint64_t t, int& pos,
                                                      uint64_t& before, uint64_t& value) {
         const int ln = threadIdx.x & 31;
@@ -226,13 +240,10 @@ struct RowCtx {
             }
             base = shfl_u64(inc, 31);
         }
+        before = base;  // the total when nothing crosses
     }
 
-    // ---------------------------------------------------------------- histogram select
-    struct Window {
-        uint32_t klo, khi;
-        int sh;
-    };
+    // ---------------------------------------------------------------- histograms
     __device__ __forceinline__ static int bitlen(uint32_t x) { return x ? 32 - __clz(x) : 0; }
     __device__ __forceinline__ static Window make_window(uint32_t klo, uint32_t khi) {
         Window w;
@@ -245,99 +256,85 @@ struct RowCtx {
         return klo <= 0x007FFFFFu ? -INFINITY : key_to_float(klo);
     }
 
-    // Adds `wt` to the bin of key `k` if it lies in the window.
-    __device__ __forceinline__ void hist_add(const Window& W, uint32_t k, uint64_t wt, bool track) {
+    __device__ __forceinline__ void lhist_add(const Window& W, uint32_t k, uint64_t wt) {
         if (k < W.klo || k > W.khi) return;
-        atomicAdd(reinterpret_cast<unsigned long long*>(&S.hist[(W.khi - k) >> W.sh]),
+        atomicAdd(reinterpret_cast<unsigned long long*>(&S.lhist[(W.khi - k) >> W.sh]),
                   static_cast<unsigned long long>(wt));
-        if (track) {
-            atomicMin(&S.mm[0], k);
-            atomicMax(&S.mm[1], k);
+    }
+
+    __device__ __forceinline__ void lhist_clear() {
+        for (int b = tid; b < kBins; b += kThreads) S.lhist[b] = 0;
+        __syncthreads();
+    }
+
+    // Clear the cluster histogram / candidate count after their last local
+    // read.  A cluster barrier must separate a clear from the next remote
+    // push into it; the push helpers add one when none has passed.
+    __device__ __forceinline__ void ghist_clear() {
+        __syncthreads();
+        for (int b = tid; b < kBins; b += kThreads) S.ghist[b] = 0;
+        ghist_zeroed = epoch;
+    }
+    __device__ __forceinline__ void cand_clear() {
+        __syncthreads();
+        if (tid == 0) S.ccount = 0;
+        cand_zeroed = epoch;
+    }
+
+    // Add this CTA's non-zero bins into every CTA's cluster histogram.
+    __device__ __forceinline__ void push_hist() {
+        if (ghist_zeroed >= epoch) xsync();
+        for (int b = tid; b < kBins; b += kThreads) {
+            const uint64_t v = S.lhist[b];
+            if (v)
+                for (int q = 0; q < s; ++q)
+                    atomicAdd(reinterpret_cast<unsigned long long*>(cl.map_shared_rank(S.ghist, q) + b),
+                              static_cast<unsigned long long>(v));
         }
     }
 
-    __device__ __forceinline__ void hist_clear() {
-        for (int b = tid; b < kBins; b += kThreads) S.hist[b] = 0;
-        if (tid == 0) {
-            S.mm[0] = 0xFFFFFFFFu;
-            S.mm[1] = 0u;
+    // Give a candidate (key, value) to every CTA of the cluster.  The count
+    // keeps growing past kCand so that every CTA sees the true total.
+    __device__ __forceinline__ void push_cand(uint32_t key, uint64_t val) {
+        for (int q = 0; q < s; ++q) {
+            const uint32_t slot_i = atomicAdd(cl.map_shared_rank(&S.ccount, q), 1u);
+            if (slot_i < static_cast<uint32_t>(kCand)) {
+                cl.map_shared_rank(S.ckey, q)[slot_i] = key;
+                cl.map_shared_rank(S.cval, q)[slot_i] = val;
+            }
         }
-        __syncthreads();
     }
 
     struct Sel {
-        int bin;          // crossing bin (-1: window total does not reach the target)
-        uint64_t before;  // weight in bins above it
+        int bin;          // crossing bin (-1: the window does not reach the target)
+        uint64_t before;  // weight in the bins above it
         uint64_t inbin;   // weight in it
-        uint64_t total;   // weight in the window
-        uint32_t mmin, mmax;
     };
 
-    // Combine the CTAs' histograms and find the first bin whose inclusive
-    // prefix (from the top key down) reaches target (>= target).
-    __device__ Sel hist_exchange(uint64_t target) {
-        Sel r;
-        const int segsz = kBins / s;
-        uint64_t* segp = (s == 1) ? S.hist : S.seg;
-        xsync();  // A: histograms complete in every CTA
-        uint64_t part = 0;
-        if (s > 1) {
-            const int b0 = rank * segsz;
-            for (int b = tid; b < segsz; b += kThreads) {
-                uint64_t acc = 0;
-                for (int q = 0; q < s; ++q) acc += cl.map_shared_rank(S.hist, q)[b0 + b];
-                S.seg[b] = acc;
-                part += acc;
+    // After the barrier that completes the cluster histogram: the first bin
+    // whose inclusive prefix (from the top key down) is >= target.
+    __device__ Sel ghist_find(uint64_t target) {
+        if (warp == 0) {
+            int pos;
+            uint64_t bf, val;
+            warp_find(S.ghist, kBins, target - 1, pos, bf, val);
+            if (lane == 0) {
+                S.bcast_i[0] = pos;
+                S.bcast_u[0] = bf;
+                S.bcast_u[1] = val;
             }
-        } else {
-            for (int b = tid; b < segsz; b += kThreads) part += S.hist[b];
         }
-        part = warp_sum_u64(part);
-        if (lane == 0) S.wred[warp] = part;
         __syncthreads();
-        if (tid == 0) {
-            uint64_t tot = 0;
-            for (int w = 0; w < kWarps; ++w) tot += S.wred[w];
-            S.slot[par][0] = tot;
-            S.slot[par][1] = S.mm[0];
-            S.slot[par][2] = S.mm[1];
-        }
-        xsync();  // B: segments combined
-        const Scan sc = xscan(0, target - 1);
-        uint32_t mn = (lane < s) ? static_cast<uint32_t>(xread(lane, 1)) : 0xFFFFFFFFu;
-        uint32_t mx = (lane < s) ? static_cast<uint32_t>(xread(lane, 2)) : 0u;
-        mn = __reduce_min_sync(0xFFFFFFFFu, mn);
-        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-        r.total = sc.total;
-        r.mmin = mn;
-        r.mmax = mx;
-        r.bin = -1;
-        r.before = r.inbin = 0;
-        if (sc.first >= 0) {
-            if (warp == 0) {
-                const uint64_t* remote = cl.map_shared_rank(segp, sc.first);
-                int pos;
-                uint64_t bf, val;
-                warp_find(remote, segsz, target - 1 - sc.before_first, pos, bf, val);
-                if (lane == 0) {
-                    S.bcast_i[0] = pos < 0 ? -1 : sc.first * segsz + pos;
-                    S.bcast_u[0] = sc.before_first + bf;
-                    S.bcast_u[1] = val;
-                }
-            }
-            __syncthreads();
-            r.bin = S.bcast_i[0];
-            r.before = S.bcast_u[0];
-            r.inbin = S.bcast_u[1];
-            __syncthreads();
-        }
-        xnext();
+        Sel r;
+        r.bin = S.bcast_i[0];
+        r.before = S.bcast_u[0];
+        r.inbin = S.bcast_u[1];
         return r;
     }
 
     // ---------------------------------------------------------------- index-order walk
-    // In CTA `owner`, find the element whose running weight (in id order over
-    // this CTA's Wsum chunks) first exceeds t.  Returns the row index or -1.
+    // In this CTA, the element whose running weight (in id order over the
+    // Wsum chunks) first exceeds t.  Returns the row index or -1.
     template <class VecW, class VecWalk>
     __device__ int walk(uint64_t t, VecW vecw, VecWalk vecwalk) {
         if (warp == 0) {
@@ -374,7 +371,6 @@ struct RowCtx {
     }
 };
 
-
 // Row parameters, read once with volatile loads so that no field is fetched
 // after the first cluster barrier (rank 0 may rewrite `step` after it).
 __device__ __forceinline__ arc_row_params load_params(const arc_row_params* p) {
@@ -396,77 +392,85 @@ __device__ __forceinline__ arc_row_params load_params(const arc_row_params* p) {
     return r;
 }
 
-// Key range [bin_lo, bin_hi] of histogram bin `b` of window W.
-template <class Ctx>
-__device__ __forceinline__ void bin_range(const typename Ctx::Window& W, int b, uint32_t& lo, uint32_t& hi) {
+// Key range [lo, hi] of histogram bin `b` of window W.
+__device__ __forceinline__ void bin_range(const Window& W, int b, uint32_t& lo, uint32_t& hi) {
     hi = W.khi - (static_cast<uint32_t>(b) << W.sh);
     int64_t lo64 = static_cast<int64_t>(hi) - ((int64_t{1} << W.sh) - 1);
     if (lo64 < static_cast<int64_t>(W.klo)) lo64 = static_cast<int64_t>(W.klo);
     lo = static_cast<uint32_t>(lo64);
 }
 
-// Count histogram of the keys in window W (every non-NaN id).
-template <class Ctx>
-__device__ void pass_count_hist(Ctx& X, const typename Ctx::Window& W, bool track) {
+// Local histogram of the ids of D whose keys lie in W: counts (MASS = false)
+// or fixed-point masses.  Vectors whose max is below the window are skipped.
+template <class Ctx, bool MASS>
+__device__ void pass_hist(Ctx& X, const Window& W, const Surv& D) {
     constexpr int VEC = Ctx::VEC;
-    X.hist_clear();
+    X.lhist_clear();
     const float zlo = Ctx::lo_float(W.klo), zhi = key_to_float(W.khi);
+    const float thr = fmaxf(zlo, D.zt);
     for (int j = 0; j < X.rounds; ++j) {
         const int v = j * kThreads + X.tid;
-        if (v < X.nv) {
-            float z[VEC];
-            X.load(v, z);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e)
-                if (z[e] >= zlo && z[e] <= zhi) X.hist_add(W, fkey(z[e]), 1, track);
-        }
-    }
-    X.passes++;
-    __syncthreads();
-}
-
-// Mass histogram of the ids of K whose keys lie in window W.
-template <class Ctx>
-__device__ void pass_mass_hist(Ctx& X, const typename Ctx::Window& W, const Surv& K, bool track) {
-    constexpr int VEC = Ctx::VEC;
-    X.hist_clear();
-    const float zlo = Ctx::lo_float(W.klo), zhi = key_to_float(W.khi);
-    for (int j = 0; j < X.rounds; ++j) {
-        const int v = j * kThreads + X.tid;
-        if (v < X.nv) {
+        if (v < X.nv && X.vmax[v] >= thr) {
             float z[VEC];
             X.load(v, z);
             const int g0 = X.a0 + v * VEC;
 #pragma unroll
             for (int e = 0; e < VEC; ++e)
-                if (z[e] >= zlo && z[e] <= zhi && (K.ge_form() || K.test(z[e], g0 + e)))
-                    X.hist_add(W, fkey(z[e]), X.fix(X.weight(z[e])), track);
+                if (z[e] >= zlo && z[e] <= zhi && D.test(z[e], g0 + e))
+                    X.lhist_add(W, fkey(z[e]), MASS ? X.fix(X.weight(z[e])) : 1u);
         }
     }
     X.passes++;
     __syncthreads();
 }
 
-// Per-(round, warp) fixed-point masses of the survivors of D into Wsum; when
-// W is given, also the mass histogram of the survivors in that key window.
-template <class Ctx, bool TIE, bool WITH_HIST>
-__device__ void pass_mass(Ctx& X, const Surv& D, const typename Ctx::Window& W) {
+// Give every CTA the ids of D whose keys lie in [lo, hi] as candidates:
+// (key, id) for counts, (key, mass) for masses.
+template <class Ctx, bool MASS>
+__device__ void pass_collect(Ctx& X, uint32_t lo, uint32_t hi, const Surv& D) {
     constexpr int VEC = Ctx::VEC;
-    if (WITH_HIST) X.hist_clear();
+    if (X.cand_zeroed >= X.epoch) X.xsync();
+    const float zlo = Ctx::lo_float(lo), zhi = key_to_float(hi);
+    const float thr = fmaxf(zlo, D.zt);
+    for (int j = 0; j < X.rounds; ++j) {
+        const int v = j * kThreads + X.tid;
+        if (v < X.nv && X.vmax[v] >= thr) {
+            float z[VEC];
+            X.load(v, z);
+            const int g0 = X.a0 + v * VEC;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                if (z[e] >= zlo && z[e] <= zhi && D.test(z[e], g0 + e)) {
+                    const uint32_t k = fkey(z[e]);
+                    if (k >= lo && k <= hi)
+                        X.push_cand(k, MASS ? X.fix(X.weight(z[e])) : static_cast<uint64_t>(g0 + e));
+                }
+            }
+        }
+    }
+    X.passes++;
+}
+
+// Per-(round, warp) fixed-point masses of the survivors of D into Wsum; with
+// HISTO also the local mass histogram of the survivors whose keys lie in W.
+template <class Ctx, bool HISTO>
+__device__ void pass_mass(Ctx& X, int mode, const Surv& D, const Window& W) {
+    constexpr int VEC = Ctx::VEC;
+    if (HISTO) X.lhist_clear();
     const float zlo = Ctx::lo_float(W.klo), zhi = key_to_float(W.khi);
     for (int j = 0; j < X.rounds; ++j) {
         const int v = j * kThreads + X.tid;
         uint64_t q = 0;
-        if (v < X.nv) {
+        if (v < X.nv && (mode == kAll || X.vmax[v] >= D.zt)) {
             float z[VEC];
             X.load(v, z);
             const int g0 = X.a0 + v * VEC;
-            q = X.template vec_mass<TIE>(z, g0, D);
-            if (WITH_HIST) {
+            q = X.vec_mass(mode, z, g0, D);
+            if (HISTO && X.vmax[v] >= zlo) {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    if (z[e] >= zlo && z[e] <= zhi && (!TIE || D.test(z[e], g0 + e)))
-                        X.hist_add(W, fkey(z[e]), X.fix(X.weight(z[e])), false);
+                    if (z[e] >= zlo && z[e] <= zhi && Ctx::in_domain(mode, D, z[e], g0 + e))
+                        X.lhist_add(W, fkey(z[e]), X.fix(X.weight(z[e])));
             }
         }
         q = warp_sum_u64(q);
@@ -476,69 +480,24 @@ __device__ void pass_mass(Ctx& X, const Surv& D, const typename Ctx::Window& W) 
 }
 
 template <class Ctx>
-__device__ __forceinline__ void pass_mass_any(Ctx& X, const Surv& D) {
-    typename Ctx::Window W{0u, 0u, 0};
-    if (D.ge_form())
-        pass_mass<Ctx, false, false>(X, D, W);
-    else
-        pass_mass<Ctx, true, false>(X, D, W);
+__device__ __forceinline__ int mass_mode(const Ctx& X, const Surv& D) {
+    if (!D.ge_form()) return kTie;
+    return (D.zt == -INFINITY && !X.row_nan) ? kAll : kGe;
 }
 
-// top-k survivor set: the first k ids by (z desc, id asc).  Exact.
+// The need-th id (1-based, id order) whose logit equals zt: the id bound of
+// a top-k set whose ties at zt are too many to gather.
 template <class Ctx>
-__device__ Surv select_topk(Ctx& X, int k, uint32_t Km, uint32_t& err) {
+__device__ int tie_walk(Ctx& X, float zt, uint64_t need) {
     constexpr int VEC = Ctx::VEC;
-    using Window = typename Ctx::Window;
-    uint64_t tgt = static_cast<uint64_t>(k);
-    // first window: 2^23 keys (one binade) below the max, widened 16x while it
-    // holds fewer than k ids
-    uint32_t width = 1u << 23;
-    Window W = Ctx::make_window(Km > width - 1 ? Km - (width - 1) : 0u, Km);
-    int level = 0;
-    float zt = -INFINITY;
-    bool tie = false;
-    while (true) {
-        pass_count_hist(X, W, level > 0);
-        const typename Ctx::Sel r = X.hist_exchange(tgt);
-        if (r.bin < 0) {
-            if (level == 0 && W.klo > 0) {
-                width = (width >= (1u << 27)) ? 0u : (width << 4);
-                const uint32_t lo = (width == 0u || Km < width - 1) ? 0u : Km - (width - 1);
-                W = Ctx::make_window(lo, Km);
-                continue;
-            }
-            return Surv{-INFINITY, INT_MAX};  // fewer than k non-NaN ids: keep all
-        }
-        if (level > 0 && r.mmin == r.mmax) {
-            // the window (the previous crossing bin) holds one key
-            zt = key_to_float(r.mmin);
-            if (tgt == r.total) return Surv{zt, INT_MAX};
-            tie = true;
-            break;
-        }
-        uint32_t lo, hi;
-        bin_range<Ctx>(W, r.bin, lo, hi);
-        if (r.before + r.inbin == tgt) return Surv{Ctx::lo_float(lo), INT_MAX};
-        tgt -= r.before;
-        if (W.sh == 0) {
-            zt = key_to_float(hi);
-            tie = true;
-            break;
-        }
-        W.klo = lo;
-        W.khi = hi;
-        W.sh = max(0, W.sh - kBinBits);
-        level++;
-    }
-    (void)tie;
-    // keep the first `tgt` ids (in id order) tied at zt: find the tgt-th one
     for (int j = 0; j < X.rounds; ++j) {
         const int v = j * kThreads + X.tid;
         uint64_t q = 0;
-        if (v < X.nv) {
+        if (v < X.nv && X.vmax[v] >= zt) {
             float z[VEC];
             X.load(v, z);
-            q = Ctx::vec_count_eq(z, zt);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) q += (z[e] == zt) ? 1u : 0u;
         }
         q = warp_sum_u64(q);
         if (X.lane == 0) X.Wsum[j * kWarps + X.warp] = q;
@@ -546,38 +505,127 @@ __device__ Surv select_topk(Ctx& X, int k, uint32_t Km, uint32_t& err) {
     X.passes++;
     X.publish_wsum_total(0);
     X.xsync();
-    const typename Ctx::Scan sc = X.xscan(0, tgt - 1);
+    const typename Ctx::Scan sc = X.xscan(0, need - 1);
     X.xnext();
     if (sc.first == X.rank) {
         const int pos = X.walk(
-            tgt - 1 - sc.before_me, [&](const float(&z)[VEC], int) { return Ctx::vec_count_eq(z, zt); },
-            [&](const float(&z)[VEC], int, uint64_t t) { return Ctx::vec_count_walk(z, zt, t); });
+            need - 1 - sc.before_me,
+            [&](const float(&z)[VEC], int) {
+                uint64_t c = 0;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) c += (z[e] == zt) ? 1u : 0u;
+                return c;
+            },
+            [&](const float(&z)[VEC], int, uint64_t t) {
+                uint64_t c = 0;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    c += (z[e] == zt) ? 1u : 0u;
+                    if (c > t) return e;
+                }
+                return -1;
+            });
         if (X.tid == 0) X.S.slot[X.par][0] = static_cast<uint64_t>(static_cast<uint32_t>(pos));
     }
     X.xsync();
     const int pos = (sc.first >= 0) ? static_cast<int>(static_cast<uint32_t>(X.xread(sc.first, 0))) : -1;
     X.xnext();
-    if (pos < 0) {
-        err |= kErrInternal;
-        return Surv{zt, INT_MAX};
-    }
-    return Surv{zt, pos + 1};
+    return pos;
 }
 
-// Continue a mass select from a window whose histogram is built: returns
-// true and the cutoff zp (z >= zp survives) when the window reaches `tgt`.
+// Exact top-k survivor set: the first k ids by (z desc, id asc).
 template <class Ctx>
-__device__ bool select_mass(Ctx& X, typename Ctx::Window W, const Surv& K, uint64_t tgt, float& zp) {
-    int level = 0;
+__device__ Surv select_topk(Ctx& X, int k, uint32_t Km, uint32_t& err) {
+    const Surv all{-INFINITY, INT_MAX};
+    uint64_t tgt = static_cast<uint64_t>(k);
+    // first window: 2^23 keys (one binade) below the max, widened 16x while it
+    // holds fewer than k ids
+    uint32_t width = 1u << 23;
+    Window W = Ctx::make_window(Km > width - 1 ? Km - (width - 1) : 0u, Km);
+    bool first = true;
     while (true) {
-        const typename Ctx::Sel r = X.hist_exchange(tgt);
-        if (r.bin < 0) return false;
-        if (level > 0 && r.mmin == r.mmax) {
-            zp = key_to_float(r.mmin);
-            return true;
+        pass_hist<Ctx, false>(X, W, all);
+        X.push_hist();
+        X.xsync();
+        const typename Ctx::Sel r = X.ghist_find(tgt);
+        X.ghist_clear();
+        if (r.bin < 0) {
+            if (first && W.klo > 0) {
+                width = (width >= (1u << 27)) ? 0u : (width << 4);
+                const uint32_t lo = (width == 0u || Km < width - 1) ? 0u : Km - (width - 1);
+                W = Ctx::make_window(lo, Km);
+                continue;
+            }
+            return all;  // fewer than k non-NaN ids: keep them all
         }
+        first = false;
         uint32_t lo, hi;
-        bin_range<Ctx>(W, r.bin, lo, hi);
+        bin_range(W, r.bin, lo, hi);
+        if (r.before + r.inbin == tgt) return Surv{Ctx::lo_float(lo), INT_MAX};
+        tgt -= r.before;  // ids still needed from this bin
+        if (r.inbin > static_cast<uint64_t>(kCand)) {
+            if (W.sh > 0) {  // too many ids in the bin: bisect it further
+                W.klo = lo;
+                W.khi = hi;
+                W.sh = max(0, W.sh - kBinBits);
+                continue;
+            }
+            // one key with too many ties to gather: walk them in id order
+            const float zt = key_to_float(hi);
+            const int pos = tie_walk(X, zt, tgt);
+            if (pos < 0) {
+                err |= kErrInternal;
+                return Surv{zt, INT_MAX};
+            }
+            return Surv{zt, pos + 1};
+        }
+        // gather the bin's ids into every CTA and rank them by (key desc, id asc)
+        pass_collect<Ctx, false>(X, lo, hi, all);
+        X.xsync();
+        const int nc = static_cast<int>(min(X.S.ccount, static_cast<uint32_t>(kCand)));
+        if (X.tid == 0) X.S.bcast_i[2] = -1;
+        __syncthreads();
+        if (X.tid < nc) {
+            const uint32_t ki = X.S.ckey[X.tid];
+            const int ii = static_cast<int>(X.S.cval[X.tid]);
+            int rk = 0;
+            for (int q = 0; q < nc; ++q) {
+                const uint32_t kq = X.S.ckey[q];
+                const int iq = static_cast<int>(X.S.cval[q]);
+                rk += (kq > ki || (kq == ki && iq < ii)) ? 1 : 0;
+            }
+            if (rk == static_cast<int>(tgt) - 1) X.S.bcast_i[2] = X.tid;
+        }
+        __syncthreads();
+        const int wi = X.S.bcast_i[2];
+        Surv K = all;
+        if (wi < 0) {
+            err |= kErrInternal;
+        } else {
+            const uint32_t kw = X.S.ckey[wi];
+            const int iw = static_cast<int>(X.S.cval[wi]);
+            // more ids tied at kw beyond iw: the id bound matters
+            int later = 0;
+            for (int q = X.tid; q < nc; q += kThreads)
+                later |= (X.S.ckey[q] == kw && static_cast<int>(X.S.cval[q]) > iw) ? 1 : 0;
+            later = __syncthreads_or(later);
+            K = Surv{key_to_float(kw), later ? iw + 1 : INT_MAX};
+        }
+        X.cand_clear();
+        return K;
+    }
+}
+
+// Top-p cutoff from the mass histogram of window W (already pushed, barrier
+// passed): true and zp (z >= zp survives) when W holds the target mass.
+template <class Ctx>
+__device__ bool select_mass(Ctx& X, Window W, const Surv& K, uint64_t tgt, float& zp) {
+    while (true) {
+        const typename Ctx::Sel r = X.ghist_find(tgt);
+        X.ghist_clear();
+        if (r.bin < 0) return false;
+        uint32_t lo, hi;
+        bin_range(W, r.bin, lo, hi);
         if (W.sh == 0) {
             zp = key_to_float(hi);
             return true;
@@ -587,19 +635,45 @@ __device__ bool select_mass(Ctx& X, typename Ctx::Window W, const Surv& K, uint6
             return true;
         }
         tgt -= r.before;
+        // gather the bin's ids (key, mass) into every CTA and find the largest
+        // key whose mass at or above it reaches the target
+        pass_collect<Ctx, true>(X, lo, hi, K);
+        X.xsync();
+        const uint32_t got = X.S.ccount;
+        if (got <= static_cast<uint32_t>(kCand)) {
+            const int nc = static_cast<int>(got);
+            uint32_t best = 0;
+            if (X.tid < nc) {
+                const uint32_t ki = X.S.ckey[X.tid];
+                uint64_t mge = 0;
+                for (int q = 0; q < nc; ++q)
+                    if (X.S.ckey[q] >= ki) mge += X.S.cval[q];
+                if (mge >= tgt) best = ki;
+            }
+            best = __reduce_max_sync(0xFFFFFFFFu, best);
+            if (X.lane == 0) X.S.wred32[X.warp] = best;
+            __syncthreads();
+            uint32_t kb = 0;
+            for (int w = 0; w < kWarps; ++w) kb = max(kb, X.S.wred32[w]);
+            X.cand_clear();  // (its barrier also orders the wred32 reads)
+            zp = key_to_float(kb);
+            return true;
+        }
+        // too many ids: bisect the bin with another histogram pass
+        X.cand_clear();
         W.klo = lo;
         W.khi = hi;
         W.sh = max(0, W.sh - kBinBits);
-        level++;
-        pass_mass_hist(X, W, K, true);
+        pass_hist<Ctx, true>(X, W, K);
+        X.push_hist();
+        X.xsync();
     }
 }
 
 template <int DT, bool HIST>
-__global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a) {
     using Ctx = RowCtx<DT, HIST>;
     using E = Elem<DT>;
-    using Window = typename Ctx::Window;
     constexpr int VEC = E::kVec;
     extern __shared__ __align__(128) unsigned char dyn[];
     __shared__ SampleShared S;
@@ -618,10 +692,15 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
     X.nvf = X.n / VEC;
     X.rounds = (X.nv + kThreads - 1) / kThreads;
     X.data = dyn;
-    X.Wsum = reinterpret_cast<uint64_t*>(dyn + a.data_bytes);
+    X.vmax = reinterpret_cast<float*>(dyn + a.vmax_off);
+    X.Wsum = reinterpret_cast<uint64_t*>(dyn + a.wsum_off);
     X.par = 0;
     X.passes = 0;
+    X.epoch = 0;
+    X.ghist_zeroed = -1;
+    X.cand_zeroed = -1;
     X.has_patch = false;
+    X.row_nan = false;
     X.bm = X.wp = nullptr;
     X.patch = nullptr;
     X.m = 0.0f;
@@ -640,7 +719,11 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         for (int p = 0; p < kPieces; ++p) mbar_init(&S.bar[p], 1);
         fence_mbar_init();
         S.flags = 0;
+        S.ccount = 0;
     }
+    // the cluster histogram must be zero before any CTA pushes into it (the
+    // first cluster barrier orders this)
+    for (int b = tid; b < kBins; b += kThreads) S.ghist[b] = 0;
     __syncthreads();
     if (a.aligned && tid == 0) {
         for (int p = 0; p < kPieces; ++p) {
@@ -668,17 +751,17 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         if (!ok) rerr |= ARC_ERR_PARAM;
     }
     // ids not covered by bulk copies: the ragged tail, or the whole slice when
-    // rows are not 16-byte aligned.  The last vector is padded with NaN, which
-    // no predicate, maximum or weight ever selects.
+    // rows are not 16-byte aligned.  The last vector is padded with -inf (zero
+    // weight, never a maximum); its padded ids lie beyond V.
     {
         const int first = a.aligned ? X.nvf * VEC : 0;
         for (int i = first + tid; i < X.nv * VEC; i += kThreads) {
             if (i < n)
                 E::store_smem_raw(data, i, rowp, a0 + i);
             else if (DT == ARC_BF16)
-                reinterpret_cast<unsigned short*>(data)[i] = 0x7FC0;
+                reinterpret_cast<unsigned short*>(data)[i] = 0xFF80;
             else
-                reinterpret_cast<uint32_t*>(data)[i] = 0x7FC00000u;
+                reinterpret_cast<uint32_t*>(data)[i] = 0xFF800000u;
         }
     }
     // -------------------------------------------------------------- history patches
@@ -690,7 +773,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         if (hn > 0 && rerr == 0) {
             const int nwords = (X.nv * VEC + 31) / 32;
             const int nwords_max = (a.rounds_max * kThreads * VEC + 31) / 32;
-            uint32_t* bmw = reinterpret_cast<uint32_t*>(dyn + a.data_bytes + a.rounds_max * kWarps * 8);
+            uint32_t* bmw = reinterpret_cast<uint32_t*>(dyn + a.hist_off_b);
             uint32_t* wpw = bmw + nwords_max;
             uint32_t* cnt = wpw + nwords_max;
             float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
@@ -759,8 +842,10 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
     __syncthreads();
 
     // -------------------------------------------------------------- pass 1: max / argmax
+    // Per vector a NaN-propagating max (packed bf16x2 for bf16); vectors with a
+    // NaN take the element path.  The NaN-free vector max is cached in vmax[].
     float bv = -INFINITY;
-    int bi = -1;
+    int bvi = -1;
     bool nanf = false, timeout = false;
     for (int j = 0; j < X.rounds; ++j) {
         if (a.aligned && (j % rpp) == 0) {
@@ -769,17 +854,39 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         }
         const int v = j * kThreads + tid;
         if (v < X.nv) {
-            float z[VEC];
-            X.load(v, z);
+            float vm;
+            if (X.vec_patched(v)) {
+                float z[VEC];
+                X.load(v, z);
+                vm = z[0];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                if (v * VEC + e < n) nanf |= (z[e] != z[e]);
-                if (z[e] > bv) {
-                    bv = z[e];
-                    bi = a0 + v * VEC + e;
-                }
+                for (int e = 1; e < VEC; ++e) vm = fmax_nan(vm, z[e]);
+            } else {
+                vm = E::vmax_nan(reinterpret_cast<const uint4*>(data)[v]);
+            }
+            if (vm != vm) {
+                nanf = true;
+                float z[VEC];
+                X.load(v, z);
+                vm = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    if (z[e] > vm) vm = z[e];
+            }
+            X.vmax[v] = vm;
+            if (vm > bv) {
+                bv = vm;
+                bvi = v;
             }
         }
+    }
+    int bi = -1;
+    if (bvi >= 0) {
+        float z[VEC];
+        X.load(bvi, z);
+#pragma unroll
+        for (int e = VEC - 1; e >= 0; --e)
+            if (z[e] == bv) bi = a0 + bvi * VEC + e;
     }
     X.passes = 1;
     warp_argmax(bv, bi);
@@ -818,6 +925,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         dflags = __reduce_or_sync(0xFFFFFFFFu, f);
     }
     X.xnext();
+    X.row_nan = (dflags & ARC_ERR_NAN) != 0;
     if ((a.flags & ARC_OPT_STEP_AUTOINC) && X.rank == 0 && tid == 0) a.params[row].step = P.step + 1;
 
     // -------------------------------------------------------------- mode
@@ -847,45 +955,56 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
     uint64_t mass_k = 0, mass_r = 0, target = 0, rbits = 0;
     bool walk_fail = false;
 
-    if (token == -2) {
+    if (token != -2) {
+        cluster_arrive();  // this CTA reads no other CTA's shared memory after this
+    } else {
         // ---------------------------------------------------------- sampling rows
         X.m = m;
         X.infm = (m == INFINITY);
         X.c = __fdiv_rn(1.4426950408889634f, T);  // w = 2^((z - m) * log2(e) / T)
         X.scale = __uint_as_float(static_cast<uint32_t>(127 + a.F) << 23);
         const uint32_t Km = fkey(m);
+        // per-row fp64 thresholds, one lane per warp:
+        //   zm: min-p, w >= min_p  <=>  z >= m + T ln(min_p), rounded up to fp32
+        //   zb: top-p window floor; ids below it carry < half of (1 - top_p) of the mass
+        float zm = -INFINITY, zb = -INFINITY;
+        if (lane == 0) {
+            if (minp_on)
+                zm = __double2float_ru(static_cast<double>(m) +
+                                       static_cast<double>(T) * log(static_cast<double>(P.min_p)));
+            if (topp_on)
+                zb = __double2float_rd(static_cast<double>(m) +
+                                       static_cast<double>(T) * log((1.0 - static_cast<double>(P.top_p)) /
+                                                                    (2.0 * static_cast<double>(a.V))));
+        }
+        zm = __shfl_sync(0xFFFFFFFFu, zm, 0);
+        zb = __shfl_sync(0xFFFFFFFFu, zb, 0);
+
         Surv K{-INFINITY, INT_MAX};  // every non-NaN id
         if (topk_on) {
             K = select_topk(X, k, Km, err);
             kap_k = (K.zt == -INFINITY && K.ge_form()) ? 0u : fkey(K.zt);
             iot_k = K.ge_form() ? a.V : K.iota;
         }
-        // min-p: w >= min_p  <=>  z >= m + T ln(min_p), rounded up to fp32
-        float zm = -INFINITY;
-        if (minp_on)
-            zm = __double2float_ru(static_cast<double>(m) +
-                                   static_cast<double>(T) * log(static_cast<double>(P.min_p)));
         Surv R = K;
         bool wsum_is_R = false;
         if (topp_on) {
-            // masses over K, plus a mass histogram over the keys whose weight is
-            // at least (1 - top_p) / (2V): the ids below carry less than half of
-            // the (1 - top_p) share of K's mass, so the cutoff lies inside
+            // masses over K, plus the mass histogram of a key window that holds
+            // the top-p cutoff
             const float zfloor = fmaxf(zm, K.zt);
-            const double zb = static_cast<double>(m) +
-                              static_cast<double>(T) *
-                                  log((1.0 - static_cast<double>(P.top_p)) / (2.0 * static_cast<double>(a.V)));
-            float zlo = fmaxf(__double2float_rd(zb), zfloor);
+            float zlo = fmaxf(zb, zfloor);
             Window W = Ctx::make_window(fkey(zlo), Km);
-            if (K.ge_form())
-                pass_mass<Ctx, false, true>(X, K, W);
-            else
-                pass_mass<Ctx, true, true>(X, K, W);
+            const int mk = mass_mode(X, K);
+            pass_mass<Ctx, true>(X, mk, K, W);
             X.publish_wsum_total(0);
+            X.push_hist();
             X.xsync();
             mass_k = X.xscan(0, ~0ull).total;
             X.xnext();
-            uint64_t tgt = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(mass_k)));
+            uint64_t tgt = 1;
+            if (lane == 0)
+                tgt = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(mass_k)));
+            tgt = shfl_u64(tgt, 0);
             if (tgt == 0) tgt = 1;
             float zp = -INFINITY;
             bool found = select_mass(X, W, K, tgt, zp);
@@ -893,7 +1012,9 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
                 // rounding left the first window just short: retry down to the hard bound
                 zlo = zfloor;
                 W = Ctx::make_window(fkey(zlo), Km);
-                pass_mass_hist(X, W, K, false);
+                pass_hist<Ctx, true>(X, W, K);
+                X.push_hist();
+                X.xsync();
                 found = select_mass(X, W, K, tgt, zp);
             }
             // short of the target even then: min-p (or top-k) bounds the window,
@@ -910,7 +1031,8 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         iot_r = R.ge_form() ? a.V : R.iota;
 
         // ---------------------------------------------------------- inverse-CDF draw
-        if (!wsum_is_R) pass_mass_any(X, R);
+        const int mr = mass_mode(X, R);
+        if (!wsum_is_R) pass_mass<Ctx, false>(X, mr, R, Window{0u, 0u, 0});
         X.publish_wsum_total(0);
         rbits = splitmix64(P.seed ^ (static_cast<uint64_t>(row) << 32) ^ P.step) >> 11;
         X.xsync();
@@ -918,24 +1040,15 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         target = scale_by_u(rbits, mass_r);
         const typename Ctx::Scan sc = X.xscan(0, target);
         X.xnext();
+        cluster_arrive();  // this CTA reads no other CTA's shared memory after this
         if (sc.first < 0) {
             err |= kErrInternal;
             token = am;
         } else if (sc.first == X.rank) {
             const uint64_t t = target - sc.before_me;
-            int tok;
-            if (R.ge_form())
-                tok = X.walk(
-                    t, [&](const float(&z)[VEC], int g0) { return X.template vec_mass<false>(z, g0, R); },
-                    [&](const float(&z)[VEC], int g0, uint64_t tt) {
-                        return X.template vec_mass_walk<false>(z, g0, R, tt);
-                    });
-            else
-                tok = X.walk(
-                    t, [&](const float(&z)[VEC], int g0) { return X.template vec_mass<true>(z, g0, R); },
-                    [&](const float(&z)[VEC], int g0, uint64_t tt) {
-                        return X.template vec_mass_walk<true>(z, g0, R, tt);
-                    });
+            int tok = X.walk(
+                t, [&](const float(&z)[VEC], int g0) { return X.vec_mass(mr, z, g0, R); },
+                [&](const float(&z)[VEC], int g0, uint64_t tt) { return X.vec_mass_walk(mr, z, g0, R, tt); });
             if (tok < 0) {
                 tok = am;
                 walk_fail = true;
@@ -970,7 +1083,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         }
     }
     // no CTA may leave while another can still read its shared memory
-    X.cl.sync();
+    cluster_wait();
     if (walk_fail && tid == 0) {
         if (a.err_word) atomicOr(a.err_word, kErrInternal);
         if (a.debug) atomicOr(&a.debug[row].err, kErrInternal);
