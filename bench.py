@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "sampled rows/s and achieved HBM GB/s (% of GB300 roofline) at B=256, V=129,280"
 NBUF = 6  # input copies cycled per step: 6 x 66 MB > L2
 PROFILE = os.path.join(ROOT, "profiles", "sample_kernel_mixed_quarters_B256.md")
-KERNEL_SOURCES = ["arc_sample.cu", "sample_kernel.cuh", "arc_device.cuh"]
+KERNEL_SOURCES = ["arc_sample.cu", "stream_kernel.cuh", "row_select.cuh", "arc_device.cuh"]
 
 
 def kernel_hash() -> str:
@@ -207,11 +207,12 @@ def bench_gpu(args) -> None:
     out = torch.zeros(B, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     geom = sampler.plan(B, V, w.dtype)
+    wspace = sampler.workspace_tensor(B, V, w.dtype)
     stream = torch.cuda.Stream()
 
     # first call on the device sets kernel attributes (outside any capture)
     with torch.cuda.stream(stream):
-        sampler.sample_batch(bufs[0], params, out, err_word=err, stream=stream)
+        sampler.sample_batch(bufs[0], params, out, err_word=err, workspace=wspace, stream=stream)
     stream.synchronize()
     assert int(err.item()) == 0, hex(int(err.item()))
 
@@ -222,7 +223,8 @@ def bench_gpu(args) -> None:
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
                 for i in range(n):
-                    sampler.sample_batch(bufs[i % NBUF], params, out, err_word=err, stream=stream)
+                    sampler.sample_batch(bufs[i % NBUF], params, out, err_word=err, workspace=wspace,
+                                         stream=stream)
         return g
 
     g_main = capture(chunk)
@@ -278,7 +280,7 @@ def bench_gpu(args) -> None:
         with torch.cuda.stream(stream):
             dev_logits.copy_(host_logits, non_blocking=True)
             dev_params.copy_(host_params, non_blocking=True)
-            sampler.sample_batch(dev_logits, dev_params, out, err_word=err, stream=stream)
+            sampler.sample_batch(dev_logits, dev_params, out, err_word=err, workspace=wspace, stream=stream)
             host_out.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -313,7 +315,7 @@ def bench_gpu(args) -> None:
                 "params": "row%4: greedy | T=1 defaults | top_k=50 T=0.7 | top_p=0.9 min_p=0.05 T=0.8",
                 "l2": f"inputs larger than L2: {NBUF} rotating copies of the batch "
                       f"({NBUF * B * V * es / 1e6:.0f} MB)",
-                "cluster_ctas": geom.cluster_ctas, "launch": "CUDA graph, one launch per step",
+                "ctas_per_row": geom.ctas_per_row, "launch": "CUDA graph, one launch per step",
                 "parallelism": f"rows sharded, {ws} independent rank(s)",
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -167,6 +167,19 @@ struct Elem<ARC_F32> {
     __device__ __forceinline__ static void store_smem_raw(void* base, int i, const void* row, int64_t gi) {
         reinterpret_cast<uint32_t*>(base)[i] = __ldg(reinterpret_cast<const uint32_t*>(row) + gi);
     }
+    // vector v of a slice in global memory holding n elements; elements past
+    // n read as -inf; 16-byte load when the slice start is 16-byte aligned
+    __device__ __forceinline__ static uint4 global_vec(const void* base, int v, int n, bool aligned) {
+        if (aligned && (v + 1) * 4 <= n) return ld_nc_v4(static_cast<const char*>(base) + static_cast<size_t>(v) * 16);
+        const uint32_t* p = static_cast<const uint32_t*>(base);
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = v * 4 + e;
+            w[e] = (i < n) ? __ldg(p + i) : 0xFF800000u;
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
 };
 
 template <>
@@ -203,6 +216,21 @@ struct Elem<ARC_BF16> {
     __device__ __forceinline__ static void store_smem_raw(void* base, int i, const void* row, int64_t gi) {
         reinterpret_cast<unsigned short*>(base)[i] =
             __ldg(reinterpret_cast<const unsigned short*>(row) + gi);
+    }
+    // vector v of a slice in global memory holding n elements; elements past
+    // n read as -inf; 16-byte load when the slice start is 16-byte aligned
+    __device__ __forceinline__ static uint4 global_vec(const void* base, int v, int n, bool aligned) {
+        if (aligned && (v + 1) * 8 <= n) return ld_nc_v4(static_cast<const char*>(base) + static_cast<size_t>(v) * 16);
+        const unsigned short* p = static_cast<const unsigned short*>(base);
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int i = v * 8 + 2 * h;
+            const uint32_t lo = (i < n) ? __ldg(p + i) : 0xFF80u;
+            const uint32_t hi = (i + 1 < n) ? __ldg(p + i + 1) : 0xFF80u;
+            w[h] = lo | (hi << 16);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
 

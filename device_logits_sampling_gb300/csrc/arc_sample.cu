@@ -1,5 +1,6 @@
 // C ABI of the GB300 sampler (include/arc_sample.h): argument checks, launch
 // geometry, per-device kernel attributes and one launch per call.
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cstdint>
@@ -7,29 +8,30 @@
 
 #include "arc_sample.h"
 #include "argmax_kernel.cuh"
-#include "sample_kernel.cuh"
+#include "stream_kernel.cuh"
 
 namespace {
 
 using namespace arc;
 
 constexpr int kMaxDevices = 64;
-constexpr int kSliceBytes = 32 * 1024;        // target bytes of a row per CTA
 constexpr int kSmemPerBlock = 232448;         // 227 KB opt-in limit of sm_100-class GPUs
-constexpr int kDefaultHist = 1024;
+constexpr int kDefaultHist = 1024;  // history capacity when max_hist_len is 0
 constexpr int kAssumedSMs = 152;
 
 struct Plan {
-    int s = 1;
-    int L = 0;
-    int vmax_off = 0;
-    int wsum_off = 0;
-    int hist_off_b = 0;
-    int rounds_max = 0;
+    int s = 1;              // slices per row
+    int L = 0;              // logits per slice
     int hist_cap = 0;
-    int smem = 0;
-    int64_t grid = 0;
+    int scan_smem = 0;      // dynamic shared memory of the scan kernel
+    int cmax_off = 0;       // finish kernel layout
+    int fb_wsum_off = 0;
+    int fb_patch_off = 0;
+    int fb_rounds = 0;
+    int fin_smem = 0;
+    int64_t slices = 0;
     int F = 0;
+    size_t ws_bytes = 0;
 };
 
 int elem_bytes(int dtype) { return dtype == ARC_BF16 ? 2 : 4; }
@@ -50,7 +52,7 @@ int check_common(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t d
     if (logits == nullptr || out == nullptr) return ARC_E_NULL;
     if (dtype != ARC_F32 && dtype != ARC_BF16) return ARC_E_DTYPE;
     if (B <= 0 || V <= 0 || V > INT_MAX || ld < V) return ARC_E_SHAPE;
-    if (B > (int64_t{1} << 26)) return ARC_E_SHAPE;
+    if (B > (int64_t{1} << 24)) return ARC_E_SHAPE;
     if (reinterpret_cast<uintptr_t>(logits) % static_cast<uintptr_t>(elem_bytes(dtype)) != 0) return ARC_E_ALIGN;
     return ARC_OK;
 }
@@ -58,58 +60,64 @@ int check_common(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t d
 int check_options(const arc_sample_options* o) {
     if (o == nullptr) return ARC_OK;
     if (o->flags & ~ARC_OPT_STEP_AUTOINC) return ARC_E_OPTION;
-    const int c = o->cluster_ctas;
-    if (!(c == 0 || c == 1 || c == 2 || c == 4 || c == 8 || c == 16)) return ARC_E_OPTION;
+    if (o->ctas_per_row < 0 || o->ctas_per_row > kMaxRowCtas) return ARC_E_OPTION;
     if (o->max_hist_len < 0 || o->max_hist_len > (1 << 20)) return ARC_E_OPTION;
     if (o->reserved != 0) return ARC_E_OPTION;
     return ARC_OK;
 }
 
-// Geometry of the fused kernel.  The row is split over s CTAs (a cluster);
-// each CTA keeps its slice, plus per-chunk masses and history patches, in
-// shared memory.
+// Geometry: a row is cut into s slices of at most kVpt * kThreads 16-byte
+// vectors (one scan CTA each); small batches use more, smaller slices so that
+// every SM gets work.
 int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_options* o, int num_sms,
               Plan& p) {
     const int es = elem_bytes(dtype);
     const int vec = 16 / es;
-    int s;
-    if (o != nullptr && o->cluster_ctas != 0) {
-        s = o->cluster_ctas;
+    const int64_t slice_max = int64_t{kVpt} * kThreads * vec;
+    int64_t s;
+    if (o != nullptr && o->ctas_per_row != 0) {
+        s = o->ctas_per_row;
     } else {
-        const int s_min = min(kMaxCluster, pow2_at_least((V * es + kSliceBytes - 1) / kSliceBytes));
-        const int s_want = min(kMaxCluster, pow2_at_least((2 * int64_t{num_sms} + B - 1) / B));
-        int s_cap = 1;
-        while (s_cap < kMaxCluster && V / (2 * s_cap) >= 2048) s_cap <<= 1;
-        s = max(s_min, min(s_want, s_cap));
+        const int64_t s_min = (V + slice_max - 1) / slice_max;
+        const int64_t s_want = (8 * int64_t{num_sms} + B - 1) / B;
+        const int64_t s_cap = std::max<int64_t>(1, V / 1024);
+        s = std::max<int64_t>(s_min, std::min<int64_t>(s_want, s_cap));
+        s = std::min<int64_t>(s, kMaxRowCtas);
     }
+    if (s * slice_max < V || s > kMaxRowCtas) return ARC_E_UNSUPPORTED;
     const int64_t per = (V + s - 1) / s;
     const int64_t L = ((per + vec - 1) / vec) * vec;
-    const int64_t nv_max = L / vec;
-    const int64_t rounds_max = (nv_max + kThreads - 1) / kThreads;
-    // dynamic shared memory: slice | per-vector max | per-(round, warp) masses | history tables
-    const int64_t data_bytes = ((nv_max * 16 + 127) / 128) * 128;
-    const int64_t vmax_off = data_bytes;
-    const int64_t wsum_off = vmax_off + ((nv_max * 4 + 15) / 16) * 16;
-    const int64_t hist_off_b = wsum_off + rounds_max * kWarps * 8;
-    int64_t smem = hist_off_b;
-    int cap = 0;
+    s = (V + L - 1) / L;  // no empty slice
+    const int cap = has_hist ? ((o != nullptr && o->max_hist_len > 0) ? o->max_hist_len : kDefaultHist) : 0;
+    int64_t scan_smem = 0;
     if (has_hist) {
-        cap = (o != nullptr && o->max_hist_len > 0) ? o->max_hist_len : kDefaultHist;
-        const int64_t nwords_max = (rounds_max * kThreads * vec + 31) / 32;
-        smem += 2 * nwords_max * 4 + 2 * int64_t{cap} * 4;
+        const int64_t nwords = (int64_t{kVpt} * kThreads * vec + 31) / 32;
+        scan_smem = 2 * nwords * 4 + 2 * int64_t{cap} * 4;
     }
-    const int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(SampleShared)) - 1024;
-    if (smem > limit) return ARC_E_UNSUPPORTED;
-    p.s = s;
+    const int64_t cmax_bytes = ((s * kChunks * 4 + 127) / 128) * 128;
+    const int64_t nv_row = (V + vec - 1) / vec;
+    const int64_t fb_rounds = (nv_row + kThreads - 1) / kThreads;
+    const int64_t fb_wsum = ((fb_rounds * kWarps * 8 + 127) / 128) * 128;
+    int64_t fb_patch = 0;
+    if (has_hist) {
+        const int64_t nwords = (fb_rounds * kThreads * vec + 31) / 32;
+        fb_patch = 2 * nwords * 4 + 2 * int64_t{cap} * 4;
+    }
+    const int64_t fin_smem = cmax_bytes + fb_wsum + fb_patch;
+    const int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
+    if (fin_smem > limit || scan_smem > limit) return ARC_E_UNSUPPORTED;
+    p.s = static_cast<int>(s);
     p.L = static_cast<int>(L);
-    p.vmax_off = static_cast<int>(vmax_off);
-    p.wsum_off = static_cast<int>(wsum_off);
-    p.hist_off_b = static_cast<int>(hist_off_b);
-    p.rounds_max = static_cast<int>(rounds_max);
     p.hist_cap = cap;
-    p.smem = static_cast<int>(smem);
-    p.grid = B * s;
+    p.scan_smem = static_cast<int>(scan_smem);
+    p.cmax_off = 0;
+    p.fb_wsum_off = static_cast<int>(cmax_bytes);
+    p.fb_patch_off = static_cast<int>(cmax_bytes + fb_wsum);
+    p.fb_rounds = static_cast<int>(fb_rounds);
+    p.fin_smem = static_cast<int>(fin_smem);
+    p.slices = B * s;
     p.F = 62 - ceil_log2(V);
+    p.ws_bytes = static_cast<size_t>(B * s) * kSummaryBytes;
     return ARC_OK;
 }
 
@@ -131,12 +139,30 @@ cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done) {
     const uint64_t bit = uint64_t{1} << (dev & 63);
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemPerBlock - static_cast<int>(sizeof(SampleShared)) - 1024);
+                                         kSmemPerBlock - static_cast<int>(sizeof(KernelShared)) - 1024);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     done.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
+}
+
+// Resident CTAs per SM for this kernel and shared memory (cached per device).
+template <class K>
+int blocks_per_sm(K kernel, int dev, int smem) {
+    static std::atomic<int> cache[kMaxDevices][8];
+    static std::atomic<int> cache_smem[kMaxDevices][8];
+    const int slot = (reinterpret_cast<uintptr_t>(reinterpret_cast<const void*>(kernel)) >> 4) & 7;
+    if (dev >= 0 && dev < kMaxDevices && cache_smem[dev][slot].load() == smem + 1) return cache[dev][slot].load();
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, static_cast<size_t>(smem)) != cudaSuccess ||
+        nb <= 0)
+        nb = 1;
+    if (dev >= 0 && dev < kMaxDevices) {
+        cache[dev][slot].store(nb);
+        cache_smem[dev][slot].store(smem + 1);
+    }
+    return nb;
 }
 
 template <class K, class A>
@@ -157,7 +183,8 @@ cudaError_t launch_cluster(K kernel, int64_t grid, int s, int smem, cudaStream_t
     return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
-std::atomic<uint64_t> g_prep_sample[2][2];
+std::atomic<uint64_t> g_prep_scan[2][2];
+std::atomic<uint64_t> g_prep_fin[2][2];
 std::atomic<uint64_t> g_prep_argmax[2];
 
 }  // namespace
@@ -173,9 +200,10 @@ const char* arc_sample_strerror(int code) {
         case ARC_E_SHAPE: return "bad shape: need B > 0, 0 < V <= 2^31-1 and ld >= V";
         case ARC_E_DTYPE: return "dtype must be ARC_F32 or ARC_BF16";
         case ARC_E_ALIGN: return "logits pointer is not aligned to its element size";
-        case ARC_E_UNSUPPORTED: return "a row slice does not fit in shared memory";
+        case ARC_E_UNSUPPORTED: return "the vocabulary needs more CTAs per row than allowed";
         case ARC_E_OPTION: return "bad field in arc_sample_options";
         case ARC_E_CUDA: return "CUDA error while configuring or launching the kernel";
+        case ARC_E_WORKSPACE: return "workspace is NULL or smaller than arc_sample_workspace_bytes()";
         default: return "unknown error code";
     }
 }
@@ -184,25 +212,46 @@ int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history, co
                     arc_sample_geometry* geom) {
     if (geom == nullptr) return ARC_E_NULL;
     if (dtype != ARC_F32 && dtype != ARC_BF16) return ARC_E_DTYPE;
-    if (B <= 0 || V <= 0 || V > INT_MAX || B > (int64_t{1} << 26)) return ARC_E_SHAPE;
+    if (B <= 0 || V <= 0 || V > INT_MAX || B > (int64_t{1} << 24)) return ARC_E_SHAPE;
     int rc = check_options(opts);
     if (rc != ARC_OK) return rc;
     Plan p;
     rc = make_plan(B, V, dtype, has_history != 0, opts, kAssumedSMs, p);
     if (rc != ARC_OK) return rc;
-    geom->cluster_ctas = p.s;
+    geom->ctas_per_row = p.s;
     geom->threads = kThreads;
     geom->slice_elems = p.L;
-    geom->smem_bytes = p.smem;
-    geom->grid_ctas = p.grid;
+    geom->smem_bytes = p.fin_smem;
+    geom->grid_ctas = p.slices;
     geom->frac_bits = p.F;
     geom->reserved = 0;
+    geom->workspace_bytes = static_cast<int64_t>(p.ws_bytes);
     return ARC_OK;
+}
+
+size_t arc_sample_workspace_bytes(int64_t B, int64_t V, int32_t dtype, int32_t has_history,
+                                  const arc_sample_options* opts) {
+    if (dtype != ARC_F32 && dtype != ARC_BF16) return 0;
+    if (B <= 0 || V <= 0 || V > INT_MAX || B > (int64_t{1} << 24)) return 0;
+    if (check_options(opts) != ARC_OK) return 0;
+    Plan p;
+    if (make_plan(B, V, dtype, has_history != 0, opts, kAssumedSMs, p) != ARC_OK) return 0;
+    // the plan depends on the SM count only through ctas_per_row; size for the
+    // largest automatic choice so one workspace fits every device
+    Plan q;
+    arc_sample_options big{};
+    if (opts != nullptr) big = *opts;
+    if (big.ctas_per_row == 0) {
+        big.ctas_per_row = kMaxRowCtas;
+        if (make_plan(B, V, dtype, has_history != 0, &big, kAssumedSMs, q) == ARC_OK)
+            return std::max(p.ws_bytes, q.ws_bytes);
+    }
+    return p.ws_bytes;
 }
 
 int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype, arc_row_params* params,
                      const int32_t* hist_offsets, const int32_t* hist_ids, int32_t* out, uint32_t* err_word,
-                     const arc_sample_options* opts, void* stream) {
+                     void* workspace, size_t workspace_bytes, const arc_sample_options* opts, void* stream) {
     int rc = check_common(logits, B, V, ld, dtype, out);
     if (rc != ARC_OK) return rc;
     if (params == nullptr) return ARC_E_NULL;
@@ -210,6 +259,8 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     if (reinterpret_cast<uintptr_t>(params) % 8 != 0) return ARC_E_ALIGN;
     rc = check_options(opts);
     if (rc != ARC_OK) return rc;
+    if (workspace == nullptr) return ARC_E_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return ARC_E_ALIGN;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ARC_E_CUDA;
@@ -217,48 +268,62 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     Plan p;
     rc = make_plan(B, V, dtype, has_hist, opts, num_sms_of(dev), p);
     if (rc != ARC_OK) return rc;
+    if (workspace_bytes < p.ws_bytes) return ARC_E_WORKSPACE;
 
-    SampleArgs a;
-    a.logits = logits;
-    a.ld = ld;
-    a.B = static_cast<int>(B);
-    a.V = static_cast<int>(V);
-    a.params = params;
-    a.hist_off = hist_offsets;
-    a.hist_ids = hist_ids;
-    a.out = out;
-    a.err_word = err_word;
-    a.debug = opts ? opts->debug : nullptr;
-    a.L = p.L;
-    a.vmax_off = p.vmax_off;
-    a.wsum_off = p.wsum_off;
-    a.hist_off_b = p.hist_off_b;
-    a.rounds_max = p.rounds_max;
-    a.hist_cap = p.hist_cap;
-    a.F = p.F;
-    a.flags = opts ? opts->flags : 0u;
     const int es = elem_bytes(dtype);
-    a.aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((ld * es) % 16 == 0);
+    const int aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((ld * es) % 16 == 0);
+    ScanArgs sa;
+    sa.logits = logits;
+    sa.ld = ld;
+    sa.B = static_cast<int>(B);
+    sa.V = static_cast<int>(V);
+    sa.s = p.s;
+    sa.L = p.L;
+    sa.params = params;
+    sa.hist_off = hist_offsets;
+    sa.hist_ids = hist_ids;
+    sa.summaries = static_cast<unsigned char*>(workspace);
+    sa.hist_cap = p.hist_cap;
+    sa.aligned = aligned;
+    sa.patch_off = 0;
+    FinishArgs fa;
+    fa.logits = logits;
+    fa.ld = ld;
+    fa.B = static_cast<int>(B);
+    fa.V = static_cast<int>(V);
+    fa.s = p.s;
+    fa.L = p.L;
+    fa.params = params;
+    fa.hist_off = hist_offsets;
+    fa.hist_ids = hist_ids;
+    fa.out = out;
+    fa.err_word = err_word;
+    fa.debug = opts ? opts->debug : nullptr;
+    fa.summaries = static_cast<const unsigned char*>(workspace);
+    fa.hist_cap = p.hist_cap;
+    fa.F = p.F;
+    fa.flags = opts ? opts->flags : 0u;
+    fa.aligned = aligned;
+    fa.cmax_off = p.cmax_off;
+    fa.fb_wsum_off = p.fb_wsum_off;
+    fa.fb_patch_off = p.fb_patch_off;
+    fa.fb_rounds = p.fb_rounds;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto go = [&](auto scan, auto fin, std::atomic<uint64_t>& done_s, std::atomic<uint64_t>& done_f) {
+        cudaError_t err = prepare(scan, dev, done_s);
+        if (err == cudaSuccess) err = prepare(fin, dev, done_f);
+        if (err == cudaSuccess) err = launch_cluster(scan, p.slices, 1, p.scan_smem, st, sa);
+        if (err == cudaSuccess) err = launch_cluster(fin, B, 1, p.fin_smem, st, fa);
+        return err;
+    };
     cudaError_t e;
-    if (dtype == ARC_BF16) {
-        if (has_hist) {
-            e = prepare(sample_kernel<ARC_BF16, true>, dev, g_prep_sample[1][1]);
-            if (e == cudaSuccess) e = launch_cluster(sample_kernel<ARC_BF16, true>, p.grid, p.s, p.smem, st, a);
-        } else {
-            e = prepare(sample_kernel<ARC_BF16, false>, dev, g_prep_sample[1][0]);
-            if (e == cudaSuccess) e = launch_cluster(sample_kernel<ARC_BF16, false>, p.grid, p.s, p.smem, st, a);
-        }
-    } else {
-        if (has_hist) {
-            e = prepare(sample_kernel<ARC_F32, true>, dev, g_prep_sample[0][1]);
-            if (e == cudaSuccess) e = launch_cluster(sample_kernel<ARC_F32, true>, p.grid, p.s, p.smem, st, a);
-        } else {
-            e = prepare(sample_kernel<ARC_F32, false>, dev, g_prep_sample[0][0]);
-            if (e == cudaSuccess) e = launch_cluster(sample_kernel<ARC_F32, false>, p.grid, p.s, p.smem, st, a);
-        }
-    }
+    if (dtype == ARC_BF16)
+        e = has_hist ? go(scan_kernel<ARC_BF16, true>, finish_kernel<ARC_BF16, true>, g_prep_scan[1][1], g_prep_fin[1][1])
+                     : go(scan_kernel<ARC_BF16, false>, finish_kernel<ARC_BF16, false>, g_prep_scan[1][0], g_prep_fin[1][0]);
+    else
+        e = has_hist ? go(scan_kernel<ARC_F32, true>, finish_kernel<ARC_F32, true>, g_prep_scan[0][1], g_prep_fin[0][1])
+                     : go(scan_kernel<ARC_F32, false>, finish_kernel<ARC_F32, false>, g_prep_scan[0][0], g_prep_fin[0][0]);
     return e == cudaSuccess ? ARC_OK : ARC_E_CUDA;
 }
 

@@ -97,8 +97,12 @@ struct RowCtx {
     cg::cluster_group cl;
     int s, rank, row, tid, lane, warp;
     int a0, a1, n, nv, nvf, rounds;
-    const unsigned char* data;
-    float* vmax;
+    const unsigned char* data;  // the slice: shared memory, or global memory when src_global
+    bool src_global;
+    bool src_aligned;
+    float* vmax;                // max per vector (vps == 0) or per 32-vector chunk, or nullptr
+    int vps;                    // vectors per slice of the chunk table (0: vmax is per vector)
+    int cps;                    // chunk slots per slice
     uint64_t* Wsum;
     // history patches
     const uint32_t* bm;
@@ -124,8 +128,19 @@ struct RowCtx {
         return ((bm[l0 >> 5] >> (l0 & 31)) & ((1u << VEC) - 1u)) != 0;
     }
 
+    __device__ __forceinline__ uint4 raw_vec(int v) const {
+        return src_global ? E::global_vec(data, v, n, src_aligned) : reinterpret_cast<const uint4*>(data)[v];
+    }
+    // false only when vector v cannot hold an id >= thr
+    __device__ __forceinline__ bool may_hold(int v, float thr) const {
+        if (vmax == nullptr) return true;
+        if (vps == 0) return vmax[v] >= thr;
+        const int c = v / vps;
+        return vmax[c * cps + ((v - c * vps) >> 5)] >= thr;
+    }
+
     __device__ __forceinline__ void load(int v, float (&z)[VEC]) const {
-        const uint4 raw = reinterpret_cast<const uint4*>(data)[v];
+        const uint4 raw = raw_vec(v);
         E::unpack(raw, z);
         if (HIST && has_patch) {
             const int l0 = v * VEC;
@@ -410,7 +425,7 @@ __device__ void pass_hist(Ctx& X, const Window& W, const Surv& D) {
     const float thr = fmaxf(zlo, D.zt);
     for (int j = 0; j < X.rounds; ++j) {
         const int v = j * kThreads + X.tid;
-        if (v < X.nv && X.vmax[v] >= thr) {
+        if (v < X.nv && X.may_hold(v, thr)) {
             float z[VEC];
             X.load(v, z);
             const int g0 = X.a0 + v * VEC;
@@ -434,7 +449,7 @@ __device__ void pass_collect(Ctx& X, uint32_t lo, uint32_t hi, const Surv& D) {
     const float thr = fmaxf(zlo, D.zt);
     for (int j = 0; j < X.rounds; ++j) {
         const int v = j * kThreads + X.tid;
-        if (v < X.nv && X.vmax[v] >= thr) {
+        if (v < X.nv && X.may_hold(v, thr)) {
             float z[VEC];
             X.load(v, z);
             const int g0 = X.a0 + v * VEC;
@@ -461,12 +476,12 @@ __device__ void pass_mass(Ctx& X, int mode, const Surv& D, const Window& W) {
     for (int j = 0; j < X.rounds; ++j) {
         const int v = j * kThreads + X.tid;
         uint64_t q = 0;
-        if (v < X.nv && (mode == kAll || X.vmax[v] >= D.zt)) {
+        if (v < X.nv && (mode == kAll || X.may_hold(v, D.zt))) {
             float z[VEC];
             X.load(v, z);
             const int g0 = X.a0 + v * VEC;
             q = X.vec_mass(mode, z, g0, D);
-            if (HISTO && X.vmax[v] >= zlo) {
+            if (HISTO && X.may_hold(v, zlo)) {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
                     if (z[e] >= zlo && z[e] <= zhi && Ctx::in_domain(mode, D, z[e], g0 + e))
@@ -493,7 +508,7 @@ __device__ int tie_walk(Ctx& X, float zt, uint64_t need) {
     for (int j = 0; j < X.rounds; ++j) {
         const int v = j * kThreads + X.tid;
         uint64_t q = 0;
-        if (v < X.nv && X.vmax[v] >= zt) {
+        if (v < X.nv && X.may_hold(v, zt)) {
             float z[VEC];
             X.load(v, z);
 #pragma unroll
@@ -667,431 +682,6 @@ __device__ bool select_mass(Ctx& X, Window W, const Surv& K, uint64_t tgt, float
         pass_hist<Ctx, true>(X, W, K);
         X.push_hist();
         X.xsync();
-    }
-}
-
-template <int DT, bool HIST>
-__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a) {
-    using Ctx = RowCtx<DT, HIST>;
-    using E = Elem<DT>;
-    constexpr int VEC = E::kVec;
-    extern __shared__ __align__(128) unsigned char dyn[];
-    __shared__ SampleShared S;
-
-    Ctx X(S, cg::this_cluster());
-    X.s = static_cast<int>(X.cl.num_blocks());
-    X.rank = static_cast<int>(X.cl.block_rank());
-    X.row = blockIdx.x / X.s;
-    X.tid = threadIdx.x;
-    X.lane = X.tid & 31;
-    X.warp = X.tid >> 5;
-    X.a0 = X.rank * a.L;
-    X.a1 = min(X.a0 + a.L, a.V);
-    X.n = max(0, X.a1 - X.a0);
-    X.nv = (X.n + VEC - 1) / VEC;
-    X.nvf = X.n / VEC;
-    X.rounds = (X.nv + kThreads - 1) / kThreads;
-    X.data = dyn;
-    X.vmax = reinterpret_cast<float*>(dyn + a.vmax_off);
-    X.Wsum = reinterpret_cast<uint64_t*>(dyn + a.wsum_off);
-    X.par = 0;
-    X.passes = 0;
-    X.epoch = 0;
-    X.ghist_zeroed = -1;
-    X.cand_zeroed = -1;
-    X.has_patch = false;
-    X.row_nan = false;
-    X.bm = X.wp = nullptr;
-    X.patch = nullptr;
-    X.m = 0.0f;
-    X.c = 0.0f;
-    X.scale = 1.0f;
-    X.infm = false;
-    const int tid = X.tid, lane = X.lane, warp = X.warp, row = X.row;
-    const int a0 = X.a0, a1 = X.a1, n = X.n;
-    unsigned char* data = dyn;
-    const char* rowp = static_cast<const char*>(a.logits) + static_cast<int64_t>(row) * a.ld * E::kBytes;
-
-    // -------------------------------------------------------------- bulk copies of the slice
-    const int rpp = max(1, (X.rounds + kPieces - 1) / kPieces);  // rounds per piece
-    auto piece_v1 = [&](int p) { return min((p + 1) * rpp * kThreads, X.nvf); };
-    if (tid == 0) {
-        for (int p = 0; p < kPieces; ++p) mbar_init(&S.bar[p], 1);
-        fence_mbar_init();
-        S.flags = 0;
-        S.ccount = 0;
-    }
-    // the cluster histogram must be zero before any CTA pushes into it (the
-    // first cluster barrier orders this)
-    for (int b = tid; b < kBins; b += kThreads) S.ghist[b] = 0;
-    __syncthreads();
-    if (a.aligned && tid == 0) {
-        for (int p = 0; p < kPieces; ++p) {
-            const int v0 = p * rpp * kThreads, v1 = piece_v1(p);
-            if (v1 > v0) {
-                const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                mbar_arrive_expect_tx(&S.bar[p], bytes);
-                bulk_load(data + static_cast<size_t>(v0) * 16,
-                          rowp + static_cast<int64_t>(a0) * E::kBytes + static_cast<int64_t>(v0) * 16, bytes,
-                          &S.bar[p]);
-            }
-        }
-    }
-    // -------------------------------------------------------------- parameters
-    const arc_row_params P = load_params(a.params + row);
-    uint32_t rerr = 0;
-    {
-        const float T = P.temperature;
-        bool ok = isfinite(T) && T >= 0.0f;
-        ok &= (P.top_p > 0.0f) && (P.top_p <= 1.0f);
-        ok &= (P.min_p >= 0.0f) && (P.min_p <= 1.0f);
-        ok &= isfinite(P.repetition_penalty) && P.repetition_penalty > 0.0f;
-        ok &= isfinite(P.frequency_penalty) && isfinite(P.presence_penalty);
-        ok &= P.flags == 0u;
-        if (!ok) rerr |= ARC_ERR_PARAM;
-    }
-    // ids not covered by bulk copies: the ragged tail, or the whole slice when
-    // rows are not 16-byte aligned.  The last vector is padded with -inf (zero
-    // weight, never a maximum); its padded ids lie beyond V.
-    {
-        const int first = a.aligned ? X.nvf * VEC : 0;
-        for (int i = first + tid; i < X.nv * VEC; i += kThreads) {
-            if (i < n)
-                E::store_smem_raw(data, i, rowp, a0 + i);
-            else if (DT == ARC_BF16)
-                reinterpret_cast<unsigned short*>(data)[i] = 0xFF80;
-            else
-                reinterpret_cast<uint32_t*>(data)[i] = 0xFF800000u;
-        }
-    }
-    // -------------------------------------------------------------- history patches
-    if (HIST && a.hist_off != nullptr) {
-        const int hbeg = a.hist_off[row];
-        const int hn = a.hist_off[row + 1] - hbeg;
-        if (hn < 0) rerr |= ARC_ERR_HIST_ID;
-        if (hn > a.hist_cap) rerr |= ARC_ERR_HIST_CAP;
-        if (hn > 0 && rerr == 0) {
-            const int nwords = (X.nv * VEC + 31) / 32;
-            const int nwords_max = (a.rounds_max * kThreads * VEC + 31) / 32;
-            uint32_t* bmw = reinterpret_cast<uint32_t*>(dyn + a.hist_off_b);
-            uint32_t* wpw = bmw + nwords_max;
-            uint32_t* cnt = wpw + nwords_max;
-            float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
-            for (int w = tid; w < nwords; w += kThreads) bmw[w] = 0;
-            __syncthreads();
-            for (int e = tid; e < hn; e += kThreads) {
-                const int id = a.hist_ids[hbeg + e];
-                if (id < 0 || id >= a.V)
-                    atomicOr(&S.flags, ARC_ERR_HIST_ID);
-                else if (id >= a0 && id < a1)
-                    atomicOr(&bmw[(id - a0) >> 5], 1u << ((id - a0) & 31));
-            }
-            __syncthreads();
-            rerr |= S.flags & ARC_ERR_HIST_ID;
-            // rank of an id among the history ids of this slice: prefix popcount
-            const int per = (nwords + kThreads - 1) / kThreads;
-            const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
-            uint32_t mine = 0;
-            for (int w = w0; w < w1; ++w) mine += __popc(bmw[w]);
-            uint32_t inc = mine;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
-                if (lane >= d) inc += o;
-            }
-            if (lane == 31) S.wred32[warp] = inc;
-            __syncthreads();
-            uint32_t wbase = 0, distinct = 0;
-            for (int w = 0; w < kWarps; ++w) {
-                if (w < warp) wbase += S.wred32[w];
-                distinct += S.wred32[w];
-            }
-            uint32_t run = wbase + inc - mine;
-            for (int w = w0; w < w1; ++w) {
-                wpw[w] = run;
-                run += __popc(bmw[w]);
-            }
-            for (int q = tid; q < static_cast<int>(distinct); q += kThreads) cnt[q] = 0;
-            __syncthreads();
-            auto rank_of = [&](int li) {
-                return static_cast<int>(wpw[li >> 5] + __popc(bmw[li >> 5] & ((1u << (li & 31)) - 1u)));
-            };
-            for (int e = tid; e < hn; e += kThreads) {
-                const int id = a.hist_ids[hbeg + e];
-                if (id >= a0 && id < a1) atomicAdd(&cnt[rank_of(id - a0)], 1u);
-            }
-            __syncthreads();
-            const float rep = P.repetition_penalty, fr = P.frequency_penalty, pr = P.presence_penalty;
-            for (int e = tid; e < hn; e += kThreads) {
-                const int id = a.hist_ids[hbeg + e];
-                if (id >= a0 && id < a1) {
-                    const int q = rank_of(id - a0);
-                    float z = E::load_scalar(rowp, id);
-                    z = (z > 0.0f) ? __fdiv_rn(z, rep) : __fmul_rn(z, rep);
-                    z = __fsub_rn(z, __fmul_rn(static_cast<float>(cnt[q]), fr));
-                    z = __fsub_rn(z, pr);
-                    pat[q] = z;  // duplicates of an id store the same value
-                }
-            }
-            X.bm = bmw;
-            X.wp = wpw;
-            X.patch = pat;
-            X.has_patch = distinct > 0;
-        }
-    }
-    __syncthreads();
-
-    // -------------------------------------------------------------- pass 1: max / argmax
-    // Per vector a NaN-propagating max (packed bf16x2 for bf16); vectors with a
-    // NaN take the element path.  The NaN-free vector max is cached in vmax[].
-    float bv = -INFINITY;
-    int bvi = -1;
-    bool nanf = false, timeout = false;
-    for (int j = 0; j < X.rounds; ++j) {
-        if (a.aligned && (j % rpp) == 0) {
-            const int p = j / rpp;
-            if (piece_v1(p) > p * rpp * kThreads && !mbar_wait_bounded(&S.bar[p], 0)) timeout = true;
-        }
-        const int v = j * kThreads + tid;
-        if (v < X.nv) {
-            float vm;
-            if (X.vec_patched(v)) {
-                float z[VEC];
-                X.load(v, z);
-                vm = z[0];
-#pragma unroll
-                for (int e = 1; e < VEC; ++e) vm = fmax_nan(vm, z[e]);
-            } else {
-                vm = E::vmax_nan(reinterpret_cast<const uint4*>(data)[v]);
-            }
-            if (vm != vm) {
-                nanf = true;
-                float z[VEC];
-                X.load(v, z);
-                vm = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < VEC; ++e)
-                    if (z[e] > vm) vm = z[e];
-            }
-            X.vmax[v] = vm;
-            if (vm > bv) {
-                bv = vm;
-                bvi = v;
-            }
-        }
-    }
-    int bi = -1;
-    if (bvi >= 0) {
-        float z[VEC];
-        X.load(bvi, z);
-#pragma unroll
-        for (int e = VEC - 1; e >= 0; --e)
-            if (z[e] == bv) bi = a0 + bvi * VEC + e;
-    }
-    X.passes = 1;
-    warp_argmax(bv, bi);
-    const bool wnan = __any_sync(0xFFFFFFFFu, nanf), wto = __any_sync(0xFFFFFFFFu, timeout);
-    if (lane == 0) {
-        S.wred[warp] = (static_cast<uint64_t>(static_cast<uint32_t>(bi)) << 32) | __float_as_uint(bv);
-        if (wnan) atomicOr(&S.flags, ARC_ERR_NAN);
-        if (wto) atomicOr(&S.flags, ARC_ERR_TIMEOUT);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float v = -INFINITY;
-        int i = -1;
-        for (int w = 0; w < kWarps; ++w)
-            better(v, i, __uint_as_float(static_cast<uint32_t>(S.wred[w])), static_cast<int>(S.wred[w] >> 32));
-        S.slot[X.par][0] = (static_cast<uint64_t>(static_cast<uint32_t>(i)) << 32) | __float_as_uint(v);
-        S.slot[X.par][1] = S.flags & (ARC_ERR_NAN | ARC_ERR_TIMEOUT);
-    }
-    X.xsync();
-    float m;
-    int am;
-    uint32_t dflags;
-    {
-        float v = -INFINITY;
-        int i = -1;
-        uint32_t f = 0;
-        if (lane < X.s) {
-            const uint64_t x = X.xread(lane, 0);
-            v = __uint_as_float(static_cast<uint32_t>(x));
-            i = static_cast<int>(x >> 32);
-            f = static_cast<uint32_t>(X.xread(lane, 1));
-        }
-        warp_argmax(v, i);
-        m = v;
-        am = i;
-        dflags = __reduce_or_sync(0xFFFFFFFFu, f);
-    }
-    X.xnext();
-    X.row_nan = (dflags & ARC_ERR_NAN) != 0;
-    if ((a.flags & ARC_OPT_STEP_AUTOINC) && X.rank == 0 && tid == 0) a.params[row].step = P.step + 1;
-
-    // -------------------------------------------------------------- mode
-    uint32_t err = rerr | dflags;
-    const float T = P.temperature;
-    const int k = P.top_k;
-    const bool topk_on = k >= 1 && k < a.V;
-    const bool topp_on = P.top_p < 1.0f;
-    const bool minp_on = P.min_p > 0.0f;
-    int mode;
-    int token = -2;  // -2: decided by the draw
-    if (rerr != 0 || (dflags & ARC_ERR_TIMEOUT)) {
-        mode = -1;
-        token = -1;
-    } else {
-        mode = (T == 0.0f || k == 1) ? 0 : ((!topk_on && !topp_on && !minp_on) ? 1 : 2);
-        if (am < 0) {
-            token = 0;
-            err |= ARC_ERR_DEGENERATE;
-        } else if (mode == 0) {
-            token = am;
-        }
-    }
-
-    uint32_t kap_k = 0, kap_r = 0;
-    int iot_k = a.V, iot_r = a.V;
-    uint64_t mass_k = 0, mass_r = 0, target = 0, rbits = 0;
-    bool walk_fail = false;
-
-    if (token != -2) {
-        cluster_arrive();  // this CTA reads no other CTA's shared memory after this
-    } else {
-        // ---------------------------------------------------------- sampling rows
-        X.m = m;
-        X.infm = (m == INFINITY);
-        X.c = __fdiv_rn(1.4426950408889634f, T);  // w = 2^((z - m) * log2(e) / T)
-        X.scale = __uint_as_float(static_cast<uint32_t>(127 + a.F) << 23);
-        const uint32_t Km = fkey(m);
-        // per-row fp64 thresholds, one lane per warp:
-        //   zm: min-p, w >= min_p  <=>  z >= m + T ln(min_p), rounded up to fp32
-        //   zb: top-p window floor; ids below it carry < half of (1 - top_p) of the mass
-        float zm = -INFINITY, zb = -INFINITY;
-        if (lane == 0) {
-            if (minp_on)
-                zm = __double2float_ru(static_cast<double>(m) +
-                                       static_cast<double>(T) * log(static_cast<double>(P.min_p)));
-            if (topp_on)
-                zb = __double2float_rd(static_cast<double>(m) +
-                                       static_cast<double>(T) * log((1.0 - static_cast<double>(P.top_p)) /
-                                                                    (2.0 * static_cast<double>(a.V))));
-        }
-        zm = __shfl_sync(0xFFFFFFFFu, zm, 0);
-        zb = __shfl_sync(0xFFFFFFFFu, zb, 0);
-
-        Surv K{-INFINITY, INT_MAX};  // every non-NaN id
-        if (topk_on) {
-            K = select_topk(X, k, Km, err);
-            kap_k = (K.zt == -INFINITY && K.ge_form()) ? 0u : fkey(K.zt);
-            iot_k = K.ge_form() ? a.V : K.iota;
-        }
-        Surv R = K;
-        bool wsum_is_R = false;
-        if (topp_on) {
-            // masses over K, plus the mass histogram of a key window that holds
-            // the top-p cutoff
-            const float zfloor = fmaxf(zm, K.zt);
-            float zlo = fmaxf(zb, zfloor);
-            Window W = Ctx::make_window(fkey(zlo), Km);
-            const int mk = mass_mode(X, K);
-            pass_mass<Ctx, true>(X, mk, K, W);
-            X.publish_wsum_total(0);
-            X.push_hist();
-            X.xsync();
-            mass_k = X.xscan(0, ~0ull).total;
-            X.xnext();
-            uint64_t tgt = 1;
-            if (lane == 0)
-                tgt = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(mass_k)));
-            tgt = shfl_u64(tgt, 0);
-            if (tgt == 0) tgt = 1;
-            float zp = -INFINITY;
-            bool found = select_mass(X, W, K, tgt, zp);
-            if (!found && zlo > zfloor) {
-                // rounding left the first window just short: retry down to the hard bound
-                zlo = zfloor;
-                W = Ctx::make_window(fkey(zlo), Km);
-                pass_hist<Ctx, true>(X, W, K);
-                X.push_hist();
-                X.xsync();
-                found = select_mass(X, W, K, tgt, zp);
-            }
-            // short of the target even then: min-p (or top-k) bounds the window,
-            // so the top-p cutoff lies below every id those filters keep
-            const float zx = found ? fmaxf(zp, zm) : zm;
-            if (zx > K.zt)
-                R = Surv{zx, INT_MAX};
-            else
-                wsum_is_R = true;
-        } else if (minp_on && zm > K.zt) {
-            R = Surv{zm, INT_MAX};
-        }
-        kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
-        iot_r = R.ge_form() ? a.V : R.iota;
-
-        // ---------------------------------------------------------- inverse-CDF draw
-        const int mr = mass_mode(X, R);
-        if (!wsum_is_R) pass_mass<Ctx, false>(X, mr, R, Window{0u, 0u, 0});
-        X.publish_wsum_total(0);
-        rbits = splitmix64(P.seed ^ (static_cast<uint64_t>(row) << 32) ^ P.step) >> 11;
-        X.xsync();
-        mass_r = X.xscan(0, ~0ull).total;
-        target = scale_by_u(rbits, mass_r);
-        const typename Ctx::Scan sc = X.xscan(0, target);
-        X.xnext();
-        cluster_arrive();  // this CTA reads no other CTA's shared memory after this
-        if (sc.first < 0) {
-            err |= kErrInternal;
-            token = am;
-        } else if (sc.first == X.rank) {
-            const uint64_t t = target - sc.before_me;
-            int tok = X.walk(
-                t, [&](const float(&z)[VEC], int g0) { return X.vec_mass(mr, z, g0, R); },
-                [&](const float(&z)[VEC], int g0, uint64_t tt) { return X.vec_mass_walk(mr, z, g0, R, tt); });
-            if (tok < 0) {
-                tok = am;
-                walk_fail = true;
-            }
-            if (tid == 0) {
-                a.out[row] = tok;
-                if (a.debug) a.debug[row].token = tok;
-            }
-        }
-    }
-
-    // -------------------------------------------------------------- results
-    if (X.rank == 0 && tid == 0) {
-        if (token != -2) a.out[row] = token;
-        if (err != 0 && a.err_word) atomicOr(a.err_word, err);
-        if (a.debug) {
-            arc_row_debug& d = a.debug[row];
-            d.mode = mode;
-            d.err = err;
-            if (token != -2) d.token = token;
-            d.passes = X.passes;
-            d.kappa_k = kap_k;
-            d.iota_k = iot_k;
-            d.kappa_r = kap_r;
-            d.iota_r = iot_r;
-            d.max_z = m;
-            d.frac_bits = a.F;
-            d.rbits = rbits;
-            d.mass_k = mass_k;
-            d.mass_r = mass_r;
-            d.target = target;
-        }
-    }
-    // no CTA may leave while another can still read its shared memory
-    cluster_wait();
-    if (walk_fail && tid == 0) {
-        if (a.err_word) atomicOr(a.err_word, kErrInternal);
-        if (a.debug) atomicOr(&a.debug[row].err, kErrInternal);
-    }
-    if (timeout && a.aligned) {
-        // give bulk copies still in flight a bounded chance to land before exit
-        for (int p = 0; p < kPieces; ++p)
-            if (piece_v1(p) > p * rpp * kThreads) (void)mbar_wait_bounded(&S.bar[p], 0);
     }
 }
 

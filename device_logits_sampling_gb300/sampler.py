@@ -25,6 +25,7 @@ ARC_E_ALIGN = -4
 ARC_E_UNSUPPORTED = -5
 ARC_E_OPTION = -6
 ARC_E_CUDA = -7
+ARC_E_WORKSPACE = -8
 
 ARC_ERR_PARAM = 0x1
 ARC_ERR_HIST_ID = 0x2
@@ -52,7 +53,7 @@ assert ROW_DEBUG_DTYPE.itemsize == 72
 class Options(ctypes.Structure):
     _fields_ = [
         ("flags", ctypes.c_uint32),
-        ("cluster_ctas", ctypes.c_int32),
+        ("ctas_per_row", ctypes.c_int32),
         ("max_hist_len", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
         ("debug", ctypes.c_void_p),
@@ -61,13 +62,14 @@ class Options(ctypes.Structure):
 
 class Geometry(ctypes.Structure):
     _fields_ = [
-        ("cluster_ctas", ctypes.c_int32),
+        ("ctas_per_row", ctypes.c_int32),
         ("threads", ctypes.c_int32),
         ("slice_elems", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
         ("grid_ctas", ctypes.c_int64),
         ("frac_bits", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_int64),
     ]
 
 
@@ -78,7 +80,9 @@ SIGNATURES = {
     "arc_sample_batch": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-        ctypes.POINTER(Options), ctypes.c_void_p]),
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(Options), ctypes.c_void_p]),
+    "arc_sample_workspace_bytes": (ctypes.c_size_t, [
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Options)]),
     "arc_sample_greedy": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
@@ -160,23 +164,46 @@ def debug_records(t) -> np.ndarray:
     return t.cpu().numpy().view(ROW_DEBUG_DTYPE)
 
 
-def make_options(cluster_ctas=0, max_hist_len=0, autoinc=False, debug=None) -> Options:
-    return Options(ARC_OPT_STEP_AUTOINC if autoinc else 0, int(cluster_ctas), int(max_hist_len), 0,
+def make_options(ctas_per_row=0, max_hist_len=0, autoinc=False, debug=None) -> Options:
+    return Options(ARC_OPT_STEP_AUTOINC if autoinc else 0, int(ctas_per_row), int(max_hist_len), 0,
                    _ptr(debug))
 
 
+def workspace_bytes(B: int, V: int, dtype: int, has_history=False, ctas_per_row=0, max_hist_len=0) -> int:
+    opts = make_options(ctas_per_row, max_hist_len)
+    return int(load().arc_sample_workspace_bytes(int(B), int(V), int(dtype), int(bool(has_history)),
+                                                 ctypes.byref(opts)))
+
+
+def workspace_tensor(B: int, V: int, dtype: int, has_history=False, ctas_per_row=0, max_hist_len=0,
+                     device="cuda"):
+    """A zero-filled device workspace for arc_sample_batch (uint8 tensor)."""
+    import torch
+
+    n = workspace_bytes(B, V, dtype, has_history, ctas_per_row, max_hist_len)
+    if n == 0:
+        raise ValueError("arc_sample_workspace_bytes rejected the shape or options")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
 def sample_batch(logits, params, out, hist_offsets=None, hist_ids=None, err_word=None, debug=None,
-                 cluster_ctas=0, max_hist_len=0, autoinc=False, stream=None, check=True) -> int:
+                 workspace=None, ctas_per_row=0, max_hist_len=0, autoinc=False, stream=None,
+                 check=True) -> int:
     """arc_sample_batch on CUDA tensors: logits [B, V] (row stride >= V), params uint8
-    [B*48], out int32 [B], optional CSR history (int32), err_word uint32 [1], debug uint8 [B*72]."""
+    [B*48], out int32 [B], optional CSR history (int32), err_word uint32 [1], debug uint8
+    [B*72], workspace uint8 (zero-filled once; allocated here when None)."""
     B, V = int(logits.shape[0]), int(logits.shape[1])
     ld = int(logits.stride(0)) if B > 1 else V
     if logits.stride(1) != 1:
         raise ValueError("logits rows must be contiguous")
-    opts = make_options(cluster_ctas, max_hist_len, autoinc, debug)
+    if workspace is None:
+        workspace = workspace_tensor(B, V, _dtype_code(logits), hist_offsets is not None, ctas_per_row,
+                                     max_hist_len, device=logits.device)
+    opts = make_options(ctas_per_row, max_hist_len, autoinc, debug)
     rc = load().arc_sample_batch(_ptr(logits), B, V, ld, _dtype_code(logits), _ptr(params),
                                  _ptr(hist_offsets), _ptr(hist_ids), _ptr(out), _ptr(err_word),
-                                 ctypes.byref(opts), _stream(stream))
+                                 _ptr(workspace), int(workspace.numel()), ctypes.byref(opts),
+                                 _stream(stream))
     if check and rc != ARC_OK:
         raise ArcError(rc)
     return rc
@@ -194,9 +221,9 @@ def sample_greedy(logits, out, err_word=None, stream=None, check=True) -> int:
     return rc
 
 
-def plan(B: int, V: int, dtype: int, has_history=False, cluster_ctas=0, max_hist_len=0) -> Geometry:
+def plan(B: int, V: int, dtype: int, has_history=False, ctas_per_row=0, max_hist_len=0) -> Geometry:
     g = Geometry()
-    opts = make_options(cluster_ctas, max_hist_len)
+    opts = make_options(ctas_per_row, max_hist_len)
     rc = load().arc_sample_plan(int(B), int(V), int(dtype), int(bool(has_history)), ctypes.byref(opts),
                                 ctypes.byref(g))
     if rc != ARC_OK:

