@@ -5,6 +5,7 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "arc_sample.h"
 #include "argmax_kernel.cuh"
@@ -25,6 +26,9 @@ struct Plan {
     int hist_cap = 0;
     int scan_smem = 0;      // dynamic shared memory of the scan kernel
     int cmax_off = 0;       // finish kernel layout
+    int cs_off = 0;
+    int clist_off = 0;
+    int cand_off = 0;
     int fb_wsum_off = 0;
     int fb_patch_off = 0;
     int fb_rounds = 0;
@@ -94,16 +98,20 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
         const int64_t nwords = (int64_t{kVpt} * kThreads * vec + 31) / 32;
         scan_smem = 2 * nwords * 4 + 2 * int64_t{cap} * 4;
     }
-    const int64_t cmax_bytes = ((s * kChunks * 4 + 127) / 128) * 128;
+    auto r128 = [](int64_t x) { return ((x + 127) / 128) * 128; };
+    const int64_t cmax_bytes = r128(s * kChunks * 4);
+    const int64_t cs_bytes = cmax_bytes;
+    const int64_t clist_bytes = r128(s * kChunks * 4);
+    const int64_t cand_bytes = r128(int64_t{kCandCap} * 16);
     const int64_t nv_row = (V + vec - 1) / vec;
     const int64_t fb_rounds = (nv_row + kThreads - 1) / kThreads;
-    const int64_t fb_wsum = ((fb_rounds * kWarps * 8 + 127) / 128) * 128;
+    const int64_t fb_wsum = r128(fb_rounds * kWarps * 8);
     int64_t fb_patch = 0;
     if (has_hist) {
         const int64_t nwords = (fb_rounds * kThreads * vec + 31) / 32;
         fb_patch = 2 * nwords * 4 + 2 * int64_t{cap} * 4;
     }
-    const int64_t fin_smem = cmax_bytes + fb_wsum + fb_patch;
+    const int64_t fin_smem = cmax_bytes + cs_bytes + clist_bytes + cand_bytes + fb_wsum + fb_patch;
     const int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
     if (fin_smem > limit || scan_smem > limit) return ARC_E_UNSUPPORTED;
     p.s = static_cast<int>(s);
@@ -111,8 +119,11 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     p.hist_cap = cap;
     p.scan_smem = static_cast<int>(scan_smem);
     p.cmax_off = 0;
-    p.fb_wsum_off = static_cast<int>(cmax_bytes);
-    p.fb_patch_off = static_cast<int>(cmax_bytes + fb_wsum);
+    p.cs_off = static_cast<int>(cmax_bytes);
+    p.clist_off = static_cast<int>(cmax_bytes + cs_bytes);
+    p.cand_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes);
+    p.fb_wsum_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes);
+    p.fb_patch_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + fb_wsum);
     p.fb_rounds = static_cast<int>(fb_rounds);
     p.fin_smem = static_cast<int>(fin_smem);
     p.slices = B * s;
@@ -143,24 +154,26 @@ cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     done.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
 }
 
-// Resident CTAs per SM for this kernel and shared memory (cached per device).
-template <class K>
-int blocks_per_sm(K kernel, int dev, int smem) {
-    static std::atomic<int> cache[kMaxDevices][8];
-    static std::atomic<int> cache_smem[kMaxDevices][8];
-    const int slot = (reinterpret_cast<uintptr_t>(reinterpret_cast<const void*>(kernel)) >> 4) & 7;
-    if (dev >= 0 && dev < kMaxDevices && cache_smem[dev][slot].load() == smem + 1) return cache[dev][slot].load();
+// Resident CTAs per SM of KERNEL with `smem` bytes of dynamic shared memory
+// (cached per device and size).
+template <auto KERNEL>
+int blocks_per_sm(int dev, int smem) {
+    static std::atomic<int> cache[kMaxDevices];
+    static std::atomic<int> cache_smem[kMaxDevices];
+    if (dev >= 0 && dev < kMaxDevices && cache_smem[dev].load() == smem + 1) return cache[dev].load();
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, static_cast<size_t>(smem)) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, KERNEL, kThreads, static_cast<size_t>(smem)) != cudaSuccess ||
         nb <= 0)
         nb = 1;
     if (dev >= 0 && dev < kMaxDevices) {
-        cache[dev][slot].store(nb);
-        cache_smem[dev][slot].store(smem + 1);
+        cache[dev].store(nb);
+        cache_smem[dev].store(smem + 1);
     }
     return nb;
 }
@@ -285,7 +298,6 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     sa.summaries = static_cast<unsigned char*>(workspace);
     sa.hist_cap = p.hist_cap;
     sa.aligned = aligned;
-    sa.patch_off = 0;
     FinishArgs fa;
     fa.logits = logits;
     fa.ld = ld;
@@ -305,6 +317,9 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.flags = opts ? opts->flags : 0u;
     fa.aligned = aligned;
     fa.cmax_off = p.cmax_off;
+    fa.cs_off = p.cs_off;
+    fa.clist_off = p.clist_off;
+    fa.cand_off = p.cand_off;
     fa.fb_wsum_off = p.fb_wsum_off;
     fa.fb_patch_off = p.fb_patch_off;
     fa.fb_rounds = p.fb_rounds;
@@ -313,7 +328,9 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     auto go = [&](auto scan, auto fin, std::atomic<uint64_t>& done_s, std::atomic<uint64_t>& done_f) {
         cudaError_t err = prepare(scan, dev, done_s);
         if (err == cudaSuccess) err = prepare(fin, dev, done_f);
-        if (err == cudaSuccess) err = launch_cluster(scan, p.slices, 1, p.scan_smem, st, sa);
+        if (err != cudaSuccess) return err;
+        scan<<<static_cast<unsigned>(p.slices), kThreads, p.scan_smem, st>>>(sa);
+        err = cudaGetLastError();
         if (err == cudaSuccess) err = launch_cluster(fin, B, 1, p.fin_smem, st, fa);
         return err;
     };

@@ -78,11 +78,13 @@ def test_single_row_decode_loop_1000_steps(cuda_lib):
     u = np.array([oracle.uniform(0, 0, s) for s in range(1000)])
     want = oracle.draw_many(r0.w, r0.R, u)
     mism = np.nonzero(got != want)[0]
-    for s in mism:  # only boundary cases may differ
-        run_ = np.cumsum(r0.w) / r0.w.sum()
-        near = np.min(np.abs(run_[max(0, want[s] - 1):want[s] + 1] - u[s]))
-        assert near <= 1e-6, (s, got[s], want[s])
-    assert mism.size <= 2
+    run_ = np.cumsum(r0.w) / r0.w.sum()
+    # draws whose u lies within 1e-6 of the oracle's CDF at the drawn token's
+    # boundaries: the only ones allowed to differ (counted and reported)
+    near = np.array([np.min(np.abs(run_[max(0, want[s] - 1):want[s] + 1] - u[s])) for s in range(1000)])
+    boundary = np.nonzero(near <= 1e-6)[0]
+    print(f"decode loop: {mism.size} of 1000 tokens differ, {boundary.size} draws lie within 1e-6 of a boundary")
+    assert set(mism.tolist()) <= set(boundary.tolist()), (mism.tolist(), boundary.tolist())
     # the draws follow the softmax: spikes carry most of the mass
     spikes = set(w.notes["spikes"].tolist())
     frac = np.mean([t in spikes for t in got])
