@@ -29,6 +29,8 @@ struct Plan {
     int cs_off = 0;
     int clist_off = 0;
     int cand_off = 0;
+    int sorted_off = 0;
+    int stage_off = 0;
     int fb_wsum_off = 0;
     int fb_patch_off = 0;
     int fb_rounds = 0;
@@ -101,8 +103,9 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     auto r128 = [](int64_t x) { return ((x + 127) / 128) * 128; };
     const int64_t cmax_bytes = r128(s * kChunks * 4);
     const int64_t cs_bytes = cmax_bytes;
-    const int64_t clist_bytes = r128(s * kChunks * 4);
+    const int64_t clist_bytes = r128((s * kChunks + kWarps) * 4);
     const int64_t cand_bytes = r128(int64_t{kCandCap} * 16);
+    const int64_t stage_bytes = int64_t{kWarps} * kCollectU * 32 * 16 + cand_bytes;  // + sorted candidates
     const int64_t nv_row = (V + vec - 1) / vec;
     const int64_t fb_rounds = (nv_row + kThreads - 1) / kThreads;
     const int64_t fb_wsum = r128(fb_rounds * kWarps * 8);
@@ -111,7 +114,7 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
         const int64_t nwords = (fb_rounds * kThreads * vec + 31) / 32;
         fb_patch = 2 * nwords * 4 + 2 * int64_t{cap} * 4;
     }
-    const int64_t fin_smem = cmax_bytes + cs_bytes + clist_bytes + cand_bytes + fb_wsum + fb_patch;
+    const int64_t fin_smem = cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch;
     const int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
     if (fin_smem > limit || scan_smem > limit) return ARC_E_UNSUPPORTED;
     p.s = static_cast<int>(s);
@@ -122,8 +125,10 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     p.cs_off = static_cast<int>(cmax_bytes);
     p.clist_off = static_cast<int>(cmax_bytes + cs_bytes);
     p.cand_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes);
-    p.fb_wsum_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes);
-    p.fb_patch_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + fb_wsum);
+    p.stage_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes);
+    p.sorted_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + int64_t{kWarps} * kCollectU * 32 * 16);
+    p.fb_wsum_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes);
+    p.fb_patch_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum);
     p.fb_rounds = static_cast<int>(fb_rounds);
     p.fin_smem = static_cast<int>(fin_smem);
     p.slices = B * s;
@@ -320,6 +325,8 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.cs_off = p.cs_off;
     fa.clist_off = p.clist_off;
     fa.cand_off = p.cand_off;
+    fa.sorted_off = p.sorted_off;
+    fa.stage_off = p.stage_off;
     fa.fb_wsum_off = p.fb_wsum_off;
     fa.fb_patch_off = p.fb_patch_off;
     fa.fb_rounds = p.fb_rounds;

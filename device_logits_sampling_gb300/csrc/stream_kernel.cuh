@@ -33,9 +33,7 @@ constexpr int kHdrBytes = 32;
 constexpr int kSummaryBytes = kHdrBytes + kChunks * 8;
 constexpr int kMaxRowCtas = 128;         // slices per row at most
 constexpr int kCandCap = 1024;           // ids the direct selection holds
-constexpr int kCandChunks = 256;         // chunks it reads at most
 constexpr int kCollectU = 8;             // chunks per warp in flight while gathering
-constexpr int kFloorBins = 1024;         // bins of the floor search (10 key bits per pass)
 
 struct ScanArgs {
     const void* logits;
@@ -72,8 +70,10 @@ struct FinishArgs {
     int aligned;
     int cmax_off;      // dynamic shared memory: chunk maxima of the row,
     int cs_off;        //   chunk masses,
-    int clist_off;     //   candidate chunk list,
+    int clist_off;     //   per-warp candidate chunk lists,
     int cand_off;      //   candidates (key, id, mass),
+    int sorted_off;    //   the candidates in (key desc, id asc) order,
+    int stage_off;     //   gather staging (kWarps x kCollectU x 32 vectors),
     int fb_wsum_off;   //   per-(round, warp) masses,
     int fb_patch_off;  //   row patch tables
     int fb_rounds;     // rounds of a whole row
@@ -84,8 +84,10 @@ struct SliceHeader {
     int am;          // its first id, -1 when none
     uint32_t flags;  // ARC_ERR_NAN | ARC_ERR_HIST_ID | ARC_ERR_HIST_CAP
     int nchunk;      // chunk entries written
-    int pad[4];
+    double tlnp;     // slice 0 of a min-p row: T ln(min_p) in fp64, else 0
+    int pad[2];
 };
+static_assert(sizeof(SliceHeader) == kHdrBytes, "slice header size");
 
 struct FinishScratch {
     uint64_t redu[kWarps];
@@ -94,14 +96,12 @@ struct FinishScratch {
     uint64_t bu[8];
     float bf[8];
     uint32_t ccount;  // candidates gathered
+    uint32_t fc[2][kWarps][4];  // floor search partial counts
     double bd[2];
 };
 
 struct __align__(16) KernelShared {
-    union {
-        SampleShared fb;              // general selection path
-        uint32_t fhist[kFloorBins + kFloorBins / 32];  // floor search (padded)
-    };
+    SampleShared fb;  // general selection path
     FinishScratch st;
 };
 
@@ -348,6 +348,11 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
     const bool need_data = rerr == 0;
     const bool row_chunks = need_data && !md.greedy;
     const bool mass = row_chunks && md.need_mass;
+    // slice 0 of a min-p row carries T ln(min_p) in fp64 for the finish kernel;
+    // thread 0 takes it while the slice's loads are still in flight
+    double tlnp = 0.0;
+    if (cidx == 0 && tid == 0 && row_chunks && md.filtered && md.minp_on)
+        tlnp = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
     const float cT = mass ? __fdiv_rn(1.4426950408889634f, P.temperature) : 0.0f;
 
     const uint32_t* pbm = nullptr;
@@ -474,7 +479,8 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         h.am = amc;
         h.flags = nanw | (rerr & (ARC_ERR_HIST_ID | ARC_ERR_HIST_CAP));
         h.nchunk = row_chunks ? kChunks : 0;
-        h.pad[0] = h.pad[1] = h.pad[2] = h.pad[3] = 0;
+        h.tlnp = tlnp;
+        h.pad[0] = h.pad[1] = 0;
         *reinterpret_cast<SliceHeader*>(mysum) = h;
     }
 }
@@ -520,73 +526,273 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
     return t;
 }
 
-// Floor search over n weighted keys: the lower edge (to 2^12 keys) of the
-// largest key x whose entries at or above it weigh at least tgt in total.
-// kw(e, key, weight) gives entry e (u32 weights whose sum fits in 32 bits).
-// False when all entries weigh less than tgt.  Two passes of 10 key bits
-// over a 1024-bin histogram (native 32-bit shared atomics; bin b lives at
-// b + b / 32 so that warp 0 scans it without bank conflicts).
+// Floor search, one pass: entries binned by (m - x) in steps of 1/8 over the
+// 32 logit units below the row max m (256 bins, 32-bit shared atomics), then
+// warp 0 finds the first bin at which the running weight reaches tgt.  The
+// floor lies below that bin: every entry counted is at or above it, so the
+// bound holds.  False when the window holds less than tgt (the exact
+// search below then decides).
 template <class KW>
-__device__ bool floor_select(int n, KW kw, uint32_t tgt, uint32_t* hist, FinishScratch& SS, uint32_t& edge) {
+__device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, FinishScratch& SS, float& zf) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    auto at = [](int b) { return b + (b >> 5); };
-    uint32_t prefix = 0;
-    uint32_t rem = tgt;
-    for (int pass = 0; pass < 2; ++pass) {
-        const int shift = pass == 0 ? 22 : 12;
-        for (int b = tid; b < kFloorBins + kFloorBins / 32; b += kThreads) hist[b] = 0;
-        __syncthreads();
-        for (int e = tid; e < n; e += kThreads) {
-            uint32_t key, w;
-            kw(e, key, w);
-            if (w != 0 && (pass == 0 || (key >> 22) == (prefix >> 22)))
-                atomicAdd(&hist[at(static_cast<int>((key >> shift) & (kFloorBins - 1)))], w);
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // lane l owns bins 1023 - 32 l down to 992 - 32 l: an inclusive scan
-            // in lane order walks the bins from the top key down
-            uint32_t loc = 0;
-#pragma unroll 8
-            for (int q = 0; q < 32; ++q) loc += hist[at(kFloorBins - 1 - 32 * lane - q)];
-            uint32_t inc = loc;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
-                if (lane >= d) inc += o;
-            }
-            const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
-            const uint32_t before = inc - loc;
-            if (lane == 0) SS.bi[4] = (total < rem) ? -2 : -1;
-            __syncwarp();
-            if (total >= rem && before < rem && inc >= rem) {
-                uint32_t run = before;
-                for (int q = 0; q < 32; ++q) {
-                    const int b = kFloorBins - 1 - 32 * lane - q;
-                    const uint32_t hb = hist[at(b)];
-                    if (run + hb >= rem) {
-                        SS.bi[4] = b;
-                        SS.bu[4] = run;
-                        break;
-                    }
-                    run += hb;
-                }
-            }
-        }
-        __syncthreads();
-        const int b = SS.bi[4];
-        if (b < 0) return false;  // uniform: every thread reads the same slot
-        rem -= static_cast<uint32_t>(SS.bu[4]);
-        prefix |= static_cast<uint32_t>(b) << shift;
-        __syncthreads();  // the histogram and the slots are rewritten next pass
+    constexpr int kHB = 256;
+    constexpr float kStep = 8.0f;  // bins per logit unit
+    for (int b = tid; b < kHB; b += kThreads) hist[b] = 0u;
+    __syncthreads();
+    for (int e = tid; e < n; e += kThreads) {
+        float x;
+        uint32_t w;
+        kw(e, x, w);
+        const float d = __fmul_rn(__fsub_rn(m, x), kStep);  // >= 0; NaN-free
+        if (w != 0u && d < static_cast<float>(kHB)) atomicAdd(&hist[static_cast<int>(d)], w);
     }
-    edge = prefix;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t loc = 0;
+#pragma unroll
+        for (int q = 0; q < kHB / 32; ++q) loc += hist[lane * (kHB / 32) + q];
+        uint32_t inc = loc;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        int bin = -1;
+        if (inc >= tgt && inc - loc < tgt) {
+            uint32_t run = inc - loc;
+#pragma unroll
+            for (int q = 0; q < kHB / 32; ++q) {
+                run += hist[lane * (kHB / 32) + q];
+                if (bin < 0 && run >= tgt) bin = lane * (kHB / 32) + q;
+            }
+        }
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, bin >= 0);
+        bin = bal ? __shfl_sync(0xFFFFFFFFu, bin, __ffs(bal) - 1) : -1;
+        // entries of bins 0..b satisfy m - x < (b + 1) / 8 up to the rounding of
+        // m - x (far below a bin): one bin of margin, the edge rounded down
+        if (lane == 0) SS.bf[3] = (bin < 0) ? -INFINITY : __fsub_rd(m, static_cast<float>(bin + 2) / kStep);
+    }
+    __syncthreads();
+    zf = SS.bf[3];
+    return zf > -INFINITY;
+}
+
+// Floor search by the whole CTA: the largest key x, to 2^12 keys, whose
+// entries at or above it weigh at least tgt in total, two key bits per step
+// from the top (three candidate prefixes counted per step; one barrier per
+// step).  kw(e, key, weight) gives entry e; PER entries per thread are held in
+// registers (n <= PER * kThreads); the weights' sum must fit in 32 bits.
+// False when all entries weigh less than tgt.
+template <int PER, class KW>
+__device__ bool floor_block(int n, KW kw, uint32_t tgt, FinishScratch& SS, uint32_t& edge) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t key[PER], w[PER];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        const int e = tid + q * kThreads;
+        key[q] = 0u;
+        w[q] = 0u;
+        if (e < n) kw(e, key[q], w[q]);
+        tot += w[q];
+    }
+    tot = __reduce_add_sync(0xFFFFFFFFu, tot);
+    if (lane == 0) SS.fc[0][warp][0] = tot;
+    __syncthreads();
+    uint32_t all = 0;
+    for (int v = 0; v < kWarps; ++v) all += SS.fc[0][v][0];
+    if (all < tgt) return false;  // uniform
+    uint32_t p = 0;
+    int par = 1;
+#pragma unroll 1
+    for (int b = 30; b >= 12; b -= 2, par ^= 1) {
+        const uint32_t t1 = p | (1u << b), t2 = p | (2u << b), t3 = p | (3u << b);
+        uint32_t c1 = 0, c2 = 0, c3 = 0;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            c1 += (key[q] >= t1) ? w[q] : 0u;
+            c2 += (key[q] >= t2) ? w[q] : 0u;
+            c3 += (key[q] >= t3) ? w[q] : 0u;
+        }
+        c1 = __reduce_add_sync(0xFFFFFFFFu, c1);
+        c2 = __reduce_add_sync(0xFFFFFFFFu, c2);
+        c3 = __reduce_add_sync(0xFFFFFFFFu, c3);
+        if (lane == 0) {
+            SS.fc[par][warp][0] = c1;
+            SS.fc[par][warp][1] = c2;
+            SS.fc[par][warp][2] = c3;
+        }
+        __syncthreads();  // (the other parity slot is rewritten only after the next barrier)
+        uint32_t s1 = 0, s2 = 0, s3 = 0;
+        for (int v = 0; v < kWarps; ++v) {
+            s1 += SS.fc[par][v][0];
+            s2 += SS.fc[par][v][1];
+            s3 += SS.fc[par][v][2];
+        }
+        p = (s3 >= tgt) ? t3 : ((s2 >= tgt) ? t2 : ((s1 >= tgt) ? t1 : p));
+    }
+    edge = p;
     return true;
 }
 
 // ------------------------------------------------------------------ finish
+// What the steps of one row's finish share, and what they report.
+struct RowState {
+    float m;         // row max of the penalised logits
+    int am;          // its first id
+    float cT;        // log2(e) / T
+    float scale;     // 2^F: fixed-point unit of a weight
+    float zm;        // min-p threshold (z >= zm survives), -inf when off
+    bool row_nan, infm;
+    uint64_t rbits;  // the row's 53 random bits
+    uint64_t S_all;  // chunk tables' total mass (rows that need it)
+    uint32_t err;
+    uint32_t kap_k, kap_r;
+    int iot_k, iot_r;
+    uint64_t mass_k, mass_r, target;
+    int token, passes;
+};
+
+// Exact selection over the row in global memory by multi-way threshold
+// bisection (row_select.cuh), skipping every 32-vector chunk whose max lies
+// below a pass's threshold: the path for rows whose floor admits too many
+// ids.  Kept out of line so that the direct path stays compact.
 template <int DT, bool HIST>
-__global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a) {
+__device__ __noinline__ void finish_general(const FinishArgs& a, const arc_row_params& P, const RowMode& md, int row,
+                                            const char* rowp, float* cm, const uint32_t* pbm, const uint32_t* pwp,
+                                            const float* ppat, bool has_patch, KernelShared& KS, unsigned char* dyn,
+                                            RowState& st) {
+    using E = Elem<DT>;
+    using Ctx = RowCtx<DT, HIST>;
+    constexpr int VEC = E::kVec;
+    FinishScratch& SS = KS.st;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float T = P.temperature;
+    const float m = st.m, zm = st.zm;
+    __syncthreads();
+    cg::cluster_group cl = cg::this_cluster();
+    Ctx X(KS.fb, cl);
+    X.s = 1;
+    X.rank = 0;
+    X.row = row;
+    X.tid = tid;
+    X.lane = lane;
+    X.warp = warp;
+    X.a0 = 0;
+    X.a1 = a.V;
+    X.n = a.V;
+    X.nv = (a.V + VEC - 1) / VEC;
+    X.nvf = a.V / VEC;
+    X.rounds = (X.nv + kThreads - 1) / kThreads;
+    X.data = reinterpret_cast<const unsigned char*>(rowp);
+    X.src_global = true;
+    X.src_aligned = a.aligned != 0;
+    X.vmax = cm;
+    X.vps = a.L / VEC;
+    X.cps = kChunks;
+    X.Wsum = reinterpret_cast<uint64_t*>(dyn + a.fb_wsum_off);
+    X.par = 0;
+    X.passes = 0;
+    X.epoch = 1;
+    X.ghist_zeroed = -1;
+    X.cand_zeroed = -1;
+    X.has_patch = has_patch;
+    X.row_nan = st.row_nan;
+    X.bm = pbm;
+    X.wp = pwp;
+    X.patch = ppat;
+    X.m = m;
+    X.c = st.cT;
+    X.scale = st.scale;
+    X.infm = st.infm;
+    for (int b = tid; b < kBins; b += kThreads) KS.fb.ghist[b] = 0;
+    if (tid == 0) {
+        KS.fb.ccount = 0;
+        KS.fb.flags = 0;
+    }
+    __syncthreads();
+    const uint32_t Km = fkey(m);
+    uint32_t err = st.err;
+    Surv K{-INFINITY, INT_MAX};
+    if (md.topk_on) {
+        K = select_topk(X, P.top_k, Km, err);
+        st.kap_k = (K.zt == -INFINITY && K.ge_form()) ? 0u : fkey(K.zt);
+        st.iot_k = K.ge_form() ? a.V : K.iota;
+    }
+    Surv R = K;
+    bool wsum_is_R = false;
+    if (md.topp_on) {
+        // below zb the whole row holds at most (1 - p) / 2 of the top mass
+        if (tid == 0)
+            SS.bf[2] = __double2float_rd(static_cast<double>(m) +
+                                         static_cast<double>(T) * log((1.0 - static_cast<double>(P.top_p)) /
+                                                                      (2.0 * static_cast<double>(a.V))));
+        __syncthreads();
+        const float zb = SS.bf[2];
+        const float zfloor = fmaxf(zm, K.zt);
+        float zlo = fmaxf(zb, zfloor);
+        Window W = Ctx::make_window(fkey(zlo), Km);
+        const int mk = mass_mode(X, K);
+        if (md.topk_on) {
+            pass_mass<Ctx, true>(X, mk, K, W);
+            X.publish_wsum_total(0);
+            X.push_hist();
+            X.xsync();
+            st.mass_k = X.xscan(0, ~0ull).total;
+            X.xnext();
+        } else {
+            // K is every id: its mass is the chunk tables' total
+            pass_hist<Ctx, true>(X, W, K);
+            X.push_hist();
+            X.xsync();
+            st.mass_k = st.S_all;
+        }
+        if (tid == 0) SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(st.mass_k)));
+        __syncthreads();
+        uint64_t tgt = SS.bu[5];
+        if (tgt == 0) tgt = 1;
+        float zp = -INFINITY;
+        bool found = select_mass(X, W, K, tgt, zp);
+        if (!found && zlo > zfloor) {
+            zlo = zfloor;
+            W = Ctx::make_window(fkey(zlo), Km);
+            pass_hist<Ctx, true>(X, W, K);
+            X.push_hist();
+            X.xsync();
+            found = select_mass(X, W, K, tgt, zp);
+        }
+        const float zx = found ? fmaxf(zp, zm) : zm;
+        if (zx > K.zt)
+            R = Surv{zx, INT_MAX};
+        else
+            wsum_is_R = md.topk_on;  // Wsum holds K's masses only when top-k ran
+    } else if (md.minp_on && zm > K.zt) {
+        R = Surv{zm, INT_MAX};
+    }
+    st.kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
+    st.iot_r = R.ge_form() ? a.V : R.iota;
+    const int mr = mass_mode(X, R);
+    if (!wsum_is_R) pass_mass<Ctx, false>(X, mr, R, Window{0u, 0u, 0});
+    X.publish_wsum_total(0);
+    X.xsync();
+    st.mass_r = X.xscan(0, ~0ull).total;
+    st.target = scale_by_u(st.rbits, st.mass_r);
+    X.xnext();
+    int tok = X.walk(
+        st.target, [&](const float(&z)[VEC], int g0) { return X.vec_mass(mr, z, g0, R); },
+        [&](const float(&z)[VEC], int g0, uint64_t tt) { return X.vec_mass_walk(mr, z, g0, R, tt); });
+    if (tok < 0) {
+        tok = st.am;
+        err |= kErrInternal;
+    }
+    st.token = tok;
+    st.passes = 1 + X.passes;
+    st.err = err;
+}
+
+// One CTA per row.
+template <int DT, bool HIST>
+__global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a) {
     using E = Elem<DT>;
     using Ctx = RowCtx<DT, HIST>;
     constexpr int VEC = E::kVec;
@@ -598,32 +804,41 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
     const int s = a.s;
     const int nch = s * kChunks;
     const char* rowp = static_cast<const char*>(a.logits) + static_cast<int64_t>(row) * a.ld * E::kBytes;
+    float* cm = reinterpret_cast<float*>(dyn + a.cmax_off);
+    float* cs = reinterpret_cast<float*>(dyn + a.cs_off);
     const arc_row_params P = load_params(a.params + row);
-    uint32_t rerr = param_errors(P);
-    const RowMode md(P, a.V);
-    const bool greedy = md.greedy, filtered = md.filtered, need_mass = md.need_mass;
-    const bool topk_on = md.topk_on, topp_on = md.topp_on, minp_on = md.minp_on;
-    const float T = P.temperature;
-    const int k = P.top_k;
-    const float cT = greedy ? 0.0f : __fdiv_rn(1.4426950408889634f, T);
     int hn = 0, hbeg = 0;
     if (HIST && a.hist_off != nullptr) {
         hbeg = a.hist_off[row];
         hn = max(0, a.hist_off[row + 1] - hbeg);
     }
-    float* cm = reinterpret_cast<float*>(dyn + a.cmax_off);
-    float* cs = reinterpret_cast<float*>(dyn + a.cs_off);
 
-    // slice headers (warp 0) and, for sampled rows, the chunk tables (warps
-    // 0-6); meanwhile one thread of warp 7 takes T ln(min_p) in fp64, whose
-    // rate on this part is a small fraction of fp32
-    const bool minp_row = minp_on && filtered && rerr == 0;
-    if (minp_row && tid == kThreads - 32)
-        SS.bd[0] = static_cast<double>(T) * log(static_cast<double>(P.min_p));
-    if (!greedy && tid < kThreads - 32) {
+    // the slice headers (warp 0) and the chunk tables (warps 1-7) load while
+    // the parameters do: nothing here waits for them
+    if (warp == 0) {
+        float v = -INFINITY;
+        int i = -1;
+        uint32_t f = 0;
+        double tl = 0.0;
+        for (int c = lane; c < s; c += 32) {
+            const SliceHeader* h = reinterpret_cast<const SliceHeader*>(summary_at(a.summaries, s, row, c));
+            better(v, i, h->m, h->am);
+            f |= h->flags;
+            if (c == 0) tl = h->tlnp;
+        }
+        warp_argmax(v, i);
+        f = __reduce_or_sync(0xFFFFFFFFu, f);
+        if (lane == 0) {
+            SS.bf[0] = v;
+            SS.bi[0] = i;
+            SS.bi[1] = static_cast<int>(f);
+            // min-p: the smallest float z with z - m >= T ln(min_p)
+            SS.bf[1] = __double2float_ru(static_cast<double>(v) + tl);
+        }
+    } else {
         constexpr int kLd = 4;  // chunk entries in flight per thread
         constexpr int kStride = kThreads - 32;
-        for (int g0 = tid; g0 < nch; g0 += kLd * kStride) {
+        for (int g0 = tid - 32; g0 < nch; g0 += kLd * kStride) {
             float2 e[kLd];
 #pragma unroll
             for (int u = 0; u < kLd; ++u) {
@@ -641,50 +856,45 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
             }
         }
     }
-    if (warp == 0) {
-        float v = -INFINITY;
-        int i = -1;
-        uint32_t f = 0;
-        for (int c = lane; c < s; c += 32) {
-            const SliceHeader* h = reinterpret_cast<const SliceHeader*>(summary_at(a.summaries, s, row, c));
-            better(v, i, h->m, h->am);
-            f |= h->flags;
-        }
-        warp_argmax(v, i);
-        f = __reduce_or_sync(0xFFFFFFFFu, f);
-        if (lane == 0) {
-            SS.bf[0] = v;
-            SS.bi[0] = i;
-            SS.bi[1] = static_cast<int>(f);
-        }
-    }
+    uint32_t rerr = param_errors(P);
+    const RowMode md(P, a.V);
+    const float T = P.temperature;
+    const int k = P.top_k;
     __syncthreads();
-    const float m = SS.bf[0];
-    const int am = SS.bi[0];
+
+    RowState st;
+    st.m = SS.bf[0];
+    st.am = SS.bi[0];
     const uint32_t rflags = static_cast<uint32_t>(SS.bi[1]);
-    const bool row_nan = (rflags & ARC_ERR_NAN) != 0;
+    st.row_nan = (rflags & ARC_ERR_NAN) != 0;
+    st.cT = md.greedy ? 0.0f : __fdiv_rn(1.4426950408889634f, T);
+    st.scale = __uint_as_float(static_cast<uint32_t>(127 + a.F) << 23);
+    st.infm = (st.m == INFINITY);
+    st.zm = md.minp_on ? SS.bf[1] : -INFINITY;
+    st.rbits = 0;
+    st.S_all = 0;
+    st.kap_k = st.kap_r = 0;
+    st.iot_k = st.iot_r = a.V;
+    st.mass_k = st.mass_r = st.target = 0;
+    st.passes = 1;
     rerr |= rflags & (ARC_ERR_HIST_ID | ARC_ERR_HIST_CAP | ARC_ERR_TIMEOUT);
-    uint32_t err = rerr | (rflags & ARC_ERR_NAN);
+    st.err = rerr | (rflags & ARC_ERR_NAN);
     int mode;
-    int token = -2;
+    st.token = -2;
     if (rerr != 0) {
         mode = -1;
-        token = -1;
+        st.token = -1;
     } else {
-        mode = greedy ? 0 : (filtered ? 2 : 1);
-        if (am < 0) {
-            token = 0;
-            err |= ARC_ERR_DEGENERATE;
-        } else if (greedy) {
-            token = am;
+        mode = md.greedy ? 0 : (md.filtered ? 2 : 1);
+        if (st.am < 0) {
+            st.token = 0;
+            st.err |= ARC_ERR_DEGENERATE;
+        } else if (md.greedy) {
+            st.token = st.am;
         }
     }
-    uint32_t kap_k = 0, kap_r = 0;
-    int iot_k = a.V, iot_r = a.V;
-    uint64_t mass_k = 0, mass_r = 0, target = 0, rbits = 0;
-    int passes = 1;
-    const float scale = __uint_as_float(static_cast<uint32_t>(127 + a.F) << 23);
-    auto fixq = [&](float w) { return __float2ull_rn(__fmul_rn(w, scale)); };
+    const float m = st.m, cT = st.cT;
+    auto fixq = [&](float w) { return __float2ull_rn(__fmul_rn(w, st.scale)); };
     // a chunk's fixed-point mass, rescaled from its own max to the row max
     auto chunk_q = [&](int e) -> uint64_t {
         const float mj = cm[e], Sj = cs[e];
@@ -694,23 +904,24 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
     const int cper = (nch + kThreads - 1) / kThreads;  // chunk entries per thread, in id order
     const int ce0 = min(nch, tid * cper), ce1 = min(nch, ce0 + cper);
 
-    if (token == -2) {
-        rbits = splitmix64(P.seed ^ (static_cast<uint64_t>(row) << 32) ^ P.step) >> 11;
+    if (st.token == -2) {
+        st.rbits = splitmix64(P.seed ^ (static_cast<uint64_t>(row) << 32) ^ P.step) >> 11;
         if (mode == 1) {
+            // ---------------------------------------------------------- default rows
             // total mass and the chunk that holds the draw, in one block scan
             uint64_t loc = 0;
             for (int e = ce0; e < ce1; ++e) loc += chunk_q(e);
             if (tid == 0) SS.bi[2] = -1;
             uint64_t total;
             const uint64_t incl = block_scan_u64(loc, SS.redu, total);
-            mass_r = total;
-            target = scale_by_u(rbits, total);
+            st.mass_r = total;
+            st.target = scale_by_u(st.rbits, total);
             const uint64_t before = incl - loc;
-            if (before <= target && target < incl) {
+            if (before <= st.target && st.target < incl) {
                 uint64_t run = before;
                 for (int e = ce0; e < ce1; ++e) {
                     const uint64_t q = chunk_q(e);
-                    if (q > 0 && run + q > target) {
+                    if (q > 0 && run + q > st.target) {
                         SS.bi[2] = e;
                         SS.bu[2] = run;
                         break;
@@ -722,8 +933,8 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
             const int hit = SS.bi[2];
             const uint64_t hit_before = SS.bu[2];
             if (hit < 0) {
-                err |= kErrInternal;
-                token = am;
+                st.err |= kErrInternal;
+                st.token = st.am;
             } else if (warp == 0) {
                 // re-read the chunk (32 vectors) and walk it
                 const int c = hit / kChunks, jr = hit % kChunks;
@@ -779,10 +990,9 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
                 const uint64_t f = fixq(__fmul_rn(ls, r));
                 const uint64_t inc = warp_inclusive_u64(f);
                 const uint64_t Q = shfl_u64(inc, 31);
-                uint64_t tres = target - hit_before;
-                if (Q == 0) {
-                    token = -3;  // no lane carries mass: take the row's first max below
-                } else {
+                uint64_t tres = st.target - hit_before;
+                int token = -3;  // no lane carries mass: take the row's first max below
+                if (Q != 0) {
                     if (tres >= Q) tres = Q - 1;  // rounding gap between the chunk total and its lanes
                     const unsigned bal = __ballot_sync(0xFFFFFFFFu, inc > tres);
                     const int l = __ffs(bal) - 1;
@@ -806,21 +1016,15 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
                 if (lane == 0) SS.bi[3] = token;
             }
             __syncthreads();
-            if (hit >= 0) token = SS.bi[3];
-            if (token == -3) token = am;
+            if (hit >= 0) st.token = SS.bi[3];
+            if (st.token == -3) st.token = st.am;
         } else {
             // ---------------------------------------------------------- filtered rows
-            float zm = -INFINITY;  // min-p: z >= zm survives
-            if (minp_on) {
-                if (tid == 0) SS.bf[1] = __double2float_ru(static_cast<double>(m) + SS.bd[0]);
-                __syncthreads();
-                zm = SS.bf[1];
-            }
-            uint64_t S_all = 0;  // top-p over every id: the chunk tables' total mass
-            if (need_mass) {
+            const float zm = st.zm;
+            if (md.need_mass) {  // top-p over every id: the chunk tables' total mass
                 uint64_t loc = 0;
                 for (int e = ce0; e < ce1; ++e) loc += chunk_q(e);
-                S_all = block_sum_u64(loc, SS.redu);
+                st.S_all = block_sum_u64(loc, SS.redu);
             }
             // history patches of the whole row (both selection paths read them)
             const uint32_t* pbm = nullptr;
@@ -834,11 +1038,10 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
                 uint32_t* cnt = wp + nwords_max;
                 float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
                 __syncthreads();
-                if (tid == 0) KS.st.bi[7] = 0;
+                if (tid == 0) SS.bi[7] = 0;
                 const int nv_row = (a.V + VEC - 1) / VEC;
                 const int distinct = build_patches<DT>(rowp, a.V, 0, a.V, nv_row, P, a.hist_ids + hbeg, hn, bm, wp,
-                                                       cnt, pat, SS.red32,
-                                                       reinterpret_cast<uint32_t*>(&KS.st.bi[7]));
+                                                       cnt, pat, SS.red32, reinterpret_cast<uint32_t*>(&SS.bi[7]));
                 pbm = bm;
                 pwp = wp;
                 ppat = pat;
@@ -846,135 +1049,131 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
             }
 
             // floor zf: every survivor has z >= zf
-            bool fast = true;
             float zf = -INFINITY;
-            if (topk_on) {
-                // every chunk holds an id >= its max, so k chunk maxima >= x
-                // put the k-th largest logit at or above x
-                uint32_t edge = 0;
-                fast = floor_select(
-                    nch,
-                    [&](int e, uint32_t& key, uint32_t& w) {
+            bool fast = true;
+            if (md.topk_on || !md.minp_on) {
+                uint32_t tgt;
+                int sh = 0;
+                if (md.topk_on) {
+                    // every chunk holds an id >= its max, so k chunk maxima >= x put
+                    // the k-th largest logit at or above x
+                    tgt = static_cast<uint32_t>(k);
+                } else {
+                    // top-p alone: the chunk maxima at or above x already carry at
+                    // least the target mass (masses in units of 2^sh rounded down,
+                    // the target rounded up: the bound holds and sums fit in 32 bits)
+                    if (tid == 0)
+                        SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(st.S_all)));
+                    __syncthreads();
+                    const uint64_t t64 = max(SS.bu[5], uint64_t{1});
+                    sh = max(0, a.F - 19);
+                    tgt = static_cast<uint32_t>((t64 + (uint64_t{1} << sh) - 1) >> sh);
+                }
+                auto wt = [&](float x) -> uint32_t {
+                    return !(x > -INFINITY) ? 0u
+                                            : (md.topk_on ? 1u : static_cast<uint32_t>(fixq(wrel(x, m, cT)) >> sh));
+                };
+                fast = isfinite(m) &&
+                       floor_hist(nch, [&](int e, float& x, uint32_t& w) { x = cm[e]; w = wt(x); }, m, tgt,
+                                  reinterpret_cast<uint32_t*>(KS.fb.lhist), SS, zf);
+                if (!fast) {
+                    auto kw = [&](int e, uint32_t& key, uint32_t& w) {
                         const float x = cm[e];
                         key = fkey(x);
-                        w = (x > -INFINITY) ? 1u : 0u;
-                    },
-                    static_cast<uint32_t>(k), KS.fhist, SS, edge);
-                if (fast) zf = Ctx::lo_float(edge);
-            } else if (minp_on) {
-                zf = zm;
+                        w = wt(x);
+                    };
+                    uint32_t edge = 0;
+                    fast = (nch <= 2 * kThreads) ? floor_block<2>(nch, kw, tgt, SS, edge)
+                                                 : floor_block<kMaxRowCtas * kChunks / kThreads>(nch, kw, tgt, SS, edge);
+                    if (fast) zf = Ctx::lo_float(edge);
+                }
             } else {
-                // top-p alone: the chunk maxima at or above x already carry
-                // at least the target mass
-                if (tid == 0) SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(S_all)));
-                __syncthreads();
-                uint64_t tgt = SS.bu[5];
-                if (tgt == 0) tgt = 1;
-                // masses in units of 2^sh rounded down, the target rounded up:
-                // the bound stays valid and every sum fits in 32 bits
-                const int sh = max(0, a.F - 19);
-                const uint32_t tgt32 = static_cast<uint32_t>((tgt + (uint64_t{1} << sh) - 1) >> sh);
-                uint32_t edge = 0;
-                fast = floor_select(
-                    nch,
-                    [&](int e, uint32_t& key, uint32_t& w) {
-                        const float x = cm[e];
-                        key = fkey(x);
-                        w = (x > -INFINITY) ? static_cast<uint32_t>(fixq(wrel(x, m, cT)) >> sh) : 0u;
-                    },
-                    tgt32, KS.fhist, SS, edge);
-                if (fast) zf = Ctx::lo_float(edge);
+                zf = zm;
             }
             fast = fast && zf > -INFINITY;
+            if (tid == 0) SS.ccount = 0;
+            __syncthreads();
 
-            // candidate chunks: max >= zf, in id order
-            int* clist = reinterpret_cast<int*>(dyn + a.clist_off);
-            int nclist = 0;
-            if (fast) {
-                uint64_t loc = 0;
-                for (int e = ce0; e < ce1; ++e) loc += (cm[e] >= zf) ? 1u : 0u;
-                uint64_t total;
-                const uint64_t incl = block_scan_u64(loc, SS.redu, total);
-                int pos = static_cast<int>(incl - loc);
-                for (int e = ce0; e < ce1; ++e)
-                    if (cm[e] >= zf) clist[pos++] = e;
-                nclist = static_cast<int>(total);
-                fast = nclist <= kCandChunks;
-                __syncthreads();
-            }
-
-            // gather the ids >= zf of those chunks, in id order: (key, id, mass)
-            uint32_t* ck = reinterpret_cast<uint32_t*>(dyn + a.cand_off);
-            int* ci = reinterpret_cast<int*>(ck + kCandCap);
-            uint64_t* cw = reinterpret_cast<uint64_t*>(ci + kCandCap);
-            const bool infm = (m == INFINITY);
+            // gather the ids >= zf as (key, id, mass): warp w takes the chunks w,
+            // w + 8, ... whose max is >= zf, stages up to kCollectU of them at a
+            // time in shared memory with 16-byte asynchronous copies (all in
+            // flight together); the ids found take slots from one counter, one
+            // atomic per warp and element position
+            // candidates as one 64-bit value: key << 32 | (2^32 - 1 - id), so
+            // that a larger value ranks first by (z desc, id asc)
+            uint64_t* cc = reinterpret_cast<uint64_t*>(dyn + a.cand_off);
             auto weight_of = [&](float z) -> float {
-                return infm ? (z == m ? 1.0f : 0.0f) : ex2(__fmul_rn(__fsub_rn(z, m), cT));
+                return st.infm ? (z == m ? 1.0f : 0.0f) : ex2(__fmul_rn(__fsub_rn(z, m), cT));
             };
             int nc = 0;
             if (fast) {
-                // warp w takes list entries w, w + 8, ...; kCollectU of its chunks'
-                // 16-byte vectors are in flight per lane; slots come from one counter
                 const int Lv = a.L / VEC;
-                if (tid == 0) SS.ccount = 0;
-                __syncthreads();
-                for (int r0 = warp; r0 < nclist; r0 += kWarps * kCollectU) {
-                    uint4 raw[kCollectU];
-                    int vrow[kCollectU];
+                uint4* stage = reinterpret_cast<uint4*>(dyn + a.stage_off) + warp * (kCollectU * 32);
+                int* wl = reinterpret_cast<int*>(dyn + a.clist_off) + warp * ((nch + kWarps - 1) / kWarps);
+                int nw = 0;
+                for (int b0 = warp; b0 < nch; b0 += kWarps * 32) {
+                    const int g = b0 + lane * kWarps;
+                    const unsigned hits = __ballot_sync(0xFFFFFFFFu, g < nch && cm[g] >= zf);
+                    if (hits & (1u << lane)) wl[nw + __popc(hits & ((1u << lane) - 1u))] = g;
+                    nw += __popc(hits);
+                }
+                __syncwarp();
+                const uint4 ninf = (DT == ARC_BF16) ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                                                    : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+                for (int r0 = 0; r0 < nw; r0 += kCollectU) {
+                    // every copy of the round in flight at once
 #pragma unroll
                     for (int u = 0; u < kCollectU; ++u) {
-                        const int li = r0 + u * kWarps;
-                        vrow[u] = -1;
-                        raw[u] = make_uint4(0u, 0u, 0u, 0u);
-                        if (li < nclist) {
-                            const int gi = clist[li];
-                            const int c = gi / kChunks, jj = gi % kChunks;
-                            const int vs = jj * 32 + lane;
-                            const int sa0 = c * a.L;
-                            const int sn = min(sa0 + a.L, a.V) - sa0;
-                            if (vs < (sn + VEC - 1) / VEC) {
-                                raw[u] = E::global_vec(rowp + static_cast<int64_t>(sa0) * E::kBytes, vs, sn, a.aligned);
-                                vrow[u] = c * Lv + vs;
-                            }
+                        if (r0 + u < nw) {
+                            const int g = wl[r0 + u];
+                            const int c = g / kChunks;
+                            const int vs = (g % kChunks) * 32 + lane;
+                            const int sn = min((c + 1) * a.L, a.V) - c * a.L;
+                            const char* sb = rowp + static_cast<int64_t>(c) * a.L * E::kBytes;
+                            uint4* dst = stage + u * 32 + lane;
+                            if (a.aligned && (vs + 1) * VEC <= sn)
+                                cp_async16(dst, sb + static_cast<size_t>(vs) * 16);
+                            else
+                                *dst = (vs * VEC < sn) ? E::global_vec(sb, vs, sn, false) : ninf;
                         }
                     }
-#pragma unroll
-                    for (int u = 0; u < kCollectU; ++u) {
-                        if (r0 + u * kWarps >= nclist) break;  // uniform over the warp
+                    cp_async_wait_all();
+                    __syncwarp();
+                    const int nst = min(kCollectU, nw - r0);
+                    for (int u = 0; u < nst; ++u) {
+                        const int g = wl[r0 + u];
+                        const int c = g / kChunks;
+                        const int vs = (g % kChunks) * 32 + lane;
                         float z[VEC];
+                        E::unpack(stage[u * 32 + lane], z);
+                        // padding vectors past the slice read as -inf and take no patch
+                        if (HIST && has_patch && vs * VEC < min((c + 1) * a.L, a.V) - c * a.L)
+                            apply_patches<VEC>(pbm, pwp, ppat, c * Lv + vs, z);
                         int cnt = 0;
-                        if (vrow[u] >= 0) {
-                            E::unpack(raw[u], z);
-                            if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, vrow[u], z);
 #pragma unroll
-                            for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
-                        }
+                        for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
+                        if (__ballot_sync(0xFFFFFFFFu, cnt > 0) == 0u) continue;  // uniform
                         int inc = cnt;
 #pragma unroll
                         for (int dd = 1; dd < 32; dd <<= 1) {
                             const int o = __shfl_up_sync(0xFFFFFFFFu, inc, dd);
                             if (lane >= dd) inc += o;
                         }
-                        const int tot = __shfl_sync(0xFFFFFFFFu, inc, 31);
-                        if (tot == 0) continue;
                         uint32_t base = 0;
-                        if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(tot));
+                        if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(inc));
                         base = __shfl_sync(0xFFFFFFFFu, base, 31);
-                        int pos = static_cast<int>(base) + inc - cnt;
-                        if (cnt > 0) {
+                        uint32_t pos = base + static_cast<uint32_t>(inc - cnt);
+                        const uint32_t id0 = static_cast<uint32_t>((c * Lv + vs) * VEC);
 #pragma unroll
-                            for (int e = 0; e < VEC; ++e) {
-                                if (z[e] >= zf) {
-                                    if (pos < kCandCap) {
-                                        ck[pos] = fkey(z[e]);
-                                        ci[pos] = vrow[u] * VEC + e;
-                                        cw[pos] = fixq(weight_of(z[e]));
-                                    }
-                                    ++pos;
-                                }
+                        for (int e = 0; e < VEC; ++e) {
+                            if (z[e] >= zf) {
+                                if (pos < static_cast<uint32_t>(kCandCap))
+                                    cc[pos] = (static_cast<uint64_t>(fkey(z[e])) << 32) | (0xFFFFFFFFu - (id0 + e));
+                                ++pos;
                             }
                         }
                     }
+                    __syncwarp();  // the stage is refilled next round
                 }
                 __syncthreads();
                 nc = static_cast<int>(SS.ccount);
@@ -983,240 +1182,136 @@ __global__ void __launch_bounds__(kThreads, 1) finish_kernel(const FinishArgs a)
 
             if (fast) {
                 // ------------------------------------------------------ direct selection
-                // candidates sit in gather order: ties are broken by id
-                Surv K{-INFINITY, INT_MAX};
-                if (topk_on) {
-                    // K: the first k ids by (z desc, id asc)
-                    if (tid == 0) SS.bi[5] = -1;
-                    __syncthreads();
-                    for (int i = tid; i < nc; i += kThreads) {
-                        const uint32_t ki = ck[i];
-                        const int ii = ci[i];
-                        int rk = 0;
-                        for (int j = 0; j < nc; ++j) {
-                            const uint32_t kj = ck[j];
-                            rk += (kj > ki || (kj == ki && ci[j] < ii)) ? 1 : 0;
-                        }
-                        if (rk == k - 1) SS.bi[5] = i;
-                    }
-                    __syncthreads();
-                    const int wi = SS.bi[5];
-                    if (wi < 0) {
-                        err |= kErrInternal;
-                    } else {
-                        const uint32_t kw = ck[wi];
-                        const int iw = ci[wi];
-                        int later = 0;
-                        for (int i = tid; i < nc; i += kThreads) later |= (ck[i] == kw && ci[i] > iw) ? 1 : 0;
-                        later = __syncthreads_or(later);
-                        K = Surv{key_to_float(kw), later ? iw + 1 : INT_MAX};
-                    }
-                    kap_k = (K.zt == -INFINITY && K.ge_form()) ? 0u : fkey(K.zt);
-                    iot_k = K.ge_form() ? a.V : K.iota;
-                    // ids outside K get key 0 (no real logit has it)
-                    uint64_t loc = 0;
-                    for (int i = tid; i < nc; i += kThreads) {
-                        if (!K.test(key_to_float(ck[i]), ci[i]))
-                            ck[i] = 0u;
-                        else
-                            loc += cw[i];
-                    }
-                    mass_k = block_sum_u64(loc, SS.redu);
-                } else {
-                    mass_k = S_all;
+                // rank every candidate by (key desc, id asc) into sorted arrays
+                uint32_t* sk = reinterpret_cast<uint32_t*>(dyn + a.sorted_off);
+                int* sid = reinterpret_cast<int*>(sk + kCandCap);
+                uint64_t* sm = reinterpret_cast<uint64_t*>(sid + kCandCap);
+                for (int i = tid; i < nc; i += kThreads) {
+                    const uint64_t vi = cc[i];
+                    int rk = 0;
+#pragma unroll 8
+                    for (int j = 0; j < nc; ++j) rk += (cc[j] > vi) ? 1 : 0;
+                    const uint32_t ki = static_cast<uint32_t>(vi >> 32);
+                    sk[rk] = ki;
+                    sid[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(vi));
+                    sm[rk] = fixq(weight_of(key_to_float(ki)));
                 }
+                if (tid == 0) {
+                    SS.bi[5] = -1;
+                    SS.bi[6] = -1;
+                }
+                __syncthreads();
+                // K: sorted positions [0, nk)
+                int nk = nc;
+                Surv K{-INFINITY, INT_MAX};
+                if (md.topk_on) {
+                    nk = min(k, nc);
+                    if (nk < k) st.err |= kErrInternal;  // the floor guarantees k ids
+                    const bool later = nk < nc && sk[nk] == sk[nk - 1];
+                    K = Surv{key_to_float(sk[nk - 1]), later ? sid[nk - 1] + 1 : INT_MAX};
+                    st.kap_k = fkey(K.zt);
+                    st.iot_k = K.ge_form() ? a.V : K.iota;
+                }
+                // thread t holds sorted positions [4t, 4t + 4)
+                const int p0 = 4 * tid;
+                uint64_t lk = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) lk += (p0 + q < nk) ? sm[p0 + q] : 0u;
+                uint64_t tot_k;
+                const uint64_t inc_k = block_scan_u64(lk, SS.redu, tot_k);
+                st.mass_k = md.topk_on ? tot_k : st.S_all;
                 bool found = false;
                 float zp = -INFINITY;
-                if (topp_on) {
-                    // largest key whose mass at or above it reaches ceil(p * mass_k)
-                    if (tid == 0) SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(mass_k)));
+                if (md.topp_on) {
+                    // first sorted position whose running mass reaches ceil(p * mass_k)
+                    if (tid == 0)
+                        SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(st.mass_k)));
                     __syncthreads();
-                    uint64_t tgt = SS.bu[5];
-                    if (tgt == 0) tgt = 1;
-                    uint32_t best = 0;
-                    for (int i = tid; i < nc; i += kThreads) {
-                        const uint32_t ki = ck[i];
-                        if (ki == 0u) continue;
-                        uint64_t mge = 0;
-                        for (int j = 0; j < nc; ++j) mge += (ck[j] >= ki) ? cw[j] : 0u;
-                        if (mge >= tgt) best = max(best, ki);
+                    const uint64_t tgt = max(SS.bu[5], uint64_t{1});
+                    uint64_t run = inc_k - lk;
+                    if (run < tgt && inc_k >= tgt) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint64_t mq = (p0 + q < nk) ? sm[p0 + q] : 0u;
+                            if (mq != 0 && run < tgt && run + mq >= tgt) SS.bi[5] = p0 + q;
+                            run += mq;
+                        }
                     }
-                    best = block_max_u32(best, SS.red32);
-                    found = best != 0u;
-                    if (found) zp = key_to_float(best);
+                    __syncthreads();
+                    if (SS.bi[5] >= 0) {
+                        found = true;
+                        zp = key_to_float(sk[SS.bi[5]]);
+                    }
+                    if (!found && !md.minp_on && !md.topk_on) st.err |= kErrInternal;  // the floor guarantees it
                 }
-                if (topp_on && !found && !minp_on && !topk_on) err |= kErrInternal;  // the floor guarantees it
                 const float zx = found ? fmaxf(zp, zm) : zm;
                 const Surv R = (zx > K.zt) ? Surv{zx, INT_MAX} : K;
-                kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
-                iot_r = R.ge_form() ? a.V : R.iota;
-                // survivors' mass, then the draw in id order: each survivor sums
-                // the survivors with smaller ids
-                auto surv_q = [&](int i) -> uint64_t {
-                    const uint32_t ki = ck[i];
-                    return (ki != 0u && R.test(key_to_float(ki), ci[i])) ? cw[i] : 0u;
-                };
-                uint64_t loc = 0;
-                for (int i = tid; i < nc; i += kThreads) loc += surv_q(i);
-                if (tid == 0) SS.bi[6] = -1;
-                mass_r = block_sum_u64(loc, SS.redu);
-                target = scale_by_u(rbits, mass_r);
-                for (int i = tid; i < nc; i += kThreads) {
-                    const uint64_t qi = surv_q(i);
-                    if (qi == 0) continue;
-                    const int ii = ci[i];
+                st.kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
+                st.iot_r = R.ge_form() ? a.V : R.iota;
+                // survivors: a prefix [0, ns) of the sorted order
+                uint64_t lr = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int pp = p0 + q;
+                    if (pp < nk && R.test(key_to_float(sk[pp]), sid[pp])) lr += sm[pp];
+                }
+                st.mass_r = block_sum_u64(lr, SS.redu);
+                st.target = scale_by_u(st.rbits, st.mass_r);
+                int nsv = 0;
+                {
+                    // ns: survivors are the first positions of the sorted order
+                    int first_out = nk;
+#pragma unroll
+                    for (int q = 3; q >= 0; --q) {
+                        const int pp = p0 + q;
+                        if (pp < nk && !R.test(key_to_float(sk[pp]), sid[pp])) first_out = pp;
+                    }
+                    nsv = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, static_cast<unsigned>(first_out)));
+                    if (lane == 0) SS.fc[0][warp][3] = static_cast<uint32_t>(nsv);
+                    __syncthreads();
+                    for (int v = 0; v < kWarps; ++v) nsv = min(nsv, static_cast<int>(SS.fc[0][v][3]));
+                }
+                // the draw in id order: each survivor sums the survivors with smaller ids
+                for (int pp = tid; pp < nsv; pp += kThreads) {
+                    const int ip = sid[pp];
+                    const uint64_t mp = sm[pp];
                     uint64_t before = 0;
-                    for (int j = 0; j < nc; ++j) before += (ci[j] < ii) ? surv_q(j) : 0u;
-                    if (before <= target && target < before + qi) SS.bi[6] = ii;
+#pragma unroll 8
+                    for (int qq = 0; qq < nsv; ++qq) before += (sid[qq] < ip) ? sm[qq] : 0u;
+                    if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
                 }
                 __syncthreads();
-                token = SS.bi[6];
-                if (token < 0) {
-                    token = am;
-                    err |= kErrInternal;
+                st.token = SS.bi[6];
+                if (st.token < 0) {
+                    st.token = st.am;
+                    st.err |= kErrInternal;
                 }
             } else {
-                // ------------------------------------------------------ general path
-                __syncthreads();
-                cg::cluster_group cl = cg::this_cluster();
-                Ctx X(KS.fb, cl);
-                X.s = 1;
-                X.rank = 0;
-                X.row = row;
-                X.tid = tid;
-                X.lane = lane;
-                X.warp = warp;
-                X.a0 = 0;
-                X.a1 = a.V;
-                X.n = a.V;
-                X.nv = (a.V + VEC - 1) / VEC;
-                X.nvf = a.V / VEC;
-                X.rounds = (X.nv + kThreads - 1) / kThreads;
-                X.data = reinterpret_cast<const unsigned char*>(rowp);
-                X.src_global = true;
-                X.src_aligned = a.aligned != 0;
-                X.vmax = cm;
-                X.vps = a.L / VEC;
-                X.cps = kChunks;
-                X.Wsum = reinterpret_cast<uint64_t*>(dyn + a.fb_wsum_off);
-                X.par = 0;
-                X.passes = 0;
-                X.epoch = 1;
-                X.ghist_zeroed = -1;
-                X.cand_zeroed = -1;
-                X.has_patch = has_patch;
-                X.row_nan = row_nan;
-                X.bm = pbm;
-                X.wp = pwp;
-                X.patch = ppat;
-                X.m = m;
-                X.c = cT;
-                X.scale = scale;
-                X.infm = infm;
-                for (int b = tid; b < kBins; b += kThreads) KS.fb.ghist[b] = 0;
-                if (tid == 0) {
-                    KS.fb.ccount = 0;
-                    KS.fb.flags = 0;
-                }
-                __syncthreads();
-                const uint32_t Km = fkey(m);
-                Surv K{-INFINITY, INT_MAX};
-                if (topk_on) {
-                    K = select_topk(X, k, Km, err);
-                    kap_k = (K.zt == -INFINITY && K.ge_form()) ? 0u : fkey(K.zt);
-                    iot_k = K.ge_form() ? a.V : K.iota;
-                }
-                Surv R = K;
-                bool wsum_is_R = false;
-                if (topp_on) {
-                    if (tid == 0)
-                        SS.bf[2] = __double2float_rd(static_cast<double>(m) +
-                                                     static_cast<double>(T) * log((1.0 - static_cast<double>(P.top_p)) /
-                                                                                  (2.0 * static_cast<double>(a.V))));
-                    __syncthreads();
-                    const float zb = SS.bf[2];
-                    const float zfloor = fmaxf(zm, K.zt);
-                    float zlo = fmaxf(zb, zfloor);
-                    Window W = Ctx::make_window(fkey(zlo), Km);
-                    const int mk = mass_mode(X, K);
-                    if (topk_on) {
-                        pass_mass<Ctx, true>(X, mk, K, W);
-                        X.publish_wsum_total(0);
-                        X.push_hist();
-                        X.xsync();
-                        mass_k = X.xscan(0, ~0ull).total;
-                        X.xnext();
-                    } else {
-                        // K is every id: its mass is the chunk tables' total
-                        pass_hist<Ctx, true>(X, W, K);
-                        X.push_hist();
-                        X.xsync();
-                        mass_k = S_all;
-                    }
-                    if (tid == 0) SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(mass_k)));
-                    __syncthreads();
-                    uint64_t tgt = SS.bu[5];
-                    if (tgt == 0) tgt = 1;
-                    float zp = -INFINITY;
-                    bool found = select_mass(X, W, K, tgt, zp);
-                    if (!found && zlo > zfloor) {
-                        zlo = zfloor;
-                        W = Ctx::make_window(fkey(zlo), Km);
-                        pass_hist<Ctx, true>(X, W, K);
-                        X.push_hist();
-                        X.xsync();
-                        found = select_mass(X, W, K, tgt, zp);
-                    }
-                    const float zx = found ? fmaxf(zp, zm) : zm;
-                    if (zx > K.zt)
-                        R = Surv{zx, INT_MAX};
-                    else
-                        wsum_is_R = topk_on;  // Wsum holds K's masses only when top-k ran
-                } else if (minp_on && zm > K.zt) {
-                    R = Surv{zm, INT_MAX};
-                }
-                kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
-                iot_r = R.ge_form() ? a.V : R.iota;
-                const int mr = mass_mode(X, R);
-                if (!wsum_is_R) pass_mass<Ctx, false>(X, mr, R, Window{0u, 0u, 0});
-                X.publish_wsum_total(0);
-                X.xsync();
-                mass_r = X.xscan(0, ~0ull).total;
-                target = scale_by_u(rbits, mass_r);
-                X.xnext();
-                int tok = X.walk(
-                    target, [&](const float(&z)[VEC], int g0) { return X.vec_mass(mr, z, g0, R); },
-                    [&](const float(&z)[VEC], int g0, uint64_t tt) { return X.vec_mass_walk(mr, z, g0, R, tt); });
-                if (tok < 0) {
-                    tok = am;
-                    err |= kErrInternal;
-                }
-                token = tok;
-                passes = 1 + X.passes;
+                finish_general<DT, HIST>(a, P, md, row, rowp, cm, pbm, pwp, ppat, has_patch, KS, dyn, st);
             }
         }
     }
 
     // -------------------------------------------------------------- results
     if (tid == 0) {
-        a.out[row] = token;
-        if (err != 0 && a.err_word) atomicOr(a.err_word, err);
+        a.out[row] = st.token;
+        if (st.err != 0 && a.err_word) atomicOr(a.err_word, st.err);
         if (a.debug) {
             arc_row_debug& dbg = a.debug[row];
             dbg.mode = mode;
-            dbg.err = err;
-            dbg.token = token;
-            dbg.passes = passes;
-            dbg.kappa_k = kap_k;
-            dbg.iota_k = iot_k;
-            dbg.kappa_r = kap_r;
-            dbg.iota_r = iot_r;
+            dbg.err = st.err;
+            dbg.token = st.token;
+            dbg.passes = st.passes;
+            dbg.kappa_k = st.kap_k;
+            dbg.iota_k = st.iot_k;
+            dbg.kappa_r = st.kap_r;
+            dbg.iota_r = st.iot_r;
             dbg.max_z = m;
             dbg.frac_bits = a.F;
-            dbg.rbits = rbits;
-            dbg.mass_k = mass_k;
-            dbg.mass_r = mass_r;
-            dbg.target = target;
+            dbg.rbits = st.rbits;
+            dbg.mass_k = st.mass_k;
+            dbg.mass_r = st.mass_r;
+            dbg.target = st.target;
         }
         if (a.flags & ARC_OPT_STEP_AUTOINC) a.params[row].step = P.step + 1;
     }
