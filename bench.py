@@ -31,7 +31,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sampled rows/s and achieved HBM GB/s (% of GB300 roofline) at B=256, V=129,280"
 NBUF = 6  # input copies cycled per step: 6 x 66 MB > L2
-PROFILE = os.path.join(ROOT, "profiles", "sample_kernel_mixed_quarters_B256.md")
+PROFILE = os.path.join(ROOT, "profiles", "scan_finish_mixed_quarters_B256.md")
+KERNELS_PER_STEP = 2  # scan_kernel + finish_kernel
 KERNEL_SOURCES = ["arc_sample.cu", "stream_kernel.cuh", "row_select.cuh", "arc_device.cuh"]
 
 
@@ -52,7 +53,8 @@ def measured_peaks() -> dict:
 
 
 def profiled_traffic():
-    """dram bytes per launch from the committed ncu summary, if it matches the current kernel."""
+    """dram bytes of one step (both kernels) from the committed ncu summary, if it
+    matches the current kernel sources."""
     try:
         text = open(PROFILE).read()
     except OSError:
@@ -321,12 +323,14 @@ def bench_gpu(args) -> None:
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": profiled_traffic(),
                          "peak_source": peak_src, "alg_bytes_per_launch": alg_bytes,
+                         "scope": "one step: scan_kernel (reads every logit once) + finish_kernel, "
+                                  "timed together with CUDA events on the launch stream",
                          "frac_of_nominal_8tbs": achieved / 8000.0},
             "e2e": {"value": e2e_value, "unit": "rows/s",
                     "h2d_bytes_per_step": int(host_logits.numel() * host_logits.element_size()
                                               + host_params.numel()),
                     "d2h_bytes_per_step": int(B * 4)},
-            "gpu_launches": args.steps,
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
             "clocks": clk,
         }
         if ws == 1 and not args.no_cpu_baseline:
