@@ -1,6 +1,6 @@
-// Device primitives for the sm_103a sampler: bulk-copy (TMA) loads with
-// mbarriers and bounded waits, order-preserving float keys, the Splitmix64
-// generator, fixed-point masses and warp/cluster reductions.
+// Device primitives for the sm_103a sampler: 16-byte global loads and
+// asynchronous global -> shared copies, order-preserving float keys, the
+// Splitmix64 generator, fixed-point scaling and warp reductions.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -19,36 +19,10 @@ constexpr int kBins = 512;                 // histogram bins per select pass
 constexpr int kBinBits = 9;
 constexpr int kCand = 256;                 // crossing-bin candidates gathered per row
 constexpr int kMaxCluster = 16;
-constexpr int kPieces = 4;                 // bulk copies per slice
-constexpr unsigned long long kWaitNs = 200ull * 1000ull * 1000ull;  // 200 ms wait bound
 
 // ------------------------------------------------------------------ PTX
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-// Bulk global -> shared copy completing on `bar` (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
 }
 
 // 16-byte asynchronous global -> shared copy (both 16-byte aligned), cached
@@ -57,45 +31,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// try_wait that lets the hardware suspend the thread for up to `ns` nanoseconds
-// while the phase is incomplete (no busy polling).
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for phase `parity` of `bar`; gives up after kWaitNs of wall time.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity, 1000000u)) return true;
-    const unsigned long long t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity, 1000000u)) return true;
-        if (global_ns() - t0 > kWaitNs) return false;
-    }
-}
-
-// Split cluster barrier: arrive after this CTA's last read of another CTA's
-// shared memory, wait before leaving.
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 // IEEE max that propagates NaN (max.NaN, sm_80+).
 __device__ __forceinline__ float fmax_nan(float a, float b) {
@@ -168,12 +103,6 @@ struct Elem<ARC_F32> {
     __device__ __forceinline__ static float load_scalar(const void* row, int64_t i) {
         return __ldg(reinterpret_cast<const float*>(row) + i);
     }
-    __device__ __forceinline__ static float from_smem(const void* base, int i) {
-        return reinterpret_cast<const float*>(base)[i];
-    }
-    __device__ __forceinline__ static void store_smem_raw(void* base, int i, const void* row, int64_t gi) {
-        reinterpret_cast<uint32_t*>(base)[i] = __ldg(reinterpret_cast<const uint32_t*>(row) + gi);
-    }
     // vector v of a slice in global memory holding n elements; elements past
     // n read as -inf; 16-byte load when the slice start is 16-byte aligned
     __device__ __forceinline__ static uint4 global_vec(const void* base, int v, int n, bool aligned) {
@@ -215,14 +144,6 @@ struct Elem<ARC_BF16> {
     __device__ __forceinline__ static float load_scalar(const void* row, int64_t i) {
         const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
         return __uint_as_float(static_cast<uint32_t>(h) << 16);
-    }
-    __device__ __forceinline__ static float from_smem(const void* base, int i) {
-        const unsigned short h = reinterpret_cast<const unsigned short*>(base)[i];
-        return __uint_as_float(static_cast<uint32_t>(h) << 16);
-    }
-    __device__ __forceinline__ static void store_smem_raw(void* base, int i, const void* row, int64_t gi) {
-        reinterpret_cast<unsigned short*>(base)[i] =
-            __ldg(reinterpret_cast<const unsigned short*>(row) + gi);
     }
     // vector v of a slice in global memory holding n elements; elements past
     // n read as -inf; 16-byte load when the slice start is 16-byte aligned

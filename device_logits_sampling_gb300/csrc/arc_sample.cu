@@ -165,24 +165,6 @@ cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done) {
     return cudaSuccess;
 }
 
-// Resident CTAs per SM of KERNEL with `smem` bytes of dynamic shared memory
-// (cached per device and size).
-template <auto KERNEL>
-int blocks_per_sm(int dev, int smem) {
-    static std::atomic<int> cache[kMaxDevices];
-    static std::atomic<int> cache_smem[kMaxDevices];
-    if (dev >= 0 && dev < kMaxDevices && cache_smem[dev].load() == smem + 1) return cache[dev].load();
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, KERNEL, kThreads, static_cast<size_t>(smem)) != cudaSuccess ||
-        nb <= 0)
-        nb = 1;
-    if (dev >= 0 && dev < kMaxDevices) {
-        cache[dev].store(nb);
-        cache_smem[dev].store(smem + 1);
-    }
-    return nb;
-}
-
 template <class K, class A>
 cudaError_t launch_cluster(K kernel, int64_t grid, int s, int smem, cudaStream_t st, const A& args) {
     cudaLaunchConfig_t cfg;

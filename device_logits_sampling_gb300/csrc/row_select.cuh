@@ -1,26 +1,24 @@
-// Fused per-row sampling kernel: one thread-block cluster of s CTAs per row.
+// Exact selection over a row by multi-way threshold bisection: the path the
+// finish kernel falls back to when the floor from the chunk maxima admits too
+// many ids (flat or heavily tied rows, top-p alone on diffuse rows).
 //
-// Each CTA bulk-copies (TMA, cp.async.bulk) its contiguous slice of the row
-// into shared memory once; every later look at the row -- max, top-k select,
-// top-p select, masses, the inverse-CDF walk -- runs out of shared memory.
-// Pass 1 also caches each 16-byte vector's max, so later threshold passes
-// skip vectors that cannot hold a survivor without reading them.
+// The row is read from global memory (or shared memory, for a slice staged
+// there); a per-chunk (or per-vector) max table lets every pass skip the
+// chunks that cannot hold an id at or above the pass's threshold.
 //
-// CTAs of a row combine partial results through distributed shared memory
-// (DSMEM).  Every decision is computed redundantly and identically by all
-// CTAs from the same exchanged data, so control flow, and with it the
-// sequence of cluster barriers, is uniform across the cluster.
+// Thresholds are found on the order-preserving u32 key of the logit: a
+// 512-bin histogram of the keys in a window below the row max locates the bin
+// that crosses the target count (top-k) or mass (top-p); the few ids in that
+// bin are gathered and ranked exactly.  Bins that hold too many ids are
+// bisected further, 9 bits per pass; ties at a top-k boundary too many to
+// gather are resolved by an id-order count walk.
 //
-// Thresholds are found by multi-way threshold bisection on the order-
-// preserving u32 key of the logit: a 512-bin histogram of the keys in a window
-// below the row max (each CTA adds its non-zero bins into every CTA's cluster
-// histogram with DSMEM atomics; one cluster barrier) locates the bin that
-// crosses the target count (top-k) or mass (top-p); the few ids in that bin
-// are then gathered into every CTA and ranked exactly.  Bins that hold too
-// many ids are bisected further, 9 bits per pass.
+// The helpers are written for a thread-block cluster of s CTAs sharing one
+// row (partials exchanged through distributed shared memory, decisions taken
+// identically by every CTA); the finish kernel uses them with s = 1.
 //
 // Masses are fixed-point integers (units of 2^-F of the max weight), so sums
-// are exact, associative and identical in every pass, CTA and cluster size.
+// are exact, associative and identical in every pass.
 #pragma once
 
 #include <climits>
@@ -29,30 +27,7 @@
 
 namespace arc {
 
-struct SampleArgs {
-    const void* logits;
-    int64_t ld;  // row stride, elements
-    int B;
-    int V;
-    arc_row_params* params;
-    const int32_t* hist_off;
-    const int32_t* hist_ids;
-    int32_t* out;
-    uint32_t* err_word;
-    arc_row_debug* debug;
-    int L;           // slice elements per CTA (multiple of the vector width)
-    int vmax_off;    // dynamic shared memory offsets: per-vector max,
-    int wsum_off;    //   per-(round, warp) masses,
-    int hist_off_b;  //   history patch tables
-    int rounds_max;  // rounds of the largest slice
-    int hist_cap;    // history entries per row (patch table capacity)
-    int F;           // fixed-point fraction bits
-    uint32_t flags;  // ARC_OPT_*
-    int aligned;     // rows start on 16-byte boundaries: bulk copies allowed
-};
-
 struct __align__(16) SampleShared {
-    uint64_t bar[kPieces];
     uint64_t lhist[kBins];  // this CTA's histogram
     uint64_t ghist[kBins];  // the cluster's histogram (every CTA adds into it)
     uint64_t cval[kCand];   // gathered candidates: id or mass

@@ -43,16 +43,18 @@
  *
  * Threading and memory: all pointers named "device" are caller-owned device
  * memory.  The library allocates nothing and never synchronises; each call
- * enqueues one kernel on `stream` and returns.  Calls are safe inside CUDA
- * stream capture once the first call for the device has returned (the first
- * call sets per-kernel shared-memory attributes).
+ * enqueues its kernels (arc_sample_batch: a streaming scan, then a per-row
+ * finish) on `stream` and returns.  Calls are safe inside CUDA stream capture
+ * once the first call for the device has returned (the first call sets
+ * per-kernel shared-memory attributes).
  *
  * Workspace: arc_sample_batch needs a caller-owned device workspace of
- * arc_sample_workspace_bytes() bytes, 16-byte aligned and filled with zeros
- * once before its first use.  Each call leaves it zero-filled where it
- * matters (per-row counters), so it can be reused by later calls without
- * clearing.  Calls that share a workspace must be ordered (same stream, or
- * events); calls that overlap on the GPU and share a workspace race.
+ * arc_sample_workspace_bytes() bytes, 16-byte aligned.  It carries one small
+ * summary per row slice from the scan kernel to the finish kernel of the same
+ * call; every byte the finish kernel uses is written earlier in that call, so
+ * the workspace needs no initial contents and keeps nothing between calls.
+ * Calls that share a workspace must be ordered (same stream, or events);
+ * calls that overlap on the GPU and share a workspace race.
  */
 #ifndef ARC_SAMPLE_H
 #define ARC_SAMPLE_H
