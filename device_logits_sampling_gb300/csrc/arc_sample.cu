@@ -187,6 +187,12 @@ std::atomic<uint64_t> g_prep_scan[2][2];
 std::atomic<uint64_t> g_prep_fin[2][2];
 std::atomic<uint64_t> g_prep_argmax[2];
 
+// Scratch of arc_sample_batch_static, for callers that cannot allocate device
+// memory: one array per device context, created with the module; its address
+// is looked up once per device and cached here.
+__device__ __align__(256) unsigned char g_static_workspace[ARC_STATIC_WORKSPACE_BYTES];
+std::atomic<uintptr_t> g_static_workspace_addr[kMaxDevices];
+
 }  // namespace
 
 extern "C" {
@@ -331,6 +337,32 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
         e = has_hist ? go(scan_kernel<ARC_F32, true>, finish_kernel<ARC_F32, true>, g_prep_scan[0][1], g_prep_fin[0][1])
                      : go(scan_kernel<ARC_F32, false>, finish_kernel<ARC_F32, false>, g_prep_scan[0][0], g_prep_fin[0][0]);
     return e == cudaSuccess ? ARC_OK : ARC_E_CUDA;
+}
+
+int arc_sample_batch_static(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,
+                            arc_row_params* params, const int32_t* hist_offsets, const int32_t* hist_ids,
+                            int32_t* out, uint32_t* err_word, const arc_sample_options* opts, void* stream) {
+    // the host checks of arc_sample_batch, before any CUDA call
+    int rc = check_common(logits, B, V, ld, dtype, out);
+    if (rc != ARC_OK) return rc;
+    if (params == nullptr) return ARC_E_NULL;
+    if (hist_offsets != nullptr && hist_ids == nullptr) return ARC_E_NULL;
+    if (reinterpret_cast<uintptr_t>(params) % 8 != 0) return ARC_E_ALIGN;
+    rc = check_options(opts);
+    if (rc != ARC_OK) return rc;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ARC_E_CUDA;
+    uintptr_t addr = g_static_workspace_addr[dev].load(std::memory_order_acquire);
+    if (addr == 0) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) return ARC_E_CUDA;
+        addr = reinterpret_cast<uintptr_t>(p);
+        g_static_workspace_addr[dev].store(addr, std::memory_order_release);
+    }
+    // a plan that needs more than the array is refused there (ARC_E_WORKSPACE)
+    return arc_sample_batch(logits, B, V, ld, dtype, params, hist_offsets, hist_ids, out, err_word,
+                            reinterpret_cast<void*>(addr), ARC_STATIC_WORKSPACE_BYTES, opts, stream);
 }
 
 int arc_sample_greedy(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype, int32_t* out,

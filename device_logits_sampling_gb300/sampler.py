@@ -36,6 +36,7 @@ ARC_ERR_TIMEOUT = 0x20
 ARC_ERR_INTERNAL = 0x40
 
 ARC_OPT_STEP_AUTOINC = 0x1
+ARC_STATIC_WORKSPACE_BYTES = 4 << 20  # scratch compiled into the library (arc_sample_batch_static)
 
 # arc_row_debug, 72 bytes
 ROW_DEBUG_DTYPE = np.dtype(
@@ -81,6 +82,10 @@ SIGNATURES = {
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(Options), ctypes.c_void_p]),
+    "arc_sample_batch_static": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.POINTER(Options), ctypes.c_void_p]),
     "arc_sample_workspace_bytes": (ctypes.c_size_t, [
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Options)]),
     "arc_sample_greedy": (ctypes.c_int, [
@@ -204,6 +209,23 @@ def sample_batch(logits, params, out, hist_offsets=None, hist_ids=None, err_word
                                  _ptr(hist_offsets), _ptr(hist_ids), _ptr(out), _ptr(err_word),
                                  _ptr(workspace), int(workspace.numel()), ctypes.byref(opts),
                                  _stream(stream))
+    if check and rc != ARC_OK:
+        raise ArcError(rc)
+    return rc
+
+
+def sample_batch_static(logits, params, out, hist_offsets=None, hist_ids=None, err_word=None, debug=None,
+                        ctas_per_row=0, max_hist_len=0, autoinc=False, stream=None, check=True) -> int:
+    """arc_sample_batch_static: as sample_batch, with the library's own scratch
+    array instead of a workspace (nothing is allocated for the call)."""
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    ld = int(logits.stride(0)) if B > 1 else V
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    opts = make_options(ctas_per_row, max_hist_len, autoinc, debug)
+    rc = load().arc_sample_batch_static(_ptr(logits), B, V, ld, _dtype_code(logits), _ptr(params),
+                                        _ptr(hist_offsets), _ptr(hist_ids), _ptr(out), _ptr(err_word),
+                                        ctypes.byref(opts), _stream(stream))
     if check and rc != ARC_OK:
         raise ArcError(rc)
     return rc

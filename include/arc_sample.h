@@ -217,6 +217,38 @@ typedef struct arc_sample_geometry {
 int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history,
                     const arc_sample_options* opts, arc_sample_geometry* geom);
 
+/*
+ * arc_sample_batch without a caller-provided workspace: the entry point for
+ * callers that cannot allocate device memory on their sampling path -- a
+ * host program that links only this library and the CUDA runtime and owns
+ * no allocator, or a serving loop held to a fixed device-memory budget that
+ * must not allocate per call.  (The pages have no counterpart: their
+ * samplers leave scratch memory to the engine around them.)
+ *
+ * Arguments, results and error codes are those of arc_sample_batch.  The
+ * per-slice summaries go to a scratch array of ARC_STATIC_WORKSPACE_BYTES
+ * compiled into the library (a static device array, one per device context,
+ * created when the CUDA runtime loads the library's kernels); the library
+ * never calls an allocator.  The first call on a device looks up the array's
+ * address (cudaGetSymbolAddress, once per device) and sets the kernels'
+ * attributes: make it before any stream capture that contains a call.
+ *
+ * Limit: a shape whose workspace on this device (arc_sample_plan
+ * workspace_bytes, B x slices-per-row x 288 bytes) exceeds
+ * ARC_STATIC_WORKSPACE_BYTES returns ARC_E_WORKSPACE with nothing enqueued;
+ * at V = 129,280 that admits B up to 910.  Nothing in the array needs to
+ * start at zero: each call writes every byte it later uses.  Every call on
+ * a device shares the one array, so calls that may overlap on the GPU
+ * (different streams without an ordering between them, or concurrent host
+ * threads) race: the caller must serialise them.
+ */
+#define ARC_STATIC_WORKSPACE_BYTES (4u << 20)
+
+int arc_sample_batch_static(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,
+                            arc_row_params* params, const int32_t* hist_offsets,
+                            const int32_t* hist_ids, int32_t* out, uint32_t* err_word,
+                            const arc_sample_options* opts, void* stream);
+
 /* Text for an ARC_E_* code (static storage). */
 const char* arc_sample_strerror(int code);
 

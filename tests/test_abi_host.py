@@ -30,8 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == sorted(["arc_sample_batch", "arc_sample_greedy", "arc_sample_plan",
-                            "arc_sample_workspace_bytes", "arc_sample_strerror",
+    assert names == sorted(["arc_sample_batch", "arc_sample_batch_static", "arc_sample_greedy",
+                            "arc_sample_plan", "arc_sample_workspace_bytes", "arc_sample_strerror",
                             "arc_sample_abi_version"]), names
 
 
