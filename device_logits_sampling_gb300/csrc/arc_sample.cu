@@ -27,6 +27,8 @@ struct Plan {
     int scan_smem = 0;      // dynamic shared memory of the scan kernel
     int cmax_off = 0;       // finish kernel layout
     int cs_off = 0;
+    int cid_off = 0;
+    int cv2_off = 0;
     int clist_off = 0;
     int cand_off = 0;
     int sorted_off = 0;
@@ -102,7 +104,7 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     }
     auto r128 = [](int64_t x) { return ((x + 127) / 128) * 128; };
     const int64_t cmax_bytes = r128(s * kChunks * 4);
-    const int64_t cs_bytes = cmax_bytes;
+    const int64_t cs_bytes = 3 * cmax_bytes;  // masses, max ids, second largest logits
     const int64_t clist_bytes = r128((s * kChunks + kWarps) * 4);
     const int64_t cand_bytes = r128(int64_t{kCandCap} * 16);
     const int64_t stage_bytes = int64_t{kWarps} * kCollectU * 32 * 16 + cand_bytes;  // + sorted candidates
@@ -123,6 +125,8 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     p.scan_smem = static_cast<int>(scan_smem);
     p.cmax_off = 0;
     p.cs_off = static_cast<int>(cmax_bytes);
+    p.cid_off = static_cast<int>(2 * cmax_bytes);
+    p.cv2_off = static_cast<int>(3 * cmax_bytes);
     p.clist_off = static_cast<int>(cmax_bytes + cs_bytes);
     p.cand_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes);
     p.stage_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes);
@@ -311,6 +315,8 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.aligned = aligned;
     fa.cmax_off = p.cmax_off;
     fa.cs_off = p.cs_off;
+    fa.cid_off = p.cid_off;
+    fa.cv2_off = p.cv2_off;
     fa.clist_off = p.clist_off;
     fa.cand_off = p.cand_off;
     fa.sorted_off = p.sorted_off;

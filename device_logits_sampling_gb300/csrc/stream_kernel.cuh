@@ -30,7 +30,7 @@ namespace arc {
 constexpr int kVpt = 4;                  // 16-byte vectors per thread in a scan CTA
 constexpr int kChunks = kVpt * kWarps;   // chunks per slice summary (32-vector chunks)
 constexpr int kHdrBytes = 32;
-constexpr int kSummaryBytes = kHdrBytes + kChunks * 8;
+constexpr int kSummaryBytes = kHdrBytes + kChunks * 16;
 constexpr int kMaxRowCtas = 128;         // slices per row at most
 constexpr int kCandCap = 1024;           // ids the direct selection holds
 constexpr int kCollectU = 8;             // chunks per warp in flight while gathering
@@ -70,6 +70,8 @@ struct FinishArgs {
     int aligned;
     int cmax_off;      // dynamic shared memory: chunk maxima of the row,
     int cs_off;        //   chunk masses,
+    int cid_off;       //   chunk max vectors,
+    int cv2_off;       //   chunk second vector maxima,
     int clist_off;     //   per-warp candidate chunk lists,
     int cand_off;      //   candidates (key, id, mass),
     int sorted_off;    //   the candidates in (key desc, id asc) order,
@@ -108,8 +110,17 @@ struct __align__(16) KernelShared {
 __device__ __forceinline__ const unsigned char* summary_at(const unsigned char* base, int s, int row, int c) {
     return base + (static_cast<size_t>(row) * s + c) * kSummaryBytes;
 }
-__device__ __forceinline__ const float2* chunk_table(const unsigned char* sm) {
-    return reinterpret_cast<const float2*>(sm + kHdrBytes);
+// One 32-vector chunk of a slice, as the scan kernel summarises it.
+struct __align__(16) ChunkEntry {
+    float m;   // chunk max (NaN ignored), -inf when the chunk holds no number
+    float S;   // rows that need masses: fp32 sum of 2^((z - m) log2(e) / T), else 0
+    int lane;  // filtered rows: the vector (lane) of the chunk holding the max first, else -1
+    float u2;  // filtered rows: the largest max of the chunk's other vectors, else +inf
+};
+static_assert(sizeof(ChunkEntry) == 16, "chunk entry size");
+
+__device__ __forceinline__ const ChunkEntry* chunk_table(const unsigned char* sm) {
+    return reinterpret_cast<const ChunkEntry*>(sm + kHdrBytes);
 }
 
 // weight of z relative to a reference max mr (chunk or row): ex2((z - mr) c);
@@ -423,20 +434,40 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
     }
 
     // chunk table: per 32-vector chunk its max and, when needed, the fp32 sum of
-    // weights relative to it (NaN ids weigh nothing); every entry is written,
-    // entries past the slice as (-inf, 0)
+    // weights relative to it (NaN ids weigh nothing); filtered rows also get
+    // the vector holding the max and the largest max of the other vectors, so
+    // that a chunk with one vector at or above a later floor is re-read as that
+    // one 16-byte vector.  Every entry is written; entries past the slice hold
+    // no number.
     unsigned char* mysum = const_cast<unsigned char*>(summary_at(a.summaries, a.s, row, cidx));
     if (row_chunks) {
-        float2* ch = reinterpret_cast<float2*>(mysum + kHdrBytes);
+        ChunkEntry* ch = reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes);
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) {
-            const float mj = key_to_float(__reduce_max_sync(0xFFFFFFFFu, fkey(vm[j])));
+            const uint32_t kj = fkey(vm[j]);
+            const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, kj);
+            const float mj = key_to_float(kmax);
             float Sj = 0.0f;
             if (mass) {
                 const float lr = (vm[j] != -INFINITY) ? __fmul_rn(ls[j], wrel(vm[j], mj, cT)) : 0.0f;
                 Sj = warp_sum_f(lr);
             }
-            if (lane == 0) ch[j * kWarps + warp] = make_float2(mj, Sj);
+            int flane = -1;
+            float u2 = INFINITY;
+            if (md.filtered) {
+                const unsigned holders = __ballot_sync(0xFFFFFFFFu, kj == kmax && vm[j] > -INFINITY);
+                flane = holders ? __ffs(holders) - 1 : -1;
+                const uint32_t k2 = __reduce_max_sync(0xFFFFFFFFu, lane == flane ? 0u : kj);
+                u2 = k2 > 0x007FFFFFu ? key_to_float(k2) : -INFINITY;
+            }
+            if (lane == 0) {
+                ChunkEntry ce;
+                ce.m = mj;
+                ce.S = Sj;
+                ce.lane = flane;
+                ce.u2 = u2;
+                ch[j * kWarps + warp] = ce;
+            }
         }
     }
 
@@ -806,6 +837,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
     const char* rowp = static_cast<const char*>(a.logits) + static_cast<int64_t>(row) * a.ld * E::kBytes;
     float* cm = reinterpret_cast<float*>(dyn + a.cmax_off);
     float* cs = reinterpret_cast<float*>(dyn + a.cs_off);
+    int* cln = reinterpret_cast<int*>(dyn + a.cid_off);
+    float* cu2 = reinterpret_cast<float*>(dyn + a.cv2_off);
     const arc_row_params P = load_params(a.params + row);
     int hn = 0, hbeg = 0;
     if (HIST && a.hist_off != nullptr) {
@@ -839,19 +872,20 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
         constexpr int kLd = 4;  // chunk entries in flight per thread
         constexpr int kStride = kThreads - 32;
         for (int g0 = tid - 32; g0 < nch; g0 += kLd * kStride) {
-            float2 e[kLd];
+            ChunkEntry e[kLd];
 #pragma unroll
             for (int u = 0; u < kLd; ++u) {
                 const int gi = g0 + u * kStride;
-                e[u] = (gi < nch) ? chunk_table(summary_at(a.summaries, s, row, gi / kChunks))[gi % kChunks]
-                                  : make_float2(0.0f, 0.0f);
+                if (gi < nch) e[u] = chunk_table(summary_at(a.summaries, s, row, gi / kChunks))[gi % kChunks];
             }
 #pragma unroll
             for (int u = 0; u < kLd; ++u) {
                 const int gi = g0 + u * kStride;
                 if (gi < nch) {
-                    cm[gi] = e[u].x;
-                    cs[gi] = e[u].y;
+                    cm[gi] = e[u].m;
+                    cs[gi] = e[u].S;
+                    cln[gi] = e[u].lane;
+                    cu2[gi] = e[u].u2;
                 }
             }
         }
@@ -1111,10 +1145,52 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
                 uint4* stage = reinterpret_cast<uint4*>(dyn + a.stage_off) + warp * (kCollectU * 32);
                 int* wl = reinterpret_cast<int*>(dyn + a.clist_off) + warp * ((nch + kWarps - 1) / kWarps);
                 int nw = 0;
+                const unsigned below = (1u << lane) - 1u;
                 for (int b0 = warp; b0 < nch; b0 += kWarps * 32) {
                     const int g = b0 + lane * kWarps;
-                    const unsigned hits = __ballot_sync(0xFFFFFFFFu, g < nch && cm[g] >= zf);
-                    if (hits & (1u << lane)) wl[nw + __popc(hits & ((1u << lane) - 1u))] = g;
+                    const bool in = g < nch && cm[g] >= zf;
+                    // a chunk whose other vectors all lie below zf: only the max's
+                    // vector can hold ids >= zf, and this thread reads it alone
+                    const bool single = in && cu2[g] < zf && cln[g] >= 0;
+                    float z[VEC];
+                    int cnt = 0;
+                    int vrow = 0;
+                    if (single) {
+                        const int c = g / kChunks;
+                        const int vs = (g % kChunks) * 32 + cln[g];
+                        const int sn = min((c + 1) * a.L, a.V) - c * a.L;
+                        vrow = c * Lv + vs;
+                        E::unpack(E::global_vec(rowp + static_cast<int64_t>(c) * a.L * E::kBytes, vs, sn, a.aligned), z);
+                        if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, vrow, z);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
+                    }
+                    int inc = cnt;
+#pragma unroll
+                    for (int dd = 1; dd < 32; dd <<= 1) {
+                        const int o = __shfl_up_sync(0xFFFFFFFFu, inc, dd);
+                        if (lane >= dd) inc += o;
+                    }
+                    uint32_t base = 0;
+                    const int tot = __shfl_sync(0xFFFFFFFFu, inc, 31);
+                    if (tot > 0) {
+                        if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(tot));
+                        base = __shfl_sync(0xFFFFFFFFu, base, 31);
+                    }
+                    if (cnt > 0) {
+                        uint32_t pos = base + static_cast<uint32_t>(inc - cnt);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) {
+                            if (z[e] >= zf) {
+                                if (pos < static_cast<uint32_t>(kCandCap))
+                                    cc[pos] = (static_cast<uint64_t>(fkey(z[e])) << 32) |
+                                              (0xFFFFFFFFu - static_cast<uint32_t>(vrow * VEC + e));
+                                ++pos;
+                            }
+                        }
+                    }
+                    const unsigned hits = __ballot_sync(0xFFFFFFFFu, in && !single);
+                    if (hits & (1u << lane)) wl[nw + __popc(hits & below)] = g;
                     nw += __popc(hits);
                 }
                 __syncwarp();
