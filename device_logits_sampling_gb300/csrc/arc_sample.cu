@@ -170,20 +170,26 @@ cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done) {
 }
 
 template <class K, class A>
-cudaError_t launch_cluster(K kernel, int64_t grid, int s, int smem, cudaStream_t st, const A& args) {
+cudaError_t launch_cluster(K kernel, int64_t grid, int s, int smem, cudaStream_t st, const A& args,
+                           bool early = false) {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(s);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // early: the kernel may start before the previous kernel on the stream has
+    // finished (programmatic dependent launch); it waits for that kernel's
+    // results with griddepcontrol.wait before reading them
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = early ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
@@ -332,7 +338,7 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
         if (err != cudaSuccess) return err;
         scan<<<static_cast<unsigned>(p.slices), kThreads, p.scan_smem, st>>>(sa);
         err = cudaGetLastError();
-        if (err == cudaSuccess) err = launch_cluster(fin, B, 1, p.fin_smem, st, fa);
+        if (err == cudaSuccess) err = launch_cluster(fin, B, 1, p.fin_smem, st, fa, /*early=*/true);
         return err;
     };
     cudaError_t e;

@@ -29,7 +29,7 @@ namespace arc {
 
 constexpr int kVpt = 4;                  // 16-byte vectors per thread in a scan CTA
 constexpr int kChunks = kVpt * kWarps;   // chunks per slice summary (32-vector chunks)
-constexpr int kHdrBytes = 32;
+constexpr int kHdrBytes = kWarps * 16;   // per-warp records of a slice
 constexpr int kSummaryBytes = kHdrBytes + kChunks * 16;
 constexpr int kMaxRowCtas = 128;         // slices per row at most
 constexpr int kCandCap = 1024;           // ids the direct selection holds
@@ -81,15 +81,15 @@ struct FinishArgs {
     int fb_rounds;     // rounds of a whole row
 };
 
-struct SliceHeader {
-    float m;         // slice max (NaN-free), -inf when none
+// One warp's share of a slice, as the scan kernel summarises it: each warp
+// writes its own record, so the scan needs no barrier between its warps.
+struct __align__(16) WarpRecord {
+    float m;         // max of the warp's vectors (NaN-free), -inf when none
     int am;          // its first id, -1 when none
     uint32_t flags;  // ARC_ERR_NAN | ARC_ERR_HIST_ID | ARC_ERR_HIST_CAP
-    int nchunk;      // chunk entries written
-    double tlnp;     // slice 0 of a min-p row: T ln(min_p) in fp64, else 0
-    int pad[2];
+    int pad;
 };
-static_assert(sizeof(SliceHeader) == kHdrBytes, "slice header size");
+static_assert(sizeof(WarpRecord) * kWarps == kHdrBytes, "slice record size");
 
 struct FinishScratch {
     uint64_t redu[kWarps];
@@ -306,9 +306,6 @@ __device__ __forceinline__ ScanRow scan_row_of(const ScanArgs& a, int row) {
 }
 
 struct ScanShared {
-    float redf[kWarps];
-    int redi[kWarps];
-    uint32_t rednan[kWarps];
     uint32_t red32[kWarps];
     uint32_t sflags;  // history id errors (written only after a barrier past its init)
 };
@@ -359,11 +356,6 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
     const bool need_data = rerr == 0;
     const bool row_chunks = need_data && !md.greedy;
     const bool mass = row_chunks && md.need_mass;
-    // slice 0 of a min-p row carries T ln(min_p) in fp64 for the finish kernel;
-    // thread 0 takes it while the slice's loads are still in flight
-    double tlnp = 0.0;
-    if (cidx == 0 && tid == 0 && row_chunks && md.filtered && md.minp_on)
-        tlnp = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
     const float cT = mass ? __fdiv_rn(1.4426950408889634f, P.temperature) : 0.0f;
 
     const uint32_t* pbm = nullptr;
@@ -396,9 +388,16 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         return ((pbm[l0 >> 5] >> (l0 & 31)) & ((1u << VEC) - 1u)) != 0;
     };
 
-    // per vector: its max with NaN ignored, and (rows that need masses) the
-    // lane's weight sum relative to that max; per lane: the best vector
-    float vm[kVpt], ls[kVpt];
+    // per vector: its max with NaN ignored and (rows that need masses) the
+    // lane's weight sum relative to that max; per lane: the best vector.  Per
+    // 32-vector chunk (the warp's vectors j), as soon as they are known: the
+    // chunk max and, when needed, the fp32 sum of weights relative to it (NaN
+    // ids weigh nothing); filtered rows also get the vector holding the max
+    // and the largest max of the other vectors, so that a chunk with one vector
+    // at or above a later floor is re-read as that one 16-byte vector.  Every
+    // entry is written; entries past the slice hold no number.
+    unsigned char* mysum = const_cast<unsigned char*>(summary_at(a.summaries, a.s, row, cidx));
+    ChunkEntry* ch = reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes);
     float bv = -INFINITY;
     int bj = -1;
     bool nanf = false;
@@ -429,33 +428,16 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
             if (mass && x != -INFINITY)
                 l = (vnan || x == INFINITY) ? lane_mass_safe<VEC>(z, x, cT) : lane_mass_packed<VEC>(z, x, cT);
         }
-        vm[j] = x;
-        ls[j] = l;
-    }
-
-    // chunk table: per 32-vector chunk its max and, when needed, the fp32 sum of
-    // weights relative to it (NaN ids weigh nothing); filtered rows also get
-    // the vector holding the max and the largest max of the other vectors, so
-    // that a chunk with one vector at or above a later floor is re-read as that
-    // one 16-byte vector.  Every entry is written; entries past the slice hold
-    // no number.
-    unsigned char* mysum = const_cast<unsigned char*>(summary_at(a.summaries, a.s, row, cidx));
-    if (row_chunks) {
-        ChunkEntry* ch = reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes);
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) {
-            const uint32_t kj = fkey(vm[j]);
+        if (row_chunks) {
+            const uint32_t kj = fkey(x);
             const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, kj);
             const float mj = key_to_float(kmax);
             float Sj = 0.0f;
-            if (mass) {
-                const float lr = (vm[j] != -INFINITY) ? __fmul_rn(ls[j], wrel(vm[j], mj, cT)) : 0.0f;
-                Sj = warp_sum_f(lr);
-            }
+            if (mass) Sj = warp_sum_f((x != -INFINITY) ? __fmul_rn(l, wrel(x, mj, cT)) : 0.0f);
             int flane = -1;
             float u2 = INFINITY;
             if (md.filtered) {
-                const unsigned holders = __ballot_sync(0xFFFFFFFFu, kj == kmax && vm[j] > -INFINITY);
+                const unsigned holders = __ballot_sync(0xFFFFFFFFu, kj == kmax && x > -INFINITY);
                 flane = holders ? __ffs(holders) - 1 : -1;
                 const uint32_t k2 = __reduce_max_sync(0xFFFFFFFFu, lane == flane ? 0u : kj);
                 u2 = k2 > 0x007FFFFFu ? key_to_float(k2) : -INFINITY;
@@ -492,27 +474,12 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
     const uint32_t wid = __reduce_min_sync(0xFFFFFFFFu, mine);
     const bool wnan = __any_sync(0xFFFFFFFFu, nanf);
     if (lane == 0) {
-        sh.redf[warp] = (wid == 0xFFFFFFFFu) ? -INFINITY : key_to_float(wkey);
-        sh.redi[warp] = (wid == 0xFFFFFFFFu) ? -1 : static_cast<int>(wid);
-        sh.rednan[warp] = wnan ? ARC_ERR_NAN : 0u;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float mc = -INFINITY;
-        int amc = -1;
-        uint32_t nanw = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            better(mc, amc, sh.redf[w], sh.redi[w]);
-            nanw |= sh.rednan[w];
-        }
-        SliceHeader h;
-        h.m = mc;
-        h.am = amc;
-        h.flags = nanw | (rerr & (ARC_ERR_HIST_ID | ARC_ERR_HIST_CAP));
-        h.nchunk = row_chunks ? kChunks : 0;
-        h.tlnp = tlnp;
-        h.pad[0] = h.pad[1] = 0;
-        *reinterpret_cast<SliceHeader*>(mysum) = h;
+        WarpRecord r;
+        r.m = (wid == 0xFFFFFFFFu) ? -INFINITY : key_to_float(wkey);
+        r.am = (wid == 0xFFFFFFFFu) ? -1 : static_cast<int>(wid);
+        r.flags = (wnan ? ARC_ERR_NAN : 0u) | (rerr & (ARC_ERR_HIST_ID | ARC_ERR_HIST_CAP));
+        r.pad = 0;
+        reinterpret_cast<WarpRecord*>(mysum)[warp] = r;
     }
 }
 
@@ -525,6 +492,10 @@ __global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const Scan
     constexpr int VEC = E::kVec;
     extern __shared__ __align__(128) unsigned char dyn[];
     __shared__ ScanShared sh;
+    // the finish kernel may be scheduled once every scan CTA is running; it
+    // waits (griddepcontrol.wait) for this grid to complete before reading
+    // the summaries
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int row = static_cast<int>(blockIdx.x) / a.s;
     const int cidx = static_cast<int>(blockIdx.x) - row * a.s;
@@ -608,24 +579,20 @@ __device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, 
     return zf > -INFINITY;
 }
 
-// Floor search by the whole CTA: the largest key x, to 2^12 keys, whose
+// Floor search by the whole CTA, exact to 2^12 keys: the largest key x whose
 // entries at or above it weigh at least tgt in total, two key bits per step
-// from the top (three candidate prefixes counted per step; one barrier per
-// step).  kw(e, key, weight) gives entry e; PER entries per thread are held in
-// registers (n <= PER * kThreads); the weights' sum must fit in 32 bits.
-// False when all entries weigh less than tgt.
-template <int PER, class KW>
+// from the top (three candidate prefixes counted per step, one barrier per
+// step).  kw(e, key, weight) gives entry e; the weights' sum must fit in 32
+// bits.  False when all entries weigh less than tgt.  The fallback of
+// floor_hist: entries are re-read every step rather than held in registers.
+template <class KW>
 __device__ bool floor_block(int n, KW kw, uint32_t tgt, FinishScratch& SS, uint32_t& edge) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t key[PER], w[PER];
     uint32_t tot = 0;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-        const int e = tid + q * kThreads;
-        key[q] = 0u;
-        w[q] = 0u;
-        if (e < n) kw(e, key[q], w[q]);
-        tot += w[q];
+    for (int e = tid; e < n; e += kThreads) {
+        uint32_t key, w;
+        kw(e, key, w);
+        tot += w;
     }
     tot = __reduce_add_sync(0xFFFFFFFFu, tot);
     if (lane == 0) SS.fc[0][warp][0] = tot;
@@ -639,11 +606,12 @@ __device__ bool floor_block(int n, KW kw, uint32_t tgt, FinishScratch& SS, uint3
     for (int b = 30; b >= 12; b -= 2, par ^= 1) {
         const uint32_t t1 = p | (1u << b), t2 = p | (2u << b), t3 = p | (3u << b);
         uint32_t c1 = 0, c2 = 0, c3 = 0;
-#pragma unroll
-        for (int q = 0; q < PER; ++q) {
-            c1 += (key[q] >= t1) ? w[q] : 0u;
-            c2 += (key[q] >= t2) ? w[q] : 0u;
-            c3 += (key[q] >= t3) ? w[q] : 0u;
+        for (int e = tid; e < n; e += kThreads) {
+            uint32_t key, w;
+            kw(e, key, w);
+            c1 += (key >= t1) ? w : 0u;
+            c2 += (key >= t2) ? w : 0u;
+            c3 += (key >= t3) ? w : 0u;
         }
         c1 = __reduce_add_sync(0xFFFFFFFFu, c1);
         c2 = __reduce_add_sync(0xFFFFFFFFu, c2);
@@ -845,6 +813,10 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
         hbeg = a.hist_off[row];
         hn = max(0, a.hist_off[row + 1] - hbeg);
     }
+    // launched early behind the scan kernel: its summaries are complete and
+    // visible after this (the parameters and history above are not written by
+    // the scan)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // the slice headers (warp 0) and the chunk tables (warps 1-7) load while
     // the parameters do: nothing here waits for them
@@ -852,12 +824,31 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
         float v = -INFINITY;
         int i = -1;
         uint32_t f = 0;
+        const int nrec = s * kWarps;
+        auto rec = [&](int q) {
+            return reinterpret_cast<const WarpRecord*>(summary_at(a.summaries, s, row, q / kWarps))[q % kWarps];
+        };
+        constexpr int kLdR = 4;  // records in flight per lane
+        WarpRecord r[kLdR];
+#pragma unroll
+        for (int u = 0; u < kLdR; ++u)
+            if (lane + 32 * u < nrec) r[u] = rec(lane + 32 * u);
+        // min-p: T ln(min_p) in fp64 by one thread while the records load
+        // (fp64 runs at a small fraction of the fp32 rate on this part)
         double tl = 0.0;
-        for (int c = lane; c < s; c += 32) {
-            const SliceHeader* h = reinterpret_cast<const SliceHeader*>(summary_at(a.summaries, s, row, c));
-            better(v, i, h->m, h->am);
-            f |= h->flags;
-            if (c == 0) tl = h->tlnp;
+        if (lane == 0 && P.min_p > 0.0f && P.min_p <= 1.0f && isfinite(P.temperature))
+            tl = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
+#pragma unroll
+        for (int u = 0; u < kLdR; ++u) {
+            if (lane + 32 * u < nrec) {
+                better(v, i, r[u].m, r[u].am);
+                f |= r[u].flags;
+            }
+        }
+        for (int q = lane + 32 * kLdR; q < nrec; q += 32) {
+            const WarpRecord x = rec(q);
+            better(v, i, x.m, x.am);
+            f |= x.flags;
         }
         warp_argmax(v, i);
         f = __reduce_or_sync(0xFFFFFFFFu, f);
@@ -1117,8 +1108,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
                         w = wt(x);
                     };
                     uint32_t edge = 0;
-                    fast = (nch <= 2 * kThreads) ? floor_block<2>(nch, kw, tgt, SS, edge)
-                                                 : floor_block<kMaxRowCtas * kChunks / kThreads>(nch, kw, tgt, SS, edge);
+                    fast = floor_block(nch, kw, tgt, SS, edge);
                     if (fast) zf = Ctx::lo_float(edge);
                 }
             } else {

@@ -102,14 +102,14 @@ def test_bad_arguments_fail_before_any_cuda_call(lib):
 
 
 def test_plan_geometry(lib):
-    # the mixed B=256 bf16 batch: 16 items per row of 8,080 logits (16,160 B) each
+    # the mixed B=256 bf16 batch: 16 slices per row of 8,080 logits (16,160 B) each
     g = sampler.plan(256, workloads.VOCAB_V4, workloads.DTYPE_BF16)
     assert (g.ctas_per_row, g.slice_elems, g.grid_ctas, g.threads) == (16, 8080, 4096, 256)
     assert g.frac_bits == 62 - 17
     # a single row is spread over many CTAs (latency), each with >= 1024 logits
     g1 = sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16)
     assert g1.ctas_per_row >= 32 and g1.slice_elems >= 1024
-    # fp32 items hold half as many logits
+    # fp32 slices hold half as many logits
     assert sampler.plan(64, workloads.VOCAB_V4, workloads.DTYPE_F32).ctas_per_row == 32
     # small vocabularies stay on one CTA
     assert sampler.plan(4, 1024, workloads.DTYPE_F32).ctas_per_row == 1
