@@ -30,7 +30,8 @@ namespace arc {
 constexpr int kVpt = 4;                  // 16-byte vectors per thread in a scan CTA
 constexpr int kChunks = kVpt * kWarps;   // chunks per slice summary (32-vector chunks)
 constexpr int kHdrBytes = kWarps * 16;   // per-warp records of a slice
-constexpr int kSummaryBytes = kHdrBytes + kChunks * 16;
+constexpr int kNoteBytes = 16;           // slice 0 of a min-p row: T ln(min_p) in fp64
+constexpr int kSummaryBytes = kHdrBytes + kChunks * 16 + kNoteBytes;
 constexpr int kMaxRowCtas = 128;         // slices per row at most
 constexpr int kCandCap = 1024;           // ids the direct selection holds
 constexpr int kCollectU = 8;             // chunks per warp in flight while gathering
@@ -121,6 +122,9 @@ static_assert(sizeof(ChunkEntry) == 16, "chunk entry size");
 
 __device__ __forceinline__ const ChunkEntry* chunk_table(const unsigned char* sm) {
     return reinterpret_cast<const ChunkEntry*>(sm + kHdrBytes);
+}
+__device__ __forceinline__ const double* slice_note(const unsigned char* sm) {
+    return reinterpret_cast<const double*>(sm + kHdrBytes + kChunks * 16);
 }
 
 // weight of z relative to a reference max mr (chunk or row): ex2((z - mr) c);
@@ -356,6 +360,13 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
     const bool need_data = rerr == 0;
     const bool row_chunks = need_data && !md.greedy;
     const bool mass = row_chunks && md.need_mass;
+    // slice 0 of a min-p row: T ln(min_p) in fp64 for the finish kernel, by one
+    // thread while the slice's loads are in flight (fp64 is slow on this part)
+    if (cidx == 0 && tid == 0 && row_chunks && md.filtered && md.minp_on) {
+        unsigned char* note = const_cast<unsigned char*>(reinterpret_cast<const unsigned char*>(
+            slice_note(summary_at(a.summaries, a.s, row, 0))));
+        *reinterpret_cast<double*>(note) = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
+    }
     const float cT = mass ? __fdiv_rn(1.4426950408889634f, P.temperature) : 0.0f;
 
     const uint32_t* pbm = nullptr;
@@ -833,11 +844,11 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
 #pragma unroll
         for (int u = 0; u < kLdR; ++u)
             if (lane + 32 * u < nrec) r[u] = rec(lane + 32 * u);
-        // min-p: T ln(min_p) in fp64 by one thread while the records load
-        // (fp64 runs at a small fraction of the fp32 rate on this part)
+        // min-p: T ln(min_p), computed in fp64 by the scan kernel (slice 0)
         double tl = 0.0;
-        if (lane == 0 && P.min_p > 0.0f && P.min_p <= 1.0f && isfinite(P.temperature))
-            tl = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
+        if (lane == 0 && P.min_p > 0.0f && P.min_p <= 1.0f && isfinite(P.temperature) && P.temperature > 0.0f &&
+            !(P.top_k == 1))
+            tl = *slice_note(summary_at(a.summaries, s, row, 0));
 #pragma unroll
         for (int u = 0; u < kLdR; ++u) {
             if (lane + 32 * u < nrec) {
@@ -1134,27 +1145,54 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
                 const int Lv = a.L / VEC;
                 uint4* stage = reinterpret_cast<uint4*>(dyn + a.stage_off) + warp * (kCollectU * 32);
                 int* wl = reinterpret_cast<int*>(dyn + a.clist_off) + warp * ((nch + kWarps - 1) / kWarps);
-                int nw = 0;
+                // classify this warp's chunks w, w + 8, ... at or above zf: "single"
+                // when the other vectors lie below zf (only the max's vector can
+                // hold ids >= zf), else "whole"; lists from both ends of wl
+                const int wcap = (nch + kWarps - 1) / kWarps;
                 const unsigned below = (1u << lane) - 1u;
+                int nsg = 0, nw = 0;
                 for (int b0 = warp; b0 < nch; b0 += kWarps * 32) {
                     const int g = b0 + lane * kWarps;
                     const bool in = g < nch && cm[g] >= zf;
-                    // a chunk whose other vectors all lie below zf: only the max's
-                    // vector can hold ids >= zf, and this thread reads it alone
                     const bool single = in && cu2[g] < zf && cln[g] >= 0;
-                    float z[VEC];
+                    const unsigned bs = __ballot_sync(0xFFFFFFFFu, single);
+                    const unsigned bw = __ballot_sync(0xFFFFFFFFu, in && !single);
+                    if (single) wl[nsg + __popc(bs & below)] = g;
+                    if (in && !single) wl[wcap - 1 - (nw + __popc(bw & below))] = g;
+                    nsg += __popc(bs);
+                    nw += __popc(bw);
+                }
+                __syncwarp();
+                const uint4 ninf = (DT == ARC_BF16) ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                                                    : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+                // whole chunks, up to kCollectU per round, staged by 16-byte
+                // asynchronous copies; the first round goes out before the singles
+                auto stage_round = [&](int r0) {
+#pragma unroll
+                    for (int u = 0; u < kCollectU; ++u) {
+                        if (r0 + u < nw) {
+                            const int g = wl[wcap - 1 - (r0 + u)];
+                            const int c = g / kChunks;
+                            const int vs = (g % kChunks) * 32 + lane;
+                            const int sn = min((c + 1) * a.L, a.V) - c * a.L;
+                            const char* sb = rowp + static_cast<int64_t>(c) * a.L * E::kBytes;
+                            uint4* dst = stage + u * 32 + lane;
+                            if (a.aligned && (vs + 1) * VEC <= sn)
+                                cp_async16(dst, sb + static_cast<size_t>(vs) * 16);
+                            else
+                                *dst = (vs * VEC < sn) ? E::global_vec(sb, vs, sn, false) : ninf;
+                        }
+                    }
+                };
+                stage_round(0);
+                // ids found go to slots from one shared counter (one atomic per warp and batch)
+                auto emit = [&](bool valid, const float (&z)[VEC], int vrow) {
                     int cnt = 0;
-                    int vrow = 0;
-                    if (single) {
-                        const int c = g / kChunks;
-                        const int vs = (g % kChunks) * 32 + cln[g];
-                        const int sn = min((c + 1) * a.L, a.V) - c * a.L;
-                        vrow = c * Lv + vs;
-                        E::unpack(E::global_vec(rowp + static_cast<int64_t>(c) * a.L * E::kBytes, vs, sn, a.aligned), z);
-                        if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, vrow, z);
+                    if (valid) {
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
                     }
+                    if (__ballot_sync(0xFFFFFFFFu, cnt > 0) == 0u) return;  // uniform
                     int inc = cnt;
 #pragma unroll
                     for (int dd = 1; dd < 32; dd <<= 1) {
@@ -1162,11 +1200,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
                         if (lane >= dd) inc += o;
                     }
                     uint32_t base = 0;
-                    const int tot = __shfl_sync(0xFFFFFFFFu, inc, 31);
-                    if (tot > 0) {
-                        if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(tot));
-                        base = __shfl_sync(0xFFFFFFFFu, base, 31);
-                    }
+                    if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(inc));
+                    base = __shfl_sync(0xFFFFFFFFu, base, 31);
                     if (cnt > 0) {
                         uint32_t pos = base + static_cast<uint32_t>(inc - cnt);
 #pragma unroll
@@ -1179,35 +1214,42 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
                             }
                         }
                     }
-                    const unsigned hits = __ballot_sync(0xFFFFFFFFu, in && !single);
-                    if (hits & (1u << lane)) wl[nw + __popc(hits & below)] = g;
-                    nw += __popc(hits);
-                }
-                __syncwarp();
-                const uint4 ninf = (DT == ARC_BF16) ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
-                                                    : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
-                for (int r0 = 0; r0 < nw; r0 += kCollectU) {
-                    // every copy of the round in flight at once
+                };
+                // single vectors: lane i reads entries i and i + 32 of each 64
+                for (int i0 = 0; i0 < nsg; i0 += 64) {
+                    uint4 raw[2];
+                    int vrow[2];
 #pragma unroll
-                    for (int u = 0; u < kCollectU; ++u) {
-                        if (r0 + u < nw) {
-                            const int g = wl[r0 + u];
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = i0 + u * 32 + lane;
+                        vrow[u] = -1;
+                        if (i < nsg) {
+                            const int g = wl[i];
                             const int c = g / kChunks;
-                            const int vs = (g % kChunks) * 32 + lane;
+                            const int vs = (g % kChunks) * 32 + cln[g];
                             const int sn = min((c + 1) * a.L, a.V) - c * a.L;
-                            const char* sb = rowp + static_cast<int64_t>(c) * a.L * E::kBytes;
-                            uint4* dst = stage + u * 32 + lane;
-                            if (a.aligned && (vs + 1) * VEC <= sn)
-                                cp_async16(dst, sb + static_cast<size_t>(vs) * 16);
-                            else
-                                *dst = (vs * VEC < sn) ? E::global_vec(sb, vs, sn, false) : ninf;
+                            raw[u] = E::global_vec(rowp + static_cast<int64_t>(c) * a.L * E::kBytes, vs, sn, a.aligned);
+                            vrow[u] = c * Lv + vs;
                         }
                     }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        float z[VEC];
+                        if (vrow[u] >= 0) {
+                            E::unpack(raw[u], z);
+                            if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, vrow[u], z);
+                        }
+                        emit(vrow[u] >= 0, z, vrow[u]);
+                    }
+                }
+                // whole chunks
+                for (int r0 = 0; r0 < nw; r0 += kCollectU) {
+                    if (r0 > 0) stage_round(r0);
                     cp_async_wait_all();
                     __syncwarp();
                     const int nst = min(kCollectU, nw - r0);
                     for (int u = 0; u < nst; ++u) {
-                        const int g = wl[r0 + u];
+                        const int g = wl[wcap - 1 - (r0 + u)];
                         const int c = g / kChunks;
                         const int vs = (g % kChunks) * 32 + lane;
                         float z[VEC];
@@ -1215,29 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
                         // padding vectors past the slice read as -inf and take no patch
                         if (HIST && has_patch && vs * VEC < min((c + 1) * a.L, a.V) - c * a.L)
                             apply_patches<VEC>(pbm, pwp, ppat, c * Lv + vs, z);
-                        int cnt = 0;
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
-                        if (__ballot_sync(0xFFFFFFFFu, cnt > 0) == 0u) continue;  // uniform
-                        int inc = cnt;
-#pragma unroll
-                        for (int dd = 1; dd < 32; dd <<= 1) {
-                            const int o = __shfl_up_sync(0xFFFFFFFFu, inc, dd);
-                            if (lane >= dd) inc += o;
-                        }
-                        uint32_t base = 0;
-                        if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(inc));
-                        base = __shfl_sync(0xFFFFFFFFu, base, 31);
-                        uint32_t pos = base + static_cast<uint32_t>(inc - cnt);
-                        const uint32_t id0 = static_cast<uint32_t>((c * Lv + vs) * VEC);
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) {
-                            if (z[e] >= zf) {
-                                if (pos < static_cast<uint32_t>(kCandCap))
-                                    cc[pos] = (static_cast<uint64_t>(fkey(z[e])) << 32) | (0xFFFFFFFFu - (id0 + e));
-                                ++pos;
-                            }
-                        }
+                        emit(true, z, c * Lv + vs);
                     }
                     __syncwarp();  // the stage is refilled next round
                 }

@@ -234,9 +234,9 @@ int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history,
  * attributes: make it before any stream capture that contains a call.
  *
  * Limit: a shape whose workspace on this device (arc_sample_plan
- * workspace_bytes, B x slices-per-row x 640 bytes) exceeds
+ * workspace_bytes, B x slices-per-row x 656 bytes) exceeds
  * ARC_STATIC_WORKSPACE_BYTES returns ARC_E_WORKSPACE with nothing enqueued;
- * at V = 129,280 that admits B up to 819.  Nothing in the array needs to
+ * at V = 129,280 that admits B up to 799.  Nothing in the array needs to
  * start at zero: each call writes every byte it later uses.  Every call on
  * a device shares the one array, so calls that may overlap on the GPU
  * (different streams without an ordering between them, or concurrent host

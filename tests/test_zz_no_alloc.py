@@ -55,7 +55,7 @@ def test_static_refuses_a_shape_beyond_its_scratch(cuda_lib):
     import torch
 
     S = cuda_lib
-    B, V = 1024, 129_280  # 1024 rows x 16 slices x 640 B > ARC_STATIC_WORKSPACE_BYTES
+    B, V = 1024, 129_280  # 1024 rows x 16 slices x 656 B > ARC_STATIC_WORKSPACE_BYTES
     assert S.plan(B, V, workloads.DTYPE_BF16).workspace_bytes > S.ARC_STATIC_WORKSPACE_BYTES
     logits = torch.zeros((B, V), dtype=torch.bfloat16, device="cuda")
     prm = S.params_tensor(workloads.make_params(B))
