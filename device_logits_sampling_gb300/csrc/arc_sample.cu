@@ -336,7 +336,10 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
         cudaError_t err = prepare(scan, dev, done_s);
         if (err == cudaSuccess) err = prepare(fin, dev, done_f);
         if (err != cudaSuccess) return err;
-        scan<<<static_cast<unsigned>(p.slices), kThreads, p.scan_smem, st>>>(sa);
+        // slices x rows; rows past 65,535 fold into z (grid y is 16-bit)
+        const unsigned gy = static_cast<unsigned>(std::min<int64_t>(B, 65535));
+        const unsigned gz = static_cast<unsigned>((B + gy - 1) / gy);
+        scan<<<dim3(static_cast<unsigned>(p.s), gy, gz), kThreads, p.scan_smem, st>>>(sa);
         err = cudaGetLastError();
         if (err == cudaSuccess) err = launch_cluster(fin, B, 1, p.fin_smem, st, fa, /*early=*/true);
         return err;

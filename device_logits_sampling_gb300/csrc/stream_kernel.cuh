@@ -288,31 +288,67 @@ __device__ __forceinline__ uint64_t block_scan_u64(uint64_t v, uint64_t* red, ui
 }
 
 // ------------------------------------------------------------------ scan
-// What the scan reads of a row besides its logits.
-struct ScanRow {
-    arc_row_params P;
-    int hbeg, hn;
+// Row-level facts every CTA of a row needs, decided once per CTA by warp 0
+// while the slice's loads are in flight.
+enum : uint32_t {
+    kRowArgmax = 1u,  // greedy rows and rows with invalid parameters: slice max and first id
+    kRowChunks = 2u,  // chunk table
+    kRowMass = 4u,    // chunk masses
+    kRowFiltered = 8u,  // chunk max vectors and second vector maxima
 };
-
-template <bool HIST>
-__device__ __forceinline__ ScanRow scan_row_of(const ScanArgs& a, int row) {
-    ScanRow r;
-    // the finish kernel of an earlier call may have rewritten `step`, never
-    // while this kernel runs: plain loads
-    r.P = a.params[row];
-    r.hbeg = 0;
-    r.hn = 0;
-    if (HIST && a.hist_off != nullptr) {
-        r.hbeg = a.hist_off[row];
-        r.hn = a.hist_off[row + 1] - r.hbeg;
-    }
-    return r;
-}
+constexpr int kAmUnknown = INT_MAX;  // slice record of a row whose first max id the scan leaves open
 
 struct ScanShared {
     uint32_t red32[kWarps];
     uint32_t sflags;  // history id errors (written only after a barrier past its init)
+    uint32_t rerr;
+    uint32_t bits;
+    float cT;  // log2(e) / T for rows that need masses
+    int hbeg, hn;
+    arc_row_params P;
 };
+
+template <bool HIST>
+__device__ __forceinline__ void scan_row_setup(const ScanArgs& a, int row, int cidx, ScanShared& sh) {
+    const int lane = threadIdx.x & 31;
+    // the finish kernel of an earlier call may have rewritten `step`, never
+    // while this kernel runs: plain loads
+    const arc_row_params P = a.params[row];
+    uint32_t rerr = param_errors(P);
+    const RowMode md(P, a.V);
+    int hbeg = 0, hn = 0;
+    if (HIST && a.hist_off != nullptr) {
+        hbeg = a.hist_off[row];
+        hn = a.hist_off[row + 1] - hbeg;
+        if (hn < 0) rerr |= ARC_ERR_HIST_ID;
+        if (hn > a.hist_cap) rerr |= ARC_ERR_HIST_CAP;
+    }
+    uint32_t bits = 0;
+    if (rerr != 0 || md.greedy) {
+        bits = kRowArgmax;
+    } else {
+        bits = kRowChunks | (md.need_mass ? kRowMass : 0u) | (md.filtered ? kRowFiltered : 0u);
+        if (HIST) bits |= kRowArgmax;  // penalised rows keep their first max id
+    }
+    if (lane == 0) {
+        // slice 0 of a min-p row: T ln(min_p) in fp64 for the finish kernel
+        // (fp64 is slow on this part: one thread, while the loads are in flight)
+        if (cidx == 0 && (bits & kRowFiltered) && md.minp_on) {
+            unsigned char* note = const_cast<unsigned char*>(reinterpret_cast<const unsigned char*>(
+                slice_note(summary_at(a.summaries, a.s, row, 0))));
+            *reinterpret_cast<double*>(note) = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
+        }
+        sh.rerr = rerr;
+        sh.bits = bits;
+        sh.cT = (bits & kRowMass) ? __fdiv_rn(1.4426950408889634f, P.temperature) : 0.0f;
+        sh.sflags = 0;
+        if (HIST) {
+            sh.P = P;
+            sh.hbeg = hbeg;
+            sh.hn = hn;
+        }
+    }
+}
 
 // sum_e 2^((z_e - ref) c) for a finite ref and NaN-free z, two elements per
 // packed f32x2 add / multiply (same rounding as the scalar operations)
@@ -337,52 +373,58 @@ __device__ __forceinline__ float lane_mass_safe(const float (&z)[VEC], float ref
     return ls;
 }
 
+// Warp max of a NaN-free float.
+__device__ __forceinline__ float warp_max_nonan(float v) {
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Four warp sums at once: lane l ends with the sum over the warp of
+// v[2 * bit4(l) + bit3(l)] (lanes 0, 8, 16, 24 hold sums 0..3).
+__device__ __forceinline__ float warp_sum4(const float (&v)[4], int lane) {
+    const bool h = (lane & 16) != 0;
+    float a0 = h ? v[2] : v[0], a1 = h ? v[3] : v[1];
+    const float s0 = h ? v[0] : v[2], s1 = h ? v[1] : v[3];
+    a0 = __fadd_rn(a0, __shfl_xor_sync(0xFFFFFFFFu, s0, 16));
+    a1 = __fadd_rn(a1, __shfl_xor_sync(0xFFFFFFFFu, s1, 16));
+    const bool q = (lane & 8) != 0;
+    float b = q ? a1 : a0;
+    const float t = q ? a0 : a1;
+    b = __fadd_rn(b, __shfl_xor_sync(0xFFFFFFFFu, t, 8));
+#pragma unroll
+    for (int d = 4; d > 0; d >>= 1) b = __fadd_rn(b, __shfl_xor_sync(0xFFFFFFFFu, b, d));
+    return b;
+}
+
 // One slice, its vectors already in registers (vectors past the slice read
-// as -inf): penalties, slice max and first id, chunk table, header.
+// as -inf): penalties, chunk table, per-warp records.
 template <int DT, bool HIST>
 __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[kVpt], int row, int cidx,
-                                           const ScanRow& R, ScanShared& sh, unsigned char* patch_mem) {
+                                           ScanShared& sh, unsigned char* patch_mem) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
+    static_assert(kVpt == 4, "warp_sum4 pairs the four vectors of a thread with lanes 0, 8, 16, 24");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int a0 = cidx * a.L;
     const int n = min(a0 + a.L, a.V) - a0;  // > 0: the plan makes no empty slice
     const int nv = (n + VEC - 1) / VEC;
-    const char* rowp = static_cast<const char*>(a.logits) + static_cast<int64_t>(row) * a.ld * E::kBytes;
-    const arc_row_params& P = R.P;
-    uint32_t rerr = param_errors(P);
-    const RowMode md(P, a.V);
-    const int hn = R.hn;
-    if (HIST && a.hist_off != nullptr) {
-        if (hn < 0) rerr |= ARC_ERR_HIST_ID;
-        if (hn > a.hist_cap) rerr |= ARC_ERR_HIST_CAP;
-    }
-    const bool need_data = rerr == 0;
-    const bool row_chunks = need_data && !md.greedy;
-    const bool mass = row_chunks && md.need_mass;
-    // slice 0 of a min-p row: T ln(min_p) in fp64 for the finish kernel, by one
-    // thread while the slice's loads are in flight (fp64 is slow on this part)
-    if (cidx == 0 && tid == 0 && row_chunks && md.filtered && md.minp_on) {
-        unsigned char* note = const_cast<unsigned char*>(reinterpret_cast<const unsigned char*>(
-            slice_note(summary_at(a.summaries, a.s, row, 0))));
-        *reinterpret_cast<double*>(note) = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
-    }
-    const float cT = mass ? __fdiv_rn(1.4426950408889634f, P.temperature) : 0.0f;
+    const uint32_t bits = sh.bits;
+    uint32_t rerr = sh.rerr;
 
     const uint32_t* pbm = nullptr;
     const uint32_t* pwp = nullptr;
     const float* ppat = nullptr;
     bool has_patch = false;
-    if (HIST && need_data && hn > 0) {
-        if (tid == 0) sh.sflags = 0;
-        __syncthreads();
+    if (HIST && rerr == 0 && sh.hn > 0) {
+        const char* rowp = static_cast<const char*>(a.logits) + static_cast<int64_t>(row) * a.ld * E::kBytes;
         const int nwords_max = (kVpt * kThreads * VEC + 31) / 32;
         uint32_t* bm = reinterpret_cast<uint32_t*>(patch_mem);
         uint32_t* wp = bm + nwords_max;
         uint32_t* cnt = wp + nwords_max;
         float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
-        const int distinct = build_patches<DT>(rowp, a.V, a0, n, nv, P, a.hist_ids + R.hbeg, hn, bm, wp, cnt, pat,
-                                               sh.red32, &sh.sflags);
+        const int distinct = build_patches<DT>(rowp, a.V, a0, n, nv, sh.P, a.hist_ids + sh.hbeg, sh.hn, bm, wp, cnt,
+                                               pat, sh.red32, &sh.sflags);
         rerr |= sh.sflags & ARC_ERR_HIST_ID;
         pbm = bm;
         pwp = wp;
@@ -399,104 +441,139 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         return ((pbm[l0 >> 5] >> (l0 & 31)) & ((1u << VEC) - 1u)) != 0;
     };
 
-    // per vector: its max with NaN ignored and (rows that need masses) the
-    // lane's weight sum relative to that max; per lane: the best vector.  Per
-    // 32-vector chunk (the warp's vectors j), as soon as they are known: the
-    // chunk max and, when needed, the fp32 sum of weights relative to it (NaN
-    // ids weigh nothing); filtered rows also get the vector holding the max
-    // and the largest max of the other vectors, so that a chunk with one vector
-    // at or above a later floor is re-read as that one 16-byte vector.  Every
-    // entry is written; entries past the slice hold no number.
-    unsigned char* mysum = const_cast<unsigned char*>(summary_at(a.summaries, a.s, row, cidx));
-    ChunkEntry* ch = reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes);
-    float bv = -INFINITY;
-    int bj = -1;
-    bool nanf = false;
+    // vector maxima with NaN ignored (-inf for vectors past the slice)
+    float xs[kVpt];
+    uint32_t vn = 0;  // vectors holding a NaN
 #pragma unroll
     for (int j = 0; j < kVpt; ++j) {
-        const int v = j * kThreads + tid;
-        float x = -INFINITY, l = 0.0f;
-        if (v < nv) {
-            float z[VEC];
-            vals(j, z);
-            x = patched(j) ? z[0] : E::vmax_nan(d[j]);
+        float x = -INFINITY;
+        if (j * kThreads + tid < nv) {
             if (patched(j)) {
+                float z[VEC];
+                vals(j, z);
+                x = z[0];
 #pragma unroll
                 for (int e = 1; e < VEC; ++e) x = fmax_nan(x, z[e]);
+            } else {
+                x = E::vmax_nan(d[j]);
             }
-            const bool vnan = (x != x);
-            if (vnan) {
-                nanf = true;
+            if (x != x) {
+                vn |= 1u << j;
+                float z[VEC];
+                vals(j, z);
                 x = -INFINITY;
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
                     if (z[e] > x) x = z[e];
             }
-            if (x > bv) {
-                bv = x;
-                bj = j;
-            }
-            if (mass && x != -INFINITY)
-                l = (vnan || x == INFINITY) ? lane_mass_safe<VEC>(z, x, cT) : lane_mass_packed<VEC>(z, x, cT);
         }
-        if (row_chunks) {
-            const uint32_t kj = fkey(x);
-            const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, kj);
-            const float mj = key_to_float(kmax);
-            float Sj = 0.0f;
-            if (mass) Sj = warp_sum_f((x != -INFINITY) ? __fmul_rn(l, wrel(x, mj, cT)) : 0.0f);
-            int flane = -1;
-            float u2 = INFINITY;
-            if (md.filtered) {
-                const unsigned holders = __ballot_sync(0xFFFFFFFFu, kj == kmax && x > -INFINITY);
-                flane = holders ? __ffs(holders) - 1 : -1;
-                const uint32_t k2 = __reduce_max_sync(0xFFFFFFFFu, lane == flane ? 0u : kj);
-                u2 = k2 > 0x007FFFFFu ? key_to_float(k2) : -INFINITY;
-            }
-            if (lane == 0) {
-                ChunkEntry ce;
-                ce.m = mj;
-                ce.S = Sj;
-                ce.lane = flane;
-                ce.u2 = u2;
-                ch[j * kWarps + warp] = ce;
-            }
-        }
+        xs[j] = x;
     }
 
-    // slice max and its first id: the warp's best key, then the first id of
-    // it among the lanes that hold it
-    const uint32_t wkey = __reduce_max_sync(0xFFFFFFFFu, fkey(bv));
-    uint32_t mine = 0xFFFFFFFFu;
-    if (bj >= 0 && fkey(bv) == wkey) {
+    unsigned char* mysum = const_cast<unsigned char*>(summary_at(a.summaries, a.s, row, cidx));
+    float wm = -INFINITY;
+    int wam = -1;
+    if (bits & kRowChunks) {
+        // per 32-vector chunk (the warp's vectors j): the chunk max; rows that
+        // need masses: the fp32 sum of weights relative to it (NaN ids weigh
+        // nothing); filtered rows: the vector holding the max first and the
+        // largest max of the other vectors, so that a chunk with one vector at
+        // or above a later floor is re-read as that one 16-byte vector.  Lane
+        // 8j writes entry j.  Every entry is written; entries past the slice
+        // hold no number.
+        float mj[kVpt];
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) mj[j] = warp_max_nonan(xs[j]);
+        float S = 0.0f;
+        if (bits & kRowMass) {
+            const float cT = sh.cT;
+            float sl[kVpt];
+#pragma unroll
+            for (int j = 0; j < kVpt; ++j) {
+                float l = 0.0f;
+                if (xs[j] != -INFINITY) {  // then mj[j] >= xs[j] > -inf
+                    float z[VEC];
+                    vals(j, z);
+                    l = (((vn >> j) & 1u) || mj[j] == INFINITY) ? lane_mass_safe<VEC>(z, mj[j], cT)
+                                                                : lane_mass_packed<VEC>(z, mj[j], cT);
+                }
+                sl[j] = l;
+            }
+            S = warp_sum4(sl, lane);
+        }
+        int fl[kVpt];
+        float u2[kVpt];
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) {
-            if (j == bj) {
-                float z[VEC];
-                vals(j, z);
-                int e0 = VEC - 1;
+            fl[j] = -1;
+            u2[j] = INFINITY;
+        }
+        if (bits & kRowFiltered) {
 #pragma unroll
-                for (int e = VEC - 1; e >= 0; --e)
-                    if (z[e] == bv) e0 = e;
-                mine = static_cast<uint32_t>(a0 + (j * kThreads + tid) * VEC + e0);
+            for (int j = 0; j < kVpt; ++j) {
+                const unsigned holders = __ballot_sync(0xFFFFFFFFu, xs[j] == mj[j] && xs[j] > -INFINITY);
+                fl[j] = holders ? __ffs(holders) - 1 : -1;
+                u2[j] = warp_max_nonan(lane == fl[j] ? -INFINITY : xs[j]);
             }
         }
+        if ((lane & 7) == 0) {
+            const int j = lane >> 3;
+            ChunkEntry ce;
+            ce.m = j == 0 ? mj[0] : (j == 1 ? mj[1] : (j == 2 ? mj[2] : mj[3]));
+            ce.S = S;
+            ce.lane = j == 0 ? fl[0] : (j == 1 ? fl[1] : (j == 2 ? fl[2] : fl[3]));
+            ce.u2 = j == 0 ? u2[0] : (j == 1 ? u2[1] : (j == 2 ? u2[2] : u2[3]));
+            reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes)[j * kWarps + warp] = ce;
+        }
+        wm = fmaxf(fmaxf(mj[0], mj[1]), fmaxf(mj[2], mj[3]));
+        wam = wm > -INFINITY ? kAmUnknown : -1;
     }
-    const uint32_t wid = __reduce_min_sync(0xFFFFFFFFu, mine);
-    const bool wnan = __any_sync(0xFFFFFFFFu, nanf);
+    if (bits & kRowArgmax) {
+        // the warp's max and its first id: the best key, then the first id of
+        // it among the lanes that hold it
+        float bv = -INFINITY;
+        int bj = -1;
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j)
+            if (xs[j] > bv) {
+                bv = xs[j];
+                bj = j;
+            }
+        const float wv = warp_max_nonan(bv);
+        uint32_t mine = 0xFFFFFFFFu;
+        if (bj >= 0 && bv == wv) {
+#pragma unroll
+            for (int j = 0; j < kVpt; ++j) {
+                if (j == bj) {
+                    float z[VEC];
+                    vals(j, z);
+                    int e0 = VEC - 1;
+#pragma unroll
+                    for (int e = VEC - 1; e >= 0; --e)
+                        if (z[e] == bv) e0 = e;
+                    mine = static_cast<uint32_t>(a0 + (j * kThreads + tid) * VEC + e0);
+                }
+            }
+        }
+        const uint32_t wid = __reduce_min_sync(0xFFFFFFFFu, mine);
+        wm = (wid == 0xFFFFFFFFu) ? -INFINITY : wv;
+        wam = (wid == 0xFFFFFFFFu) ? -1 : static_cast<int>(wid);
+    }
+    const bool wnan = __any_sync(0xFFFFFFFFu, vn != 0);
     if (lane == 0) {
         WarpRecord r;
-        r.m = (wid == 0xFFFFFFFFu) ? -INFINITY : key_to_float(wkey);
-        r.am = (wid == 0xFFFFFFFFu) ? -1 : static_cast<int>(wid);
+        r.m = wm;
+        r.am = wam;
         r.flags = (wnan ? ARC_ERR_NAN : 0u) | (rerr & (ARC_ERR_HIST_ID | ARC_ERR_HIST_CAP));
         r.pad = 0;
         reinterpret_cast<WarpRecord*>(mysum)[warp] = r;
     }
 }
 
-// One CTA per slice: every 16-byte load of the slice is issued first (they
-// depend on nothing), then the row's parameters; registers stay few so that
-// many CTAs per SM keep enough bytes in flight.
+// One CTA per slice (grid: slices x rows, rows past 65,535 folded into z):
+// every 16-byte load of the slice is issued first (they depend on nothing),
+// then warp 0 reads the row's parameters; registers stay few so that many
+// CTAs per SM keep enough bytes in flight.
 template <int DT, bool HIST>
 __global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const ScanArgs a) {
     using E = Elem<DT>;
@@ -508,8 +585,9 @@ __global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const Scan
     // the summaries
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
-    const int row = static_cast<int>(blockIdx.x) / a.s;
-    const int cidx = static_cast<int>(blockIdx.x) - row * a.s;
+    const int row = static_cast<int>(blockIdx.z * gridDim.y + blockIdx.y);
+    if (row >= a.B) return;  // the whole CTA, before any barrier
+    const int cidx = static_cast<int>(blockIdx.x);
     const int a0 = cidx * a.L;
     const int n = min(a0 + a.L, a.V) - a0;
     const int nv = (n + VEC - 1) / VEC;
@@ -523,8 +601,9 @@ __global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const Scan
         const int v = j * kThreads + tid;
         d[j] = (v < nv) ? E::global_vec(sp, v, n, a.aligned) : ninf;
     }
-    const ScanRow R = scan_row_of<HIST>(a, row);
-    scan_slice<DT, HIST>(a, d, row, cidx, R, sh, dyn);
+    if (tid < 32) scan_row_setup<HIST>(a, row, cidx, sh);
+    __syncthreads();
+    scan_slice<DT, HIST>(a, d, row, cidx, sh, dyn);
 }
 
 // ------------------------------------------------------------------ finish helpers
@@ -646,10 +725,30 @@ __device__ bool floor_block(int n, KW kw, uint32_t tgt, FinishScratch& SS, uint3
 }
 
 // ------------------------------------------------------------------ finish
+// First id of the row max m (NaN ignored) for a row whose scan left it open
+// (rows without history): the first chunk, in id order, whose max is m,
+// re-read by the calling thread alone.  Only error and rounding fallbacks
+// need it.
+template <int DT>
+__device__ __noinline__ int first_max_id(const FinishArgs& a, const char* rowp, const float* cm, int nch, float m) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    const uint32_t km = fkey(m);
+    for (int g = 0; g < nch; ++g) {
+        if (!(cm[g] > -INFINITY) || fkey(cm[g]) != km) continue;
+        const int c = g / kChunks, jr = g % kChunks;
+        const int ca0 = c * a.L, cn = min(ca0 + a.L, a.V) - ca0;
+        const int v0 = (jr / kWarps) * kThreads + (jr % kWarps) * 32;
+        for (int i = v0 * VEC; i < min(cn, (v0 + 32) * VEC); ++i)
+            if (E::load_scalar(rowp, ca0 + i) == m) return ca0 + i;
+    }
+    return 0;
+}
+
 // What the steps of one row's finish share, and what they report.
 struct RowState {
     float m;         // row max of the penalised logits
-    int am;          // its first id
+    int am;          // its first id (kAmUnknown: not recorded by the scan)
     float cT;        // log2(e) / T
     float scale;     // 2^F: fixed-point unit of a weight
     float zm;        // min-p threshold (z >= zm survives), -inf when off
@@ -792,7 +891,7 @@ __device__ __noinline__ void finish_general(const FinishArgs& a, const arc_row_p
         st.target, [&](const float(&z)[VEC], int g0) { return X.vec_mass(mr, z, g0, R); },
         [&](const float(&z)[VEC], int g0, uint64_t tt) { return X.vec_mass_walk(mr, z, g0, R, tt); });
     if (tok < 0) {
-        tok = st.am;
+        tok = st.am != kAmUnknown ? st.am : first_max_id<DT>(a, rowp, cm, a.s * kChunks, m);
         err |= kErrInternal;
     }
     st.token = tok;
@@ -930,6 +1029,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
         }
     }
     const float m = st.m, cT = st.cT;
+    // the row max's first id where a fallback needs it
+    auto max_id = [&]() { return st.am != kAmUnknown ? st.am : first_max_id<DT>(a, rowp, cm, nch, m); };
     auto fixq = [&](float w) { return __float2ull_rn(__fmul_rn(w, st.scale)); };
     // a chunk's fixed-point mass, rescaled from its own max to the row max
     auto chunk_q = [&](int e) -> uint64_t {
@@ -970,7 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
             const uint64_t hit_before = SS.bu[2];
             if (hit < 0) {
                 st.err |= kErrInternal;
-                st.token = st.am;
+                st.token = max_id();
             } else if (warp == 0) {
                 // re-read the chunk (32 vectors) and walk it
                 const int c = hit / kChunks, jr = hit % kChunks;
@@ -1053,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
             }
             __syncthreads();
             if (hit >= 0) st.token = SS.bi[3];
-            if (st.token == -3) st.token = st.am;
+            if (st.token == -3) st.token = max_id();
         } else {
             // ---------------------------------------------------------- filtered rows
             const float zm = st.zm;
@@ -1369,7 +1470,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a)
                 __syncthreads();
                 st.token = SS.bi[6];
                 if (st.token < 0) {
-                    st.token = st.am;
+                    st.token = max_id();
                     st.err |= kErrInternal;
                 }
             } else {
