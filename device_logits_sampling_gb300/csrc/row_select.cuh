@@ -361,13 +361,8 @@ struct RowCtx {
     }
 };
 
-// Row parameters, read once with volatile loads so that no field is fetched
-// after the first cluster barrier (rank 0 may rewrite `step` after it).
-__device__ __forceinline__ arc_row_params load_params(const arc_row_params* p) {
-    const volatile uint64_t* q = reinterpret_cast<const volatile uint64_t*>(p);
-    uint64_t w[6];
-#pragma unroll
-    for (int i = 0; i < 6; ++i) w[i] = q[i];
+// The parameter record from its six 64-bit words.
+__device__ __forceinline__ arc_row_params params_from_words(const uint64_t (&w)[6]) {
     arc_row_params r;
     r.temperature = __uint_as_float(static_cast<uint32_t>(w[0]));
     r.top_k = static_cast<int32_t>(w[0] >> 32);
@@ -380,6 +375,15 @@ __device__ __forceinline__ arc_row_params load_params(const arc_row_params* p) {
     r.seed = w[4];
     r.step = w[5];
     return r;
+}
+// Row parameters, read once with volatile loads so that no field is fetched
+// after the first cluster barrier (rank 0 may rewrite `step` after it).
+__device__ __forceinline__ arc_row_params load_params(const arc_row_params* p) {
+    const volatile uint64_t* q = reinterpret_cast<const volatile uint64_t*>(p);
+    uint64_t w[6];
+#pragma unroll
+    for (int i = 0; i < 6; ++i) w[i] = q[i];
+    return params_from_words(w);
 }
 
 // Key range [lo, hi] of histogram bin `b` of window W.

@@ -295,6 +295,7 @@ enum : uint32_t {
     kRowChunks = 2u,  // chunk table
     kRowMass = 4u,    // chunk masses
     kRowFiltered = 8u,  // chunk max vectors and second vector maxima
+    kRowNote = 16u,     // min-p rows: slice 0 writes T ln(min_p)
 };
 constexpr int kAmUnknown = INT_MAX;  // slice record of a row whose first max id the scan leaves open
 
@@ -308,12 +309,20 @@ struct ScanShared {
     arc_row_params P;
 };
 
+// The row's parameter record as six 64-bit words through the non-coherent
+// path: the finish kernel of an earlier call may have rewritten `step`, never
+// while this kernel runs.  Volatile, so that these loads go out before the
+// slice's.
+__device__ __forceinline__ void params_words_nc(const arc_row_params* p, uint64_t (&w)[6]) {
+    const uint64_t* q = reinterpret_cast<const uint64_t*>(p);
+#pragma unroll
+    for (int i = 0; i < 6; ++i) asm volatile("ld.global.nc.u64 %0, [%1];" : "=l"(w[i]) : "l"(q + i));
+}
+
 template <bool HIST>
-__device__ __forceinline__ void scan_row_setup(const ScanArgs& a, int row, int cidx, ScanShared& sh) {
+__device__ __forceinline__ void scan_row_setup(const ScanArgs& a, int row, const uint64_t (&pw)[6], ScanShared& sh) {
     const int lane = threadIdx.x & 31;
-    // the finish kernel of an earlier call may have rewritten `step`, never
-    // while this kernel runs: plain loads
-    const arc_row_params P = a.params[row];
+    const arc_row_params P = params_from_words(pw);
     uint32_t rerr = param_errors(P);
     const RowMode md(P, a.V);
     int hbeg = 0, hn = 0;
@@ -328,25 +337,17 @@ __device__ __forceinline__ void scan_row_setup(const ScanArgs& a, int row, int c
         bits = kRowArgmax;
     } else {
         bits = kRowChunks | (md.need_mass ? kRowMass : 0u) | (md.filtered ? kRowFiltered : 0u);
+        if (md.filtered && md.minp_on) bits |= kRowNote;
         if (HIST) bits |= kRowArgmax;  // penalised rows keep their first max id
     }
     if (lane == 0) {
-        // slice 0 of a min-p row: T ln(min_p) in fp64 for the finish kernel
-        // (fp64 is slow on this part: one thread, while the loads are in flight)
-        if (cidx == 0 && (bits & kRowFiltered) && md.minp_on) {
-            unsigned char* note = const_cast<unsigned char*>(reinterpret_cast<const unsigned char*>(
-                slice_note(summary_at(a.summaries, a.s, row, 0))));
-            *reinterpret_cast<double*>(note) = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
-        }
         sh.rerr = rerr;
         sh.bits = bits;
         sh.cT = (bits & kRowMass) ? __fdiv_rn(1.4426950408889634f, P.temperature) : 0.0f;
         sh.sflags = 0;
-        if (HIST) {
-            sh.P = P;
-            sh.hbeg = hbeg;
-            sh.hn = hn;
-        }
+        sh.P = P;
+        sh.hbeg = hbeg;
+        sh.hn = hn;
     }
 }
 
@@ -540,24 +541,28 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
                 bj = j;
             }
         const float wv = warp_max_nonan(bv);
-        uint32_t mine = 0xFFFFFFFFu;
-        if (bj >= 0 && bv == wv) {
+        // ids of a warp run vector-major: the holder with the smallest
+        // (vector, lane) has the first id of wv, in its first element equal to it
+        const uint32_t code = (bj >= 0 && bv == wv) ? static_cast<uint32_t>(bj * 32 + lane) : 0xFFFFFFFFu;
+        const uint32_t wc = __reduce_min_sync(0xFFFFFFFFu, code);
+        int wid = -1;
+        if (wc != 0xFFFFFFFFu) {
+            const int jw = static_cast<int>(wc >> 5), lw = static_cast<int>(wc & 31u);
+            if (lane == lw) {
+                const uint4 dv = jw == 0 ? d[0] : (jw == 1 ? d[1] : (jw == 2 ? d[2] : d[3]));
+                float z[VEC];
+                E::unpack(dv, z);
+                if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, jw * kThreads + tid, z);
+                int e0 = VEC - 1;
 #pragma unroll
-            for (int j = 0; j < kVpt; ++j) {
-                if (j == bj) {
-                    float z[VEC];
-                    vals(j, z);
-                    int e0 = VEC - 1;
-#pragma unroll
-                    for (int e = VEC - 1; e >= 0; --e)
-                        if (z[e] == bv) e0 = e;
-                    mine = static_cast<uint32_t>(a0 + (j * kThreads + tid) * VEC + e0);
-                }
+                for (int e = VEC - 1; e >= 0; --e)
+                    if (z[e] == wv) e0 = e;
+                wid = a0 + (jw * kThreads + tid) * VEC + e0;
             }
+            wid = __shfl_sync(0xFFFFFFFFu, wid, lw);
         }
-        const uint32_t wid = __reduce_min_sync(0xFFFFFFFFu, mine);
-        wm = (wid == 0xFFFFFFFFu) ? -INFINITY : wv;
-        wam = (wid == 0xFFFFFFFFu) ? -1 : static_cast<int>(wid);
+        wm = (wid < 0) ? -INFINITY : wv;
+        wam = wid;
     }
     const bool wnan = __any_sync(0xFFFFFFFFu, vn != 0);
     if (lane == 0) {
@@ -595,15 +600,24 @@ __global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const Scan
                      (static_cast<int64_t>(row) * a.ld + static_cast<int64_t>(a0)) * E::kBytes;
     const uint4 ninf = (DT == ARC_BF16) ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
                                         : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+    uint64_t pw[6];
+    if (tid < 32) params_words_nc(a.params + row, pw);
     uint4 d[kVpt];
 #pragma unroll
     for (int j = 0; j < kVpt; ++j) {
         const int v = j * kThreads + tid;
         d[j] = (v < nv) ? E::global_vec(sp, v, n, a.aligned) : ninf;
     }
-    if (tid < 32) scan_row_setup<HIST>(a, row, cidx, sh);
+    if (tid < 32) scan_row_setup<HIST>(a, row, pw, sh);
     __syncthreads();
     scan_slice<DT, HIST>(a, d, row, cidx, sh, dyn);
+    // slice 0 of a min-p row: T ln(min_p) in fp64 for the finish kernel, by
+    // one thread after its slice (fp64 is slow on this part)
+    if (cidx == 0 && tid == 0 && (sh.bits & kRowNote)) {
+        unsigned char* note = const_cast<unsigned char*>(
+            reinterpret_cast<const unsigned char*>(slice_note(summary_at(a.summaries, a.s, row, 0))));
+        *reinterpret_cast<double*>(note) = static_cast<double>(sh.P.temperature) * log(static_cast<double>(sh.P.min_p));
+    }
 }
 
 // ------------------------------------------------------------------ finish helpers
