@@ -302,53 +302,61 @@ constexpr int kAmUnknown = INT_MAX;  // slice record of a row whose first max id
 struct ScanShared {
     uint32_t red32[kWarps];
     uint32_t sflags;  // history id errors (written only after a barrier past its init)
-    uint32_t rerr;
-    uint32_t bits;
-    float cT;  // log2(e) / T for rows that need masses
-    int hbeg, hn;
-    arc_row_params P;
 };
 
-// The row's parameter record as six 64-bit words through the non-coherent
-// path: the finish kernel of an earlier call may have rewritten `step`, never
-// while this kernel runs.  Volatile, so that these loads go out before the
+// What the scan does for a row, decoded by every thread from its parameter
+// record: no barrier, no validation.  Rows with invalid parameters are
+// rejected by the finish kernel, which reads nothing the scan wrote for them
+// but the error flags; only a history length outside [0, cap] must keep the
+// scan from building penalties.
+struct ScanRowInfo {
+    uint32_t bits;
+    uint32_t rerr;  // history length errors
+    float cT;       // log2(e) / T for rows that need masses
+    arc_row_params P;
+    int hbeg, hn;
+};
+
+// The row's parameter record through the non-coherent path (the finish kernel
+// of an earlier call may have rewritten `step`, never while this kernel
+// runs): the first two words (temperature, top_k, top_p, min_p), or all six
+// for rows with history.  Volatile, so that these loads go out before the
 // slice's.
+template <bool HIST>
 __device__ __forceinline__ void params_words_nc(const arc_row_params* p, uint64_t (&w)[6]) {
     const uint64_t* q = reinterpret_cast<const uint64_t*>(p);
 #pragma unroll
-    for (int i = 0; i < 6; ++i) asm volatile("ld.global.nc.u64 %0, [%1];" : "=l"(w[i]) : "l"(q + i));
+    for (int i = 0; i < 6; ++i) {
+        if (i < 2 || HIST)
+            asm volatile("ld.global.nc.u64 %0, [%1];" : "=l"(w[i]) : "l"(q + i));
+        else
+            w[i] = 0;
+    }
 }
 
 template <bool HIST>
-__device__ __forceinline__ void scan_row_setup(const ScanArgs& a, int row, const uint64_t (&pw)[6], ScanShared& sh) {
-    const int lane = threadIdx.x & 31;
-    const arc_row_params P = params_from_words(pw);
-    uint32_t rerr = param_errors(P);
-    const RowMode md(P, a.V);
-    int hbeg = 0, hn = 0;
+__device__ __forceinline__ ScanRowInfo scan_row_info(const ScanArgs& a, int row, const uint64_t (&pw)[6]) {
+    ScanRowInfo R;
+    R.P = params_from_words(pw);
+    const RowMode md(R.P, a.V);  // reads temperature, top_k, top_p and min_p only
+    R.rerr = 0;
+    R.hbeg = 0;
+    R.hn = 0;
     if (HIST && a.hist_off != nullptr) {
-        hbeg = a.hist_off[row];
-        hn = a.hist_off[row + 1] - hbeg;
-        if (hn < 0) rerr |= ARC_ERR_HIST_ID;
-        if (hn > a.hist_cap) rerr |= ARC_ERR_HIST_CAP;
+        R.hbeg = a.hist_off[row];
+        R.hn = a.hist_off[row + 1] - R.hbeg;
+        if (R.hn < 0) R.rerr |= ARC_ERR_HIST_ID;
+        if (R.hn > a.hist_cap) R.rerr |= ARC_ERR_HIST_CAP;
     }
-    uint32_t bits = 0;
-    if (rerr != 0 || md.greedy) {
-        bits = kRowArgmax;
+    if (R.rerr != 0 || md.greedy) {
+        R.bits = kRowArgmax;
     } else {
-        bits = kRowChunks | (md.need_mass ? kRowMass : 0u) | (md.filtered ? kRowFiltered : 0u);
-        if (md.filtered && md.minp_on) bits |= kRowNote;
-        if (HIST) bits |= kRowArgmax;  // penalised rows keep their first max id
+        R.bits = kRowChunks | (md.need_mass ? kRowMass : 0u) | (md.filtered ? kRowFiltered : 0u);
+        if (md.filtered && md.minp_on) R.bits |= kRowNote;
+        if (HIST) R.bits |= kRowArgmax;  // penalised rows keep their first max id
     }
-    if (lane == 0) {
-        sh.rerr = rerr;
-        sh.bits = bits;
-        sh.cT = (bits & kRowMass) ? __fdiv_rn(1.4426950408889634f, P.temperature) : 0.0f;
-        sh.sflags = 0;
-        sh.P = P;
-        sh.hbeg = hbeg;
-        sh.hn = hn;
-    }
+    R.cT = (R.bits & kRowMass) ? __fdiv_rn(1.4426950408889634f, R.P.temperature) : 0.0f;
+    return R;
 }
 
 // sum_e 2^((z_e - ref) c) for a finite ref and NaN-free z, two elements per
@@ -402,7 +410,7 @@ __device__ __forceinline__ float warp_sum4(const float (&v)[4], int lane) {
 // as -inf): penalties, chunk table, per-warp records.
 template <int DT, bool HIST>
 __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[kVpt], int row, int cidx,
-                                           ScanShared& sh, unsigned char* patch_mem) {
+                                           const ScanRowInfo& R, ScanShared& sh, unsigned char* patch_mem) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     static_assert(kVpt == 4, "warp_sum4 pairs the four vectors of a thread with lanes 0, 8, 16, 24");
@@ -410,21 +418,23 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
     const int a0 = cidx * a.L;
     const int n = min(a0 + a.L, a.V) - a0;  // > 0: the plan makes no empty slice
     const int nv = (n + VEC - 1) / VEC;
-    const uint32_t bits = sh.bits;
-    uint32_t rerr = sh.rerr;
+    const uint32_t bits = R.bits;
+    uint32_t rerr = R.rerr;
 
     const uint32_t* pbm = nullptr;
     const uint32_t* pwp = nullptr;
     const float* ppat = nullptr;
     bool has_patch = false;
-    if (HIST && rerr == 0 && sh.hn > 0) {
+    if (HIST && rerr == 0 && R.hn > 0) {
+        if (threadIdx.x == 0) sh.sflags = 0;
+        __syncthreads();
         const char* rowp = static_cast<const char*>(a.logits) + static_cast<int64_t>(row) * a.ld * E::kBytes;
         const int nwords_max = (kVpt * kThreads * VEC + 31) / 32;
         uint32_t* bm = reinterpret_cast<uint32_t*>(patch_mem);
         uint32_t* wp = bm + nwords_max;
         uint32_t* cnt = wp + nwords_max;
         float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
-        const int distinct = build_patches<DT>(rowp, a.V, a0, n, nv, sh.P, a.hist_ids + sh.hbeg, sh.hn, bm, wp, cnt,
+        const int distinct = build_patches<DT>(rowp, a.V, a0, n, nv, R.P, a.hist_ids + R.hbeg, R.hn, bm, wp, cnt,
                                                pat, sh.red32, &sh.sflags);
         rerr |= sh.sflags & ARC_ERR_HIST_ID;
         pbm = bm;
@@ -487,7 +497,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         for (int j = 0; j < kVpt; ++j) mj[j] = warp_max_nonan(xs[j]);
         float S = 0.0f;
         if (bits & kRowMass) {
-            const float cT = sh.cT;
+            const float cT = R.cT;
             float sl[kVpt];
 #pragma unroll
             for (int j = 0; j < kVpt; ++j) {
@@ -576,8 +586,9 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
 }
 
 // One CTA per slice (grid: slices x rows, rows past 65,535 folded into z):
-// every 16-byte load of the slice is issued first (they depend on nothing),
-// then warp 0 reads the row's parameters; registers stay few so that many
+// the row's parameter words and every 16-byte load of the slice are issued
+// first (they depend on nothing); the warps share nothing and meet at no
+// barrier (rows with history excepted), and registers stay few so that many
 // CTAs per SM keep enough bytes in flight.
 template <int DT, bool HIST>
 __global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const ScanArgs a) {
@@ -601,22 +612,21 @@ __global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const Scan
     const uint4 ninf = (DT == ARC_BF16) ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
                                         : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
     uint64_t pw[6];
-    if (tid < 32) params_words_nc(a.params + row, pw);
+    params_words_nc<HIST>(a.params + row, pw);
     uint4 d[kVpt];
 #pragma unroll
     for (int j = 0; j < kVpt; ++j) {
         const int v = j * kThreads + tid;
         d[j] = (v < nv) ? E::global_vec(sp, v, n, a.aligned) : ninf;
     }
-    if (tid < 32) scan_row_setup<HIST>(a, row, pw, sh);
-    __syncthreads();
-    scan_slice<DT, HIST>(a, d, row, cidx, sh, dyn);
+    const ScanRowInfo R = scan_row_info<HIST>(a, row, pw);
+    scan_slice<DT, HIST>(a, d, row, cidx, R, sh, dyn);
     // slice 0 of a min-p row: T ln(min_p) in fp64 for the finish kernel, by
     // one thread after its slice (fp64 is slow on this part)
-    if (cidx == 0 && tid == 0 && (sh.bits & kRowNote)) {
+    if (cidx == 0 && tid == 0 && (R.bits & kRowNote)) {
         unsigned char* note = const_cast<unsigned char*>(
             reinterpret_cast<const unsigned char*>(slice_note(summary_at(a.summaries, a.s, row, 0))));
-        *reinterpret_cast<double*>(note) = static_cast<double>(sh.P.temperature) * log(static_cast<double>(sh.P.min_p));
+        *reinterpret_cast<double*>(note) = static_cast<double>(R.P.temperature) * log(static_cast<double>(R.P.min_p));
     }
 }
 
