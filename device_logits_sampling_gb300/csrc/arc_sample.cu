@@ -154,8 +154,12 @@ int num_sms_of(int dev) {
 
 // Function attributes are set once per (device, kernel): the first call on a
 // device must come before any stream capture that contains a call.
+// `carveout` is the preferred shared-memory share of the SM's L1/shared
+// storage in percent: 0 for the streaming kernels, which use (almost) no
+// shared memory and keep more loads in flight with a larger L1, 100 for
+// the kernels that stage rows or penalty tables in shared memory.
 template <class K>
-cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done) {
+cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done, int carveout) {
     const uint64_t bit = uint64_t{1} << (dev & 63);
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -163,7 +167,7 @@ cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
     if (e != cudaSuccess) return e;
     done.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
@@ -333,8 +337,8 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto go = [&](auto scan, auto fin, std::atomic<uint64_t>& done_s, std::atomic<uint64_t>& done_f) {
-        cudaError_t err = prepare(scan, dev, done_s);
-        if (err == cudaSuccess) err = prepare(fin, dev, done_f);
+        cudaError_t err = prepare(scan, dev, done_s, has_hist ? 100 : 0);
+        if (err == cudaSuccess) err = prepare(fin, dev, done_f, 100);
         if (err != cudaSuccess) return err;
         // slices x rows; rows past 65,535 fold into z (grid y is 16-bit)
         const unsigned gy = static_cast<unsigned>(std::min<int64_t>(B, 65535));
@@ -406,10 +410,10 @@ int arc_sample_greedy(const void* logits, int64_t B, int64_t V, int64_t ld, int3
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dtype == ARC_BF16) {
-        e = prepare(argmax_kernel<ARC_BF16>, dev, g_prep_argmax[1]);
+        e = prepare(argmax_kernel<ARC_BF16>, dev, g_prep_argmax[1], 0);
         if (e == cudaSuccess) e = launch_cluster(argmax_kernel<ARC_BF16>, B * s, s, 0, st, a);
     } else {
-        e = prepare(argmax_kernel<ARC_F32>, dev, g_prep_argmax[0]);
+        e = prepare(argmax_kernel<ARC_F32>, dev, g_prep_argmax[0], 0);
         if (e == cudaSuccess) e = launch_cluster(argmax_kernel<ARC_F32>, B * s, s, 0, st, a);
     }
     return e == cudaSuccess ? ARC_OK : ARC_E_CUDA;
