@@ -789,9 +789,10 @@ struct RowState {
 // Exact selection over the row in global memory by multi-way threshold
 // bisection (row_select.cuh), skipping every 32-vector chunk whose max lies
 // below a pass's threshold: the path for rows whose floor admits too many
-// ids.  Kept out of line so that the direct path stays compact.
+// ids.  Inlined: out of line, the row state, parameters and mode it takes by
+// reference would live in local memory for the whole kernel.
 template <int DT, bool HIST>
-__device__ __noinline__ void finish_general(const FinishArgs& a, const arc_row_params& P, const RowMode& md, int row,
+__device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_row_params& P, const RowMode& md, int row,
                                             const char* rowp, float* cm, const uint32_t* pbm, const uint32_t* pwp,
                                             const float* ppat, bool has_patch, KernelShared& KS, unsigned char* dyn,
                                             RowState& st) {
@@ -925,7 +926,7 @@ __device__ __noinline__ void finish_general(const FinishArgs& a, const arc_row_p
 
 // One CTA per row.
 template <int DT, bool HIST>
-__global__ void __launch_bounds__(kThreads, 2) finish_kernel(const FinishArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_constant__ FinishArgs a) {
     using E = Elem<DT>;
     using Ctx = RowCtx<DT, HIST>;
     constexpr int VEC = E::kVec;
