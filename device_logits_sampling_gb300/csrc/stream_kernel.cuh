@@ -373,6 +373,28 @@ __device__ __forceinline__ float lane_mass_packed(const float (&z)[VEC], float r
     return __fadd_rn(acc.x, acc.y);
 }
 
+// The same for 8 bf16 logits held raw in a 16-byte vector: z - ref by
+// mixed-precision subtraction (the bf16 operand is exact, one rounding, as
+// unpacking then subtracting), then the same products, powers and sums.
+__device__ __forceinline__ float lane_mass_bf16(const uint4& v, float ref, float c) {
+    float t[8];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "sub.rn.f32.bf16 %0, lo, %3;\n\tsub.rn.f32.bf16 %1, hi, %3;\n\t}"
+            : "=f"(t[2 * i]), "=f"(t[2 * i + 1])
+            : "r"(w[i]), "f"(ref));
+    const float2 c2 = make_float2(c, c);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const float2 x = __fmul2_rn(make_float2(t[e], t[e + 1]), c2);
+        acc = __fadd2_rn(acc, make_float2(ex2(x.x), ex2(x.y)));
+    }
+    return __fadd_rn(acc.x, acc.y);
+}
+
 // The same with NaN ids weighing nothing and an infinite ref handled.
 template <int VEC>
 __device__ __forceinline__ float lane_mass_safe(const float (&z)[VEC], float ref, float c) {
@@ -503,10 +525,14 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
             for (int j = 0; j < kVpt; ++j) {
                 float l = 0.0f;
                 if (xs[j] != -INFINITY) {  // then mj[j] >= xs[j] > -inf
-                    float z[VEC];
-                    vals(j, z);
-                    l = (((vn >> j) & 1u) || mj[j] == INFINITY) ? lane_mass_safe<VEC>(z, mj[j], cT)
-                                                                : lane_mass_packed<VEC>(z, mj[j], cT);
+                    if (DT == ARC_BF16 && !patched(j) && !((vn >> j) & 1u) && mj[j] != INFINITY) {
+                        l = lane_mass_bf16(d[j], mj[j], cT);
+                    } else {
+                        float z[VEC];
+                        vals(j, z);
+                        l = (((vn >> j) & 1u) || mj[j] == INFINITY) ? lane_mass_safe<VEC>(z, mj[j], cT)
+                                                                    : lane_mass_packed<VEC>(z, mj[j], cT);
+                    }
                 }
                 sl[j] = l;
             }
