@@ -679,20 +679,22 @@ __device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kHB = 256;
     constexpr float kStep = 8.0f;  // bins per logit unit
-    for (int b = tid; b < kHB; b += kThreads) hist[b] = 0u;
+    // bin b at b + b / 8: warp 0 reads its lanes' 8-bin runs without bank conflicts
+    auto at = [](int b) { return b + (b >> 3); };
+    for (int b = tid; b < kHB + kHB / 8; b += kThreads) hist[b] = 0u;
     __syncthreads();
     for (int e = tid; e < n; e += kThreads) {
         float x;
         uint32_t w;
         kw(e, x, w);
         const float d = __fmul_rn(__fsub_rn(m, x), kStep);  // >= 0; NaN-free
-        if (w != 0u && d < static_cast<float>(kHB)) atomicAdd(&hist[static_cast<int>(d)], w);
+        if (w != 0u && d < static_cast<float>(kHB)) atomicAdd(&hist[at(static_cast<int>(d))], w);
     }
     __syncthreads();
     if (warp == 0) {
         uint32_t loc = 0;
 #pragma unroll
-        for (int q = 0; q < kHB / 32; ++q) loc += hist[lane * (kHB / 32) + q];
+        for (int q = 0; q < kHB / 32; ++q) loc += hist[at(lane * (kHB / 32) + q)];
         uint32_t inc = loc;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -704,7 +706,7 @@ __device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, 
             uint32_t run = inc - loc;
 #pragma unroll
             for (int q = 0; q < kHB / 32; ++q) {
-                run += hist[lane * (kHB / 32) + q];
+                run += hist[at(lane * (kHB / 32) + q)];
                 if (bin < 0 && run >= tgt) bin = lane * (kHB / 32) + q;
             }
         }
@@ -1281,8 +1283,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
             if (tid == 0) SS.ccount = 0;
             __syncthreads();
 
-            // gather the ids >= zf as (key, id, mass): warp w takes the chunks w,
-            // w + 8, ... whose max is >= zf, stages up to kCollectU of them at a
+            // gather the ids >= zf as (key, id, mass): each warp takes the chunks
+            // of its eighth whose max is >= zf, stages up to kCollectU of them at a
             // time in shared memory with 16-byte asynchronous copies (all in
             // flight together); the ids found take slots from one counter, one
             // atomic per warp and element position
@@ -1297,15 +1299,17 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                 const int Lv = a.L / VEC;
                 uint4* stage = reinterpret_cast<uint4*>(dyn + a.stage_off) + warp * (kCollectU * 32);
                 int* wl = reinterpret_cast<int*>(dyn + a.clist_off) + warp * ((nch + kWarps - 1) / kWarps);
-                // classify this warp's chunks w, w + 8, ... at or above zf: "single"
-                // when the other vectors lie below zf (only the max's vector can
-                // hold ids >= zf), else "whole"; lists from both ends of wl
+                // classify this warp's chunks (a contiguous eighth of the table,
+                // read without bank conflicts) at or above zf: "single" when the
+                // other vectors lie below zf (only the max's vector can hold ids
+                // >= zf), else "whole"; lists from both ends of wl
                 const int wcap = (nch + kWarps - 1) / kWarps;
                 const unsigned below = (1u << lane) - 1u;
                 int nsg = 0, nw = 0;
-                for (int b0 = warp; b0 < nch; b0 += kWarps * 32) {
-                    const int g = b0 + lane * kWarps;
-                    const bool in = g < nch && cm[g] >= zf;
+                const int gw0 = warp * wcap, gw1 = min(nch, gw0 + wcap);
+                for (int b0 = gw0; b0 < gw1; b0 += 32) {
+                    const int g = b0 + lane;
+                    const bool in = g < gw1 && cm[g] >= zf;
                     const bool single = in && cu2[g] < zf && cln[g] >= 0;
                     const unsigned bs = __ballot_sync(0xFFFFFFFFu, single);
                     const unsigned bw = __ballot_sync(0xFFFFFFFFu, in && !single);
