@@ -668,6 +668,10 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
     return t;
 }
 
+// Histogram words of floor_hist (256 bins, padded); the caller zeroes them
+// before a barrier that precedes the call.
+constexpr int kFloorHistWords = 256 + 256 / 8;
+
 // Floor search, one pass: entries binned by (m - x) in steps of 1/8 over the
 // 32 logit units below the row max m (256 bins, 32-bit shared atomics), then
 // warp 0 finds the first bin at which the running weight reaches tgt.  The
@@ -678,11 +682,10 @@ template <class KW>
 __device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, FinishScratch& SS, float& zf) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kHB = 256;
+    static_assert(kHB + kHB / 8 == kFloorHistWords, "floor histogram size");
     constexpr float kStep = 8.0f;  // bins per logit unit
     // bin b at b + b / 8: warp 0 reads its lanes' 8-bin runs without bank conflicts
     auto at = [](int b) { return b + (b >> 3); };
-    for (int b = tid; b < kHB + kHB / 8; b += kThreads) hist[b] = 0u;
-    __syncthreads();
     for (int e = tid; e < n; e += kThreads) {
         float x;
         uint32_t w;
@@ -1044,6 +1047,9 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
             }
         }
     }
+    // the floor histogram starts at zero (filtered rows), cleared while the
+    // summaries load
+    for (int b = tid; b < kFloorHistWords; b += kThreads) reinterpret_cast<uint32_t*>(KS.fb.lhist)[b] = 0u;
     uint32_t rerr = param_errors(P);
     const RowMode md(P, a.V);
     const float T = P.temperature;
@@ -1454,11 +1460,25 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                     st.kap_k = fkey(K.zt);
                     st.iot_k = K.ge_form() ? a.V : K.iota;
                 }
-                // thread t holds sorted positions [4t, 4t + 4)
+                // thread t holds sorted positions [4t, 4t + 4), read once as 16-byte
+                // vectors (kCandCap = 4 kThreads: always inside the arrays)
                 const int p0 = 4 * tid;
+                uint32_t tk[4];
+                int ti[4];
+                uint64_t tm[4];
+                {
+                    const uint4 kv = reinterpret_cast<const uint4*>(sk)[tid];
+                    const int4 iv = reinterpret_cast<const int4*>(sid)[tid];
+                    const ulonglong2 m0 = reinterpret_cast<const ulonglong2*>(sm)[2 * tid];
+                    const ulonglong2 m1 = reinterpret_cast<const ulonglong2*>(sm)[2 * tid + 1];
+                    tk[0] = kv.x, tk[1] = kv.y, tk[2] = kv.z, tk[3] = kv.w;
+                    ti[0] = iv.x, ti[1] = iv.y, ti[2] = iv.z, ti[3] = iv.w;
+                    tm[0] = m0.x, tm[1] = m0.y, tm[2] = m1.x, tm[3] = m1.y;
+                }
+                static_assert(kCandCap == 4 * kThreads, "four sorted positions per thread");
                 uint64_t lk = 0;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) lk += (p0 + q < nk) ? sm[p0 + q] : 0u;
+                for (int q = 0; q < 4; ++q) lk += (p0 + q < nk) ? tm[q] : 0u;
                 uint64_t tot_k;
                 const uint64_t inc_k = block_scan_u64(lk, SS.redu, tot_k);
                 st.mass_k = md.topk_on ? tot_k : st.S_all;
@@ -1474,7 +1494,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                     if (run < tgt && inc_k >= tgt) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const uint64_t mq = (p0 + q < nk) ? sm[p0 + q] : 0u;
+                            const uint64_t mq = (p0 + q < nk) ? tm[q] : 0u;
                             if (mq != 0 && run < tgt && run + mq >= tgt) SS.bi[5] = p0 + q;
                             run += mq;
                         }
@@ -1495,7 +1515,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int pp = p0 + q;
-                    if (pp < nk && R.test(key_to_float(sk[pp]), sid[pp])) lr += sm[pp];
+                    if (pp < nk && R.test(key_to_float(tk[q]), ti[q])) lr += tm[q];
                 }
                 st.mass_r = block_sum_u64(lr, SS.redu);
                 st.target = scale_by_u(st.rbits, st.mass_r);
@@ -1506,7 +1526,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
 #pragma unroll
                     for (int q = 3; q >= 0; --q) {
                         const int pp = p0 + q;
-                        if (pp < nk && !R.test(key_to_float(sk[pp]), sid[pp])) first_out = pp;
+                        if (pp < nk && !R.test(key_to_float(tk[q]), ti[q])) first_out = pp;
                     }
                     nsv = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, static_cast<unsigned>(first_out)));
                     if (lane == 0) SS.fc[0][warp][3] = static_cast<uint32_t>(nsv);
