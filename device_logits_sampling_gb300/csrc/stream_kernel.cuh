@@ -1511,28 +1511,40 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                 st.kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
                 st.iot_r = R.ge_form() ? a.V : R.iota;
                 // survivors: a prefix [0, ns) of the sorted order
-                uint64_t lr = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int pp = p0 + q;
-                    if (pp < nk && R.test(key_to_float(tk[q]), ti[q])) lr += tm[q];
-                }
-                st.mass_r = block_sum_u64(lr, SS.redu);
-                st.target = scale_by_u(st.rbits, st.mass_r);
-                int nsv = 0;
-                {
-                    // ns: survivors are the first positions of the sorted order
+                int nsv = nk;
+                if (!(zx > K.zt)) {
+                    // R is K: its positions are [0, nk) and its mass the scan's total
+                    st.mass_r = tot_k;
+                } else {
+                    // the survivors' mass and their count, in one reduction
+                    uint64_t lr = 0;
                     int first_out = nk;
 #pragma unroll
                     for (int q = 3; q >= 0; --q) {
                         const int pp = p0 + q;
-                        if (pp < nk && !R.test(key_to_float(tk[q]), ti[q])) first_out = pp;
+                        if (pp < nk) {
+                            if (R.test(key_to_float(tk[q]), ti[q]))
+                                lr += tm[q];
+                            else
+                                first_out = pp;
+                        }
                     }
-                    nsv = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, static_cast<unsigned>(first_out)));
-                    if (lane == 0) SS.fc[0][warp][3] = static_cast<uint32_t>(nsv);
+                    lr = warp_sum_u64(lr);
+                    first_out = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, static_cast<unsigned>(first_out)));
+                    if (lane == 0) {
+                        SS.fc[1][warp][0] = static_cast<uint32_t>(lr);
+                        SS.fc[1][warp][1] = static_cast<uint32_t>(lr >> 32);
+                        SS.fc[1][warp][2] = static_cast<uint32_t>(first_out);
+                    }
                     __syncthreads();
-                    for (int v = 0; v < kWarps; ++v) nsv = min(nsv, static_cast<int>(SS.fc[0][v][3]));
+                    uint64_t mr = 0;
+                    for (int v = 0; v < kWarps; ++v) {
+                        mr += (static_cast<uint64_t>(SS.fc[1][v][1]) << 32) | SS.fc[1][v][0];
+                        nsv = min(nsv, static_cast<int>(SS.fc[1][v][2]));
+                    }
+                    st.mass_r = mr;
                 }
+                st.target = scale_by_u(st.rbits, st.mass_r);
                 // the draw in id order: each survivor sums the survivors with smaller ids
                 for (int pp = tid; pp < nsv; pp += kThreads) {
                     const int ip = sid[pp];
