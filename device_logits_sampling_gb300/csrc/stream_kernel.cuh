@@ -271,11 +271,12 @@ __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* red) {
 }
 
 // Block-wide inclusive scan of a u64 in thread order; returns the inclusive
-// value and sets total.  Uses red[kWarps].
-__device__ __forceinline__ uint64_t block_scan_u64(uint64_t v, uint64_t* red, uint64_t& total) {
+// value and sets total.  Uses red[kWarps]; `fresh`: every earlier reader of
+// red is already behind a barrier, so the leading one is skipped.
+__device__ __forceinline__ uint64_t block_scan_u64(uint64_t v, uint64_t* red, uint64_t& total, bool fresh = false) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t inc = warp_inclusive_u64(v);
-    __syncthreads();
+    if (!fresh) __syncthreads();
     if (lane == 31) red[warp] = inc;
     __syncthreads();
     uint64_t base = 0;
@@ -674,17 +675,17 @@ constexpr int kFloorHistWords = 256 + 256 / 8;
 
 // Floor search, one pass: entries binned by (m - x) in steps of 1/8 over the
 // 32 logit units below the row max m (256 bins, 32-bit shared atomics), then
-// warp 0 finds the first bin at which the running weight reaches tgt.  The
+// every warp finds the first bin at which the running weight reaches tgt.  The
 // floor lies below that bin: every entry counted is at or above it, so the
 // bound holds.  False when the window holds less than tgt (the exact
 // search below then decides).
 template <class KW>
-__device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, FinishScratch& SS, float& zf) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, float& zf) {
+    const int tid = threadIdx.x, lane = tid & 31;
     constexpr int kHB = 256;
     static_assert(kHB + kHB / 8 == kFloorHistWords, "floor histogram size");
     constexpr float kStep = 8.0f;  // bins per logit unit
-    // bin b at b + b / 8: warp 0 reads its lanes' 8-bin runs without bank conflicts
+    // bin b at b + b / 8: a warp reads its lanes' 8-bin runs without bank conflicts
     auto at = [](int b) { return b + (b >> 3); };
     for (int e = tid; e < n; e += kThreads) {
         float x;
@@ -694,7 +695,8 @@ __device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, 
         if (w != 0u && d < static_cast<float>(kHB)) atomicAdd(&hist[at(static_cast<int>(d))], w);
     }
     __syncthreads();
-    if (warp == 0) {
+    // every warp finds the same bin itself (no second barrier)
+    {
         uint32_t loc = 0;
 #pragma unroll
         for (int q = 0; q < kHB / 32; ++q) loc += hist[at(lane * (kHB / 32) + q)];
@@ -717,10 +719,8 @@ __device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, 
         bin = bal ? __shfl_sync(0xFFFFFFFFu, bin, __ffs(bal) - 1) : -1;
         // entries of bins 0..b satisfy m - x < (b + 1) / 8 up to the rounding of
         // m - x (far below a bin): one bin of margin, the edge rounded down
-        if (lane == 0) SS.bf[3] = (bin < 0) ? -INFINITY : __fsub_rd(m, static_cast<float>(bin + 2) / kStep);
+        zf = (bin < 0) ? -INFINITY : __fsub_rd(m, static_cast<float>(bin + 2) / kStep);
     }
-    __syncthreads();
-    zf = SS.bf[3];
     return zf > -INFINITY;
 }
 
@@ -1047,9 +1047,10 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
             }
         }
     }
-    // the floor histogram starts at zero (filtered rows), cleared while the
-    // summaries load
+    // the floor histogram and the candidate counter start at zero (filtered
+    // rows), cleared while the summaries load
     for (int b = tid; b < kFloorHistWords; b += kThreads) reinterpret_cast<uint32_t*>(KS.fb.lhist)[b] = 0u;
+    if (tid == 0) SS.ccount = 0;  // candidates gathered (filtered rows)
     uint32_t rerr = param_errors(P);
     const RowMode md(P, a.V);
     const float T = P.temperature;
@@ -1271,7 +1272,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                 };
                 fast = isfinite(m) &&
                        floor_hist(nch, [&](int e, float& x, uint32_t& w) { x = cm[e]; w = wt(x); }, m, tgt,
-                                  reinterpret_cast<uint32_t*>(KS.fb.lhist), SS, zf);
+                                  reinterpret_cast<uint32_t*>(KS.fb.lhist), zf);
                 if (!fast) {
                     auto kw = [&](int e, uint32_t& key, uint32_t& w) {
                         const float x = cm[e];
@@ -1285,9 +1286,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
             } else {
                 zf = zm;
             }
-            fast = fast && zf > -INFINITY;
-            if (tid == 0) SS.ccount = 0;
-            __syncthreads();
+            fast = fast && zf > -INFINITY;  // (the candidate counter was cleared with the summaries)
 
             // gather the ids >= zf as (key, id, mass): each warp takes the chunks
             // of its eighth whose max is >= zf, stages up to kCollectU of them at a
@@ -1480,7 +1479,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
 #pragma unroll
                 for (int q = 0; q < 4; ++q) lk += (p0 + q < nk) ? tm[q] : 0u;
                 uint64_t tot_k;
-                const uint64_t inc_k = block_scan_u64(lk, SS.redu, tot_k);
+                // (the barrier after the ranking follows every earlier use of SS.redu)
+                const uint64_t inc_k = block_scan_u64(lk, SS.redu, tot_k, /*fresh=*/true);
                 st.mass_k = md.topk_on ? tot_k : st.S_all;
                 bool found = false;
                 float zp = -INFINITY;
