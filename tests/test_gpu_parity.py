@@ -170,6 +170,44 @@ def test_top_k_ties_break_to_lowest_ids(cuda_lib):
     assert dbg["iota_k"][1] == 7 * 99 + 1
 
 
+@pytest.mark.parametrize("dtype", [wl.DTYPE_F32, wl.DTYPE_BF16])
+def test_top_k_cut_inside_small_tie_group(cuda_lib, dtype):
+    """The k-th logit falls in a run of 30 equal values above 20 distinct ones and
+    a N(0, 1) background: few candidates, so the direct selection ranks them.
+    Rows alternate pure top-k (the survivors are K), top-k with top-p (the cut
+    can land inside K) and top-k with min-p."""
+    B, V = 12, 40_000
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal((B, V)).astype(np.float32)
+    p = wl.make_params(B)
+    ks = [25, 20, 21, 50, 49, 3]
+    tied_ids = []
+    for r in range(B):
+        ids = rng.choice(V, size=50, replace=False)
+        z[r, ids[:20]] = 8.0 + 0.125 * np.arange(20, dtype=np.float32)  # exact in bf16 too
+        z[r, ids[20:]] = 6.0
+        tied_ids.append(np.sort(ids[20:]))
+        p[r]["top_k"] = ks[r % len(ks)]
+        p[r]["temperature"] = 1.0 if r % 2 == 0 else 0.7
+        if r % 3 == 1:
+            p[r]["top_p"] = 0.6
+        elif r % 3 == 2:
+            p[r]["min_p"] = 0.02
+        p[r]["seed"] = 100 + r
+    logits = wl.f32_to_bf16_bits(z) if dtype == wl.DTYPE_BF16 else z
+    w = wl.Workload("tie_group", dtype, logits, p)
+    tokens, dbg, err = run(cuda_lib, w)
+    rep = parity.check_batch(w, tokens, dbg)
+    assert rep.rows == B
+    assert err == 0, hex(err)
+    for r in range(B):
+        k = int(p[r]["top_k"])
+        if 20 < k < 50:  # the cut inside the run: the first k - 20 tied ids survive
+            assert dbg["iota_k"][r] == tied_ids[r][k - 21] + 1, r
+        else:  # the cut between distinct values, or after the run: every id of the key survives
+            assert dbg["iota_k"][r] == V, r
+
+
 def test_row_errors_and_degenerate_rows(cuda_lib):
     V = 3000
     rng = np.random.default_rng(0)
