@@ -475,34 +475,42 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         return ((pbm[l0 >> 5] >> (l0 & 31)) & ((1u << VEC) - 1u)) != 0;
     };
 
-    // vector maxima with NaN ignored (-inf for vectors past the slice)
+    // vector maxima with NaN ignored (-inf for vectors past the slice, which
+    // were loaded as -inf); NaN is rare: one test for the thread's vectors
     float xs[kVpt];
-    uint32_t vn = 0;  // vectors holding a NaN
 #pragma unroll
     for (int j = 0; j < kVpt; ++j) {
-        float x = -INFINITY;
-        if (j * kThreads + tid < nv) {
-            if (patched(j)) {
-                float z[VEC];
-                vals(j, z);
-                x = z[0];
+        if (j * kThreads + tid < nv && patched(j)) {
+            float z[VEC];
+            vals(j, z);
+            float x = z[0];
 #pragma unroll
-                for (int e = 1; e < VEC; ++e) x = fmax_nan(x, z[e]);
-            } else {
-                x = E::vmax_nan(d[j]);
-            }
-            if (x != x) {
+            for (int e = 1; e < VEC; ++e) x = fmax_nan(x, z[e]);
+            xs[j] = x;
+        } else {
+            xs[j] = E::vmax_nan(d[j]);
+        }
+    }
+    uint32_t vn = 0;  // vectors holding a NaN
+    bool anynan = false;
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) anynan |= (xs[j] != xs[j]);
+    if (anynan) {
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            if (xs[j] != xs[j]) {
                 vn |= 1u << j;
                 float z[VEC];
                 vals(j, z);
-                x = -INFINITY;
+                float x = -INFINITY;
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
                     if (z[e] > x) x = z[e];
+                xs[j] = x;
             }
         }
-        xs[j] = x;
     }
+    const bool wnan = __any_sync(0xFFFFFFFFu, vn != 0);
 
     unsigned char* mysum = const_cast<unsigned char*>(summary_at(a.summaries, a.s, row, cidx));
     float wm = -INFINITY;
@@ -525,15 +533,15 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
 #pragma unroll
             for (int j = 0; j < kVpt; ++j) {
                 float l = 0.0f;
-                if (xs[j] != -INFINITY) {  // then mj[j] >= xs[j] > -inf
-                    if (DT == ARC_BF16 && !patched(j) && !((vn >> j) & 1u) && mj[j] != INFINITY) {
-                        l = lane_mass_bf16(d[j], mj[j], cT);
-                    } else {
-                        float z[VEC];
-                        vals(j, z);
-                        l = (((vn >> j) & 1u) || mj[j] == INFINITY) ? lane_mass_safe<VEC>(z, mj[j], cT)
-                                                                    : lane_mass_packed<VEC>(z, mj[j], cT);
-                    }
+                if (DT == ARC_BF16 && !(HIST && has_patch) && !wnan && mj[j] > -INFINITY && mj[j] < INFINITY) {
+                    // the common case, decided for the whole warp: every lane by the
+                    // raw-vector formula (its -inf logits, padding included, weigh 0)
+                    l = lane_mass_bf16(d[j], mj[j], cT);
+                } else if (xs[j] != -INFINITY) {  // then mj[j] >= xs[j] > -inf
+                    float z[VEC];
+                    vals(j, z);
+                    l = (((vn >> j) & 1u) || mj[j] == INFINITY) ? lane_mass_safe<VEC>(z, mj[j], cT)
+                                                                : lane_mass_packed<VEC>(z, mj[j], cT);
                 }
                 sl[j] = l;
             }
@@ -601,7 +609,6 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         wm = (wid < 0) ? -INFINITY : wv;
         wam = wid;
     }
-    const bool wnan = __any_sync(0xFFFFFFFFu, vn != 0);
     if (lane == 0) {
         WarpRecord r;
         r.m = wm;
@@ -644,7 +651,10 @@ __global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const Scan
 #pragma unroll
     for (int j = 0; j < kVpt; ++j) {
         const int v = j * kThreads + tid;
-        d[j] = (v < nv) ? E::global_vec(sp, v, n, a.aligned) : ninf;
+        if (a.aligned && (j + 1) * kThreads * VEC <= n)  // the whole round inside the slice
+            d[j] = ld_nc_v4(sp + static_cast<size_t>(v) * 16);
+        else
+            d[j] = (v < nv) ? E::global_vec(sp, v, n, a.aligned) : ninf;
     }
     const ScanRowInfo R = scan_row_info<HIST>(a, row, pw);
     scan_slice<DT, HIST>(a, d, row, cidx, R, sh, dyn);
