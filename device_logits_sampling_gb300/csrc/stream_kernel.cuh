@@ -547,29 +547,27 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
             }
             S = warp_sum4(sl, lane);
         }
-        int fl[kVpt];
-        float u2[kVpt];
+        // entry j as soon as its fields are known, by lane 8j (which holds the
+        // chunk's mass): nothing per chunk stays live across the loop
+        ChunkEntry* ch = reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes);
+        const bool filtered = (bits & kRowFiltered) != 0;
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) {
-            fl[j] = -1;
-            u2[j] = INFINITY;
-        }
-        if (bits & kRowFiltered) {
-#pragma unroll
-            for (int j = 0; j < kVpt; ++j) {
+            int fl = -1;
+            float u2 = INFINITY;
+            if (filtered) {
                 const unsigned holders = __ballot_sync(0xFFFFFFFFu, xs[j] == mj[j] && xs[j] > -INFINITY);
-                fl[j] = holders ? __ffs(holders) - 1 : -1;
-                u2[j] = warp_max_nonan(lane == fl[j] ? -INFINITY : xs[j]);
+                fl = holders ? __ffs(holders) - 1 : -1;
+                u2 = warp_max_nonan(lane == fl ? -INFINITY : xs[j]);
             }
-        }
-        if ((lane & 7) == 0) {
-            const int j = lane >> 3;
-            ChunkEntry ce;
-            ce.m = j == 0 ? mj[0] : (j == 1 ? mj[1] : (j == 2 ? mj[2] : mj[3]));
-            ce.S = S;
-            ce.lane = j == 0 ? fl[0] : (j == 1 ? fl[1] : (j == 2 ? fl[2] : fl[3]));
-            ce.u2 = j == 0 ? u2[0] : (j == 1 ? u2[1] : (j == 2 ? u2[2] : u2[3]));
-            reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes)[j * kWarps + warp] = ce;
+            if (lane == 8 * j) {
+                ChunkEntry ce;
+                ce.m = mj[j];
+                ce.S = S;
+                ce.lane = fl;
+                ce.u2 = u2;
+                ch[j * kWarps + warp] = ce;
+            }
         }
         wm = fmaxf(fmaxf(mj[0], mj[1]), fmaxf(mj[2], mj[3]));
         wam = wm > -INFINITY ? kAmUnknown : -1;
@@ -625,7 +623,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
 // barrier (rows with history excepted), and registers stay few so that many
 // CTAs per SM keep enough bytes in flight.
 template <int DT, bool HIST>
-__global__ void __launch_bounds__(kThreads, HIST ? 4 : 6) scan_kernel(const ScanArgs a) {
+__global__ void __launch_bounds__(kThreads, HIST ? 4 : 8) scan_kernel(const ScanArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     extern __shared__ __align__(128) unsigned char dyn[];
