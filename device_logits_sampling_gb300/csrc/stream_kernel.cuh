@@ -530,20 +530,27 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         if (bits & kRowMass) {
             const float cT = R.cT;
             float sl[kVpt];
+            bool plain = DT == ARC_BF16 && !(HIST && has_patch) && !wnan;
 #pragma unroll
-            for (int j = 0; j < kVpt; ++j) {
-                float l = 0.0f;
-                if (DT == ARC_BF16 && !(HIST && has_patch) && !wnan && mj[j] > -INFINITY && mj[j] < INFINITY) {
-                    // the common case, decided for the whole warp: every lane by the
-                    // raw-vector formula (its -inf logits, padding included, weigh 0)
-                    l = lane_mass_bf16(d[j], mj[j], cT);
-                } else if (xs[j] != -INFINITY) {  // then mj[j] >= xs[j] > -inf
-                    float z[VEC];
-                    vals(j, z);
-                    l = (((vn >> j) & 1u) || mj[j] == INFINITY) ? lane_mass_safe<VEC>(z, mj[j], cT)
-                                                                : lane_mass_packed<VEC>(z, mj[j], cT);
+            for (int j = 0; j < kVpt; ++j) plain &= mj[j] < INFINITY;
+            if (plain) {
+                // the common case, decided once for the warp: every lane by the
+                // raw-vector formula; -inf logits (padding included) weigh 0, and a
+                // chunk with no number takes any finite reference
+#pragma unroll
+                for (int j = 0; j < kVpt; ++j) sl[j] = lane_mass_bf16(d[j], fmaxf(mj[j], -3.0e38f), cT);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVpt; ++j) {
+                    float l = 0.0f;
+                    if (xs[j] != -INFINITY) {  // then mj[j] >= xs[j] > -inf
+                        float z[VEC];
+                        vals(j, z);
+                        l = (((vn >> j) & 1u) || mj[j] == INFINITY) ? lane_mass_safe<VEC>(z, mj[j], cT)
+                                                                    : lane_mass_packed<VEC>(z, mj[j], cT);
+                    }
+                    sl[j] = l;
                 }
-                sl[j] = l;
             }
             S = warp_sum4(sl, lane);
         }
