@@ -376,16 +376,6 @@ __device__ __forceinline__ arc_row_params params_from_words(const uint64_t (&w)[
     r.step = w[5];
     return r;
 }
-// Row parameters, read once with volatile loads so that no field is fetched
-// after the first cluster barrier (rank 0 may rewrite `step` after it).
-__device__ __forceinline__ arc_row_params load_params(const arc_row_params* p) {
-    const volatile uint64_t* q = reinterpret_cast<const volatile uint64_t*>(p);
-    uint64_t w[6];
-#pragma unroll
-    for (int i = 0; i < 6; ++i) w[i] = q[i];
-    return params_from_words(w);
-}
-
 // Key range [lo, hi] of histogram bin `b` of window W.
 __device__ __forceinline__ void bin_range(const Window& W, int b, uint32_t& lo, uint32_t& hi) {
     hi = W.khi - (static_cast<uint32_t>(b) << W.sh);

@@ -988,7 +988,12 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
     float* cs = reinterpret_cast<float*>(dyn + a.cs_off);
     int* cln = reinterpret_cast<int*>(dyn + a.cid_off);
     float* cu2 = reinterpret_cast<float*>(dyn + a.cv2_off);
-    const arc_row_params P = load_params(a.params + row);
+    // plain loads, issued before the wait below: only this CTA writes its
+    // row's record (`step`, at the very end)
+    uint64_t pw[6];
+#pragma unroll
+    for (int i = 0; i < 6; ++i) pw[i] = reinterpret_cast<const uint64_t*>(a.params + row)[i];
+    const arc_row_params P = params_from_words(pw);
     int hn = 0, hbeg = 0;
     if (HIST && a.hist_off != nullptr) {
         hbeg = a.hist_off[row];
