@@ -1366,25 +1366,16 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                     }
                 };
                 stage_round(0);
-                // ids found go to slots from one shared counter (one atomic per warp and batch)
+                // ids found take slots from one shared counter: one atomic per lane
+                // that found any (few lanes of a chunk do)
                 auto emit = [&](bool valid, const float (&z)[VEC], int vrow) {
                     int cnt = 0;
                     if (valid) {
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
                     }
-                    if (__ballot_sync(0xFFFFFFFFu, cnt > 0) == 0u) return;  // uniform
-                    int inc = cnt;
-#pragma unroll
-                    for (int dd = 1; dd < 32; dd <<= 1) {
-                        const int o = __shfl_up_sync(0xFFFFFFFFu, inc, dd);
-                        if (lane >= dd) inc += o;
-                    }
-                    uint32_t base = 0;
-                    if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(inc));
-                    base = __shfl_sync(0xFFFFFFFFu, base, 31);
                     if (cnt > 0) {
-                        uint32_t pos = base + static_cast<uint32_t>(inc - cnt);
+                        uint32_t pos = atomicAdd(&SS.ccount, static_cast<uint32_t>(cnt));
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) {
                             if (z[e] >= zf) {
