@@ -37,10 +37,15 @@ KERNEL_SOURCES = ["arc_sample.cu", "stream_kernel.cuh", "row_select.cuh", "arc_d
 
 
 def kernel_hash() -> str:
+    """Hash of the kernel sources' code: comments and layout do not count, so a
+    profile stays matched to the build it measured until the code changes."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "device_logits_sampling_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "device_logits_sampling_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -3,10 +3,13 @@
 // scan_kernel: a row is split into s slices of at most kVpt * kThreads
 // 16-byte vectors; one CTA per slice issues all its 16-byte loads first (they
 // depend on nothing), applies the history penalties in registers, and writes
-// a small summary to the workspace: the slice max and its first id, and per
-// 32-vector chunk (256 bf16 / 128 fp32 logits) the chunk max and, for rows
-// that need masses, the fp32 sum of 2^((z - chunk max) log2(e) / T).  No CTA
-// waits for another and registers stay few, so many CTAs per SM keep HBM busy.
+// a small summary to the workspace: per warp the max of its vectors (with its
+// first id for greedy rows and rows with a history), and per 32-vector chunk
+// (256 bf16 / 128 fp32 logits) the chunk max, for rows that need masses the
+// fp32 sum of 2^((z - chunk max) log2(e) / T), and for filtered rows where
+// the max lies and the largest max of the chunk's other vectors.  No CTA
+// waits for another, no warp for another (rows with history excepted), and
+// registers stay at 32, so 8 CTAs per SM keep HBM busy.
 //
 // finish_kernel: one CTA per row combines the slice summaries.
 //  - greedy rows take the row max;
@@ -16,9 +19,9 @@
 //  - filtered rows first bound the cutoff from below with the chunk maxima
 //    (the k-th largest chunk max for top-k, the min-p threshold, or a mass
 //    bound for top-p), gather the few ids at or above that floor from the
-//    chunks that can hold them, in id order, into shared memory, and select
-//    exactly there by ranking.  When the floor admits too many ids, the
-//    general threshold bisection of row_select.cuh runs over the row instead.
+//    chunks that can hold them into shared memory, and select exactly there
+//    by ranking.  When the floor admits too many ids, the general threshold
+//    bisection of row_select.cuh runs over the row instead.
 #pragma once
 
 #include <climits>
@@ -86,7 +89,7 @@ struct FinishArgs {
 // writes its own record, so the scan needs no barrier between its warps.
 struct __align__(16) WarpRecord {
     float m;         // max of the warp's vectors (NaN-free), -inf when none
-    int am;          // its first id, -1 when none
+    int am;          // its first id, -1 when none, kAmUnknown when left open
     uint32_t flags;  // ARC_ERR_NAN | ARC_ERR_HIST_ID | ARC_ERR_HIST_CAP
     int pad;
 };
