@@ -1473,100 +1473,123 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                     st.kap_k = fkey(K.zt);
                     st.iot_k = K.ge_form() ? a.V : K.iota;
                 }
-                // thread t holds sorted positions [4t, 4t + 4), read once as 16-byte
-                // vectors (kCandCap = 4 kThreads: always inside the arrays)
-                const int p0 = 4 * tid;
-                uint32_t tk[4];
-                int ti[4];
-                uint64_t tm[4];
-                {
-                    const uint4 kv = reinterpret_cast<const uint4*>(sk)[tid];
-                    const int4 iv = reinterpret_cast<const int4*>(sid)[tid];
-                    const ulonglong2 m0 = reinterpret_cast<const ulonglong2*>(sm)[2 * tid];
-                    const ulonglong2 m1 = reinterpret_cast<const ulonglong2*>(sm)[2 * tid + 1];
-                    tk[0] = kv.x, tk[1] = kv.y, tk[2] = kv.z, tk[3] = kv.w;
-                    ti[0] = iv.x, ti[1] = iv.y, ti[2] = iv.z, ti[3] = iv.w;
-                    tm[0] = m0.x, tm[1] = m0.y, tm[2] = m1.x, tm[3] = m1.y;
-                }
-                static_assert(kCandCap == 4 * kThreads, "four sorted positions per thread");
-                uint64_t lk = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) lk += (p0 + q < nk) ? tm[q] : 0u;
-                uint64_t tot_k;
-                // (the barrier after the ranking follows every earlier use of SS.redu)
-                const uint64_t inc_k = block_scan_u64(lk, SS.redu, tot_k, /*fresh=*/true);
-                st.mass_k = md.topk_on ? tot_k : st.S_all;
-                bool found = false;
-                float zp = -INFINITY;
-                if (md.topp_on) {
-                    // first sorted position whose running mass reaches ceil(p * mass_k)
-                    if (tid == 0)
-                        SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(st.mass_k)));
-                    __syncthreads();
-                    const uint64_t tgt = max(SS.bu[5], uint64_t{1});
-                    uint64_t run = inc_k - lk;
-                    if (run < tgt && inc_k >= tgt) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint64_t mq = (p0 + q < nk) ? tm[q] : 0u;
-                            if (mq != 0 && run < tgt && run + mq >= tgt) SS.bi[5] = p0 + q;
-                            run += mq;
-                        }
-                    }
-                    __syncthreads();
-                    if (SS.bi[5] >= 0) {
-                        found = true;
-                        zp = key_to_float(sk[SS.bi[5]]);
-                    }
-                    if (!found && !md.minp_on && !md.topk_on) st.err |= kErrInternal;  // the floor guarantees it
-                }
-                const float zx = found ? fmaxf(zp, zm) : zm;
-                const Surv R = (zx > K.zt) ? Surv{zx, INT_MAX} : K;
-                st.kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
-                st.iot_r = R.ge_form() ? a.V : R.iota;
-                // survivors: a prefix [0, ns) of the sorted order
-                int nsv = nk;
-                if (!(zx > K.zt)) {
-                    // R is K: its positions are [0, nk) and its mass the scan's total
-                    st.mass_r = tot_k;
-                } else {
-                    // the survivors' mass and their count, in one reduction
-                    uint64_t lr = 0;
-                    int first_out = nk;
-#pragma unroll
-                    for (int q = 3; q >= 0; --q) {
-                        const int pp = p0 + q;
-                        if (pp < nk) {
-                            if (R.test(key_to_float(tk[q]), ti[q]))
-                                lr += tm[q];
-                            else
-                                first_out = pp;
-                        }
-                    }
-                    lr = warp_sum_u64(lr);
-                    first_out = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, static_cast<unsigned>(first_out)));
-                    if (lane == 0) {
-                        SS.fc[1][warp][0] = static_cast<uint32_t>(lr);
-                        SS.fc[1][warp][1] = static_cast<uint32_t>(lr >> 32);
-                        SS.fc[1][warp][2] = static_cast<uint32_t>(first_out);
-                    }
-                    __syncthreads();
-                    uint64_t mr = 0;
-                    for (int v = 0; v < kWarps; ++v) {
-                        mr += (static_cast<uint64_t>(SS.fc[1][v][1]) << 32) | SS.fc[1][v][0];
-                        nsv = min(nsv, static_cast<int>(SS.fc[1][v][2]));
-                    }
-                    st.mass_r = mr;
-                }
-                st.target = scale_by_u(st.rbits, st.mass_r);
-                // the draw in id order: each survivor sums the survivors with smaller ids
-                for (int pp = tid; pp < nsv; pp += kThreads) {
-                    const int ip = sid[pp];
-                    const uint64_t mp = sm[pp];
-                    uint64_t before = 0;
+                if (md.topk_on && !md.topp_on && !md.minp_on) {
+                    // top-k alone: the survivors are K = positions [0, nk); each
+                    // survivor's thread sums the K masses with smaller ids and all of
+                    // them (the total, hence the target), so no scan runs
+                    st.kap_r = st.kap_k;
+                    st.iot_r = st.iot_k;
+                    for (int pp = tid; pp < nk; pp += kThreads) {
+                        const int ip = sid[pp];
+                        uint64_t before = 0, tot = 0;
 #pragma unroll 8
-                    for (int qq = 0; qq < nsv; ++qq) before += (sid[qq] < ip) ? sm[qq] : 0u;
-                    if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
+                        for (int qq = 0; qq < nk; ++qq) {
+                            const uint64_t mq = sm[qq];
+                            tot += mq;
+                            before += (sid[qq] < ip) ? mq : 0u;
+                        }
+                        const uint64_t target = scale_by_u(st.rbits, tot);
+                        const uint64_t mp = sm[pp];
+                        if (mp != 0 && before <= target && target < before + mp) SS.bi[6] = ip;
+                        st.mass_k = st.mass_r = tot;  // thread 0 (position 0) reports them
+                        st.target = target;
+                    }
+                } else {
+                    // thread t holds sorted positions [4t, 4t + 4), read once as 16-byte
+                    // vectors (kCandCap = 4 kThreads: always inside the arrays)
+                    const int p0 = 4 * tid;
+                    uint32_t tk[4];
+                    int ti[4];
+                    uint64_t tm[4];
+                    {
+                        const uint4 kv = reinterpret_cast<const uint4*>(sk)[tid];
+                        const int4 iv = reinterpret_cast<const int4*>(sid)[tid];
+                        const ulonglong2 m0 = reinterpret_cast<const ulonglong2*>(sm)[2 * tid];
+                        const ulonglong2 m1 = reinterpret_cast<const ulonglong2*>(sm)[2 * tid + 1];
+                        tk[0] = kv.x, tk[1] = kv.y, tk[2] = kv.z, tk[3] = kv.w;
+                        ti[0] = iv.x, ti[1] = iv.y, ti[2] = iv.z, ti[3] = iv.w;
+                        tm[0] = m0.x, tm[1] = m0.y, tm[2] = m1.x, tm[3] = m1.y;
+                    }
+                    static_assert(kCandCap == 4 * kThreads, "four sorted positions per thread");
+                    uint64_t lk = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) lk += (p0 + q < nk) ? tm[q] : 0u;
+                    uint64_t tot_k;
+                    // (the barrier after the ranking follows every earlier use of SS.redu)
+                    const uint64_t inc_k = block_scan_u64(lk, SS.redu, tot_k, /*fresh=*/true);
+                    st.mass_k = md.topk_on ? tot_k : st.S_all;
+                    bool found = false;
+                    float zp = -INFINITY;
+                    if (md.topp_on) {
+                        // first sorted position whose running mass reaches ceil(p * mass_k)
+                        if (tid == 0)
+                            SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(st.mass_k)));
+                        __syncthreads();
+                        const uint64_t tgt = max(SS.bu[5], uint64_t{1});
+                        uint64_t run = inc_k - lk;
+                        if (run < tgt && inc_k >= tgt) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint64_t mq = (p0 + q < nk) ? tm[q] : 0u;
+                                if (mq != 0 && run < tgt && run + mq >= tgt) SS.bi[5] = p0 + q;
+                                run += mq;
+                            }
+                        }
+                        __syncthreads();
+                        if (SS.bi[5] >= 0) {
+                            found = true;
+                            zp = key_to_float(sk[SS.bi[5]]);
+                        }
+                        if (!found && !md.minp_on && !md.topk_on) st.err |= kErrInternal;  // the floor guarantees it
+                    }
+                    const float zx = found ? fmaxf(zp, zm) : zm;
+                    const Surv R = (zx > K.zt) ? Surv{zx, INT_MAX} : K;
+                    st.kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
+                    st.iot_r = R.ge_form() ? a.V : R.iota;
+                    // survivors: a prefix [0, ns) of the sorted order
+                    int nsv = nk;
+                    if (!(zx > K.zt)) {
+                        // R is K: its positions are [0, nk) and its mass the scan's total
+                        st.mass_r = tot_k;
+                    } else {
+                        // the survivors' mass and their count, in one reduction
+                        uint64_t lr = 0;
+                        int first_out = nk;
+#pragma unroll
+                        for (int q = 3; q >= 0; --q) {
+                            const int pp = p0 + q;
+                            if (pp < nk) {
+                                if (R.test(key_to_float(tk[q]), ti[q]))
+                                    lr += tm[q];
+                                else
+                                    first_out = pp;
+                            }
+                        }
+                        lr = warp_sum_u64(lr);
+                        first_out = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, static_cast<unsigned>(first_out)));
+                        if (lane == 0) {
+                            SS.fc[1][warp][0] = static_cast<uint32_t>(lr);
+                            SS.fc[1][warp][1] = static_cast<uint32_t>(lr >> 32);
+                            SS.fc[1][warp][2] = static_cast<uint32_t>(first_out);
+                        }
+                        __syncthreads();
+                        uint64_t mr = 0;
+                        for (int v = 0; v < kWarps; ++v) {
+                            mr += (static_cast<uint64_t>(SS.fc[1][v][1]) << 32) | SS.fc[1][v][0];
+                            nsv = min(nsv, static_cast<int>(SS.fc[1][v][2]));
+                        }
+                        st.mass_r = mr;
+                    }
+                    st.target = scale_by_u(st.rbits, st.mass_r);
+                    // the draw in id order: each survivor sums the survivors with smaller ids
+                    for (int pp = tid; pp < nsv; pp += kThreads) {
+                        const int ip = sid[pp];
+                        const uint64_t mp = sm[pp];
+                        uint64_t before = 0;
+#pragma unroll 8
+                        for (int qq = 0; qq < nsv; ++qq) before += (sid[qq] < ip) ? sm[qq] : 0u;
+                        if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
+                    }
                 }
                 __syncthreads();
                 st.token = SS.bi[6];
