@@ -736,8 +736,9 @@ __device__ bool floor_hist(int n, KW kw, float m, uint32_t tgt, uint32_t* hist, 
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, bin >= 0);
         bin = bal ? __shfl_sync(0xFFFFFFFFu, bin, __ffs(bal) - 1) : -1;
         // entries of bins 0..b satisfy m - x < (b + 1) / 8 up to the rounding of
-        // m - x (far below a bin): one bin of margin, the edge rounded down
-        zf = (bin < 0) ? -INFINITY : __fsub_rd(m, static_cast<float>(bin + 2) / kStep);
+        // m - x, below 3e-5 of a bin for the 256 bins: a thousandth of a bin
+        // of margin, the edge rounded down
+        zf = (bin < 0) ? -INFINITY : __fsub_rd(m, (static_cast<float>(bin) + 1.001f) / kStep);
     }
     return zf > -INFINITY;
 }
