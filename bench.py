@@ -345,6 +345,76 @@ def bench_gpu(args) -> None:
         torch.distributed.destroy_process_group()
 
 
+def bench_decode_loop(args) -> None:
+    """--decode-loop: the decode step after sampling (arc_decode_commit into a
+    pinned host ring).  Times, with CUDA events over graph replays on the
+    mixed B=256 batch, one step of sampling alone, one step of sampling
+    followed by the commit, and the commit alone; the host drains every
+    record of the timed replays afterwards and checks their count and owners."""
+    import numpy as np
+    import torch
+
+    from device_logits_sampling_gb300 import decode, sampler, workloads
+
+    w = workloads.mixed_batch()
+    B, V = w.B, w.V
+    bufs = [sampler.logits_tensor(w) for _ in range(NBUF)]
+    prm = sampler.params_tensor(w.params)
+    out = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ws = sampler.workspace_tensor(B, V, w.dtype)
+    ids = torch.zeros(B, dtype=torch.int32, device="cuda")
+    pos = torch.zeros(B, dtype=torch.int32, device="cuda")
+    owners = torch.arange(B, dtype=torch.int32, device="cuda")
+    head = torch.zeros(1, dtype=torch.int64, device="cuda")
+    fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n = max(1, args.steps)
+    ring = decode.Ring(B * (n * 3 + args.warmup * 3 + 8))
+    s = torch.cuda.Stream()
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            sampler.sample_batch(bufs[0], prm, out, workspace=ws, stream=s)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(NBUF):
+                    fn(i)
+            for _ in range(max(1, args.warmup // NBUF)):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(1, n // NBUF)
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+            s.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (reps * NBUF)
+
+    def sample(i):
+        sampler.sample_batch(bufs[i], prm, out, workspace=ws, autoinc=True, stream=s)
+
+    def commit():
+        decode.decode_commit(out, ids, pos, 1 << 30, V, ring, head, owners=owners, fault_word=fault, stream=s)
+
+    def both(i):
+        sample(i)
+        commit()
+
+    t_sample = timed(sample)
+    t_both = timed(both)
+    t_commit = timed(lambda i: commit())
+    published = int(head.item())
+    recs = ring.drain(published, max_spins=1 << 20)
+    assert len(recs) == published and int(fault.item()) == 0
+    assert np.array_equal(recs["owner"], np.tile(np.arange(B), published // B))
+    print(json.dumps({
+        "metric": "decode step after sampling: sample + commit into a pinned host ring", "unit": "us",
+        "B": B, "V": V, "sample_us": t_sample, "sample_and_commit_us": t_both, "commit_alone_us": t_commit,
+        "commit_added_us": t_both - t_sample, "records_drained": published, "higher_is_better": False,
+    }))
+    ring.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -352,10 +422,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-loop", action="store_true", help="time the decode-loop commit (separate JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.decode_loop:
+        bench_decode_loop(args)
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_gpu(args)

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libarcsample.so")
-SOURCES = [os.path.join(CSRC, "arc_sample.cu")]
+SOURCES = [os.path.join(CSRC, "arc_sample.cu"), os.path.join(CSRC, "arc_decode.cu")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <type_traits>
 
+#include "arc_decode.h"
 #include "arc_sample.h"
 #include "argmax_kernel.cuh"
 #include "stream_kernel.cuh"
@@ -224,6 +225,7 @@ const char* arc_sample_strerror(int code) {
         case ARC_E_OPTION: return "bad field in arc_sample_options";
         case ARC_E_CUDA: return "CUDA error while configuring or launching the kernel";
         case ARC_E_WORKSPACE: return "workspace is NULL or smaller than arc_sample_workspace_bytes()";
+        case ARC_E_RING_OVERRUN: return "a commit ring slot was overwritten before it was drained";
         default: return "unknown error code";
     }
 }

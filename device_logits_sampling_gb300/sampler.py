@@ -96,6 +96,16 @@ SIGNATURES = {
         ctypes.POINTER(Options), ctypes.POINTER(Geometry)]),
     "arc_sample_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "arc_sample_abi_version": (ctypes.c_int, []),
+    # arc_decode.h
+    "arc_decode_commit": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "arc_ring_drain": (ctypes.c_int64, [
+        ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint64]),
+    "arc_stream_idle": (ctypes.c_int, [ctypes.c_void_p]),
+    "arc_ring_alloc": (ctypes.c_int, [ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p),
+                                      ctypes.POINTER(ctypes.c_void_p)]),
+    "arc_ring_free": (ctypes.c_int, [ctypes.c_void_p]),
 }
 
 

@@ -10,3 +10,4 @@ from .sampler import (  # noqa: F401
     row_mode, sample_batch, sample_row, sample_row_u, splitmix64, top_k_mask,
     top_p_cutoff, uniform,
 )
+from . import decode_commit  # noqa: F401,E402

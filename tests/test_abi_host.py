@@ -11,7 +11,8 @@ import pytest
 from conftest import ROOT
 from device_logits_sampling_gb300 import sampler, workloads
 
-HEADER = os.path.join(ROOT, "include", "arc_sample.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -24,15 +25,17 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s*(arc_\w+)\s*\(", text, re.M)))
+    text = "\n".join(open(h).read() for h in HEADERS)
+    return sorted(set(re.findall(r"^\s*(?:int|int64_t|size_t|const char\s*\*)\s*(arc_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["arc_sample_batch", "arc_sample_batch_static", "arc_sample_greedy",
                             "arc_sample_plan", "arc_sample_workspace_bytes", "arc_sample_strerror",
-                            "arc_sample_abi_version"]), names
+                            "arc_sample_abi_version",
+                            "arc_decode_commit", "arc_ring_drain", "arc_stream_idle", "arc_ring_alloc",
+                            "arc_ring_free"]), names
 
 
 def test_library_exports_every_declared_symbol(lib):
