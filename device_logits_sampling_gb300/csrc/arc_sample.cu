@@ -68,7 +68,7 @@ int check_common(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t d
 
 int check_options(const arc_sample_options* o) {
     if (o == nullptr) return ARC_OK;
-    if (o->flags & ~ARC_OPT_STEP_AUTOINC) return ARC_E_OPTION;
+    if (o->flags & ~(ARC_OPT_STEP_AUTOINC | ARC_OPT_FORCE_BISECTION)) return ARC_E_OPTION;
     if (o->ctas_per_row < 0 || o->ctas_per_row > kMaxRowCtas) return ARC_E_OPTION;
     if (o->max_hist_len < 0 || o->max_hist_len > (1 << 20)) return ARC_E_OPTION;
     if (o->reserved != 0) return ARC_E_OPTION;

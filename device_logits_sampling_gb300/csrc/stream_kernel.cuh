@@ -1310,7 +1310,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
             } else {
                 zf = zm;
             }
-            fast = fast && zf > -INFINITY;  // (the candidate counter was cleared with the summaries)
+            // (the candidate counter was cleared with the summaries)
+            fast = fast && zf > -INFINITY && !(a.flags & ARC_OPT_FORCE_BISECTION);
 
             // gather the ids >= zf as (key, id, mass): each warp takes the chunks
             // of its eighth whose max is >= zf, stages up to kCollectU of them at a

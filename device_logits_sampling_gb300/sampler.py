@@ -36,6 +36,7 @@ ARC_ERR_TIMEOUT = 0x20
 ARC_ERR_INTERNAL = 0x40
 
 ARC_OPT_STEP_AUTOINC = 0x1
+ARC_OPT_FORCE_BISECTION = 0x2
 ARC_STATIC_WORKSPACE_BYTES = 8 << 20  # scratch compiled into the library (arc_sample_batch_static)
 
 # arc_row_debug, 72 bytes
@@ -179,9 +180,9 @@ def debug_records(t) -> np.ndarray:
     return t.cpu().numpy().view(ROW_DEBUG_DTYPE)
 
 
-def make_options(ctas_per_row=0, max_hist_len=0, autoinc=False, debug=None) -> Options:
-    return Options(ARC_OPT_STEP_AUTOINC if autoinc else 0, int(ctas_per_row), int(max_hist_len), 0,
-                   _ptr(debug))
+def make_options(ctas_per_row=0, max_hist_len=0, autoinc=False, debug=None, force_bisection=False) -> Options:
+    flags = (ARC_OPT_STEP_AUTOINC if autoinc else 0) | (ARC_OPT_FORCE_BISECTION if force_bisection else 0)
+    return Options(flags, int(ctas_per_row), int(max_hist_len), 0, _ptr(debug))
 
 
 def workspace_bytes(B: int, V: int, dtype: int, has_history=False, ctas_per_row=0, max_hist_len=0) -> int:
@@ -203,7 +204,7 @@ def workspace_tensor(B: int, V: int, dtype: int, has_history=False, ctas_per_row
 
 def sample_batch(logits, params, out, hist_offsets=None, hist_ids=None, err_word=None, debug=None,
                  workspace=None, ctas_per_row=0, max_hist_len=0, autoinc=False, stream=None,
-                 check=True) -> int:
+                 check=True, force_bisection=False) -> int:
     """arc_sample_batch on CUDA tensors: logits [B, V] (row stride >= V), params uint8
     [B*48], out int32 [B], optional CSR history (int32), err_word uint32 [1], debug uint8
     [B*72], workspace uint8 (zero-filled once; allocated here when None)."""
@@ -214,7 +215,7 @@ def sample_batch(logits, params, out, hist_offsets=None, hist_ids=None, err_word
     if workspace is None:
         workspace = workspace_tensor(B, V, _dtype_code(logits), hist_offsets is not None, ctas_per_row,
                                      max_hist_len, device=logits.device)
-    opts = make_options(ctas_per_row, max_hist_len, autoinc, debug)
+    opts = make_options(ctas_per_row, max_hist_len, autoinc, debug, force_bisection)
     rc = load().arc_sample_batch(_ptr(logits), B, V, ld, _dtype_code(logits), _ptr(params),
                                  _ptr(hist_offsets), _ptr(hist_ids), _ptr(out), _ptr(err_word),
                                  _ptr(workspace), int(workspace.numel()), ctypes.byref(opts),

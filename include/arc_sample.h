@@ -133,7 +133,8 @@ typedef struct arc_row_debug {
     int32_t mode;       /* -1 invalid, 0 greedy, 1 inert, 2 filtered */
     uint32_t err;       /* ARC_ERR_* bits of this row */
     int32_t token;      /* the value written to out[row] */
-    int32_t passes;     /* passes over the row's on-chip copy */
+    int32_t passes;     /* 1: greedy, default or direct selection; >= 2: threshold
+                           bisection ran, one more per pass over the row */
     uint32_t kappa_k;   /* top-k survivor set */
     int32_t iota_k;
     uint32_t kappa_r;   /* final survivor set (top-k, then top-p, then min-p) */
@@ -148,6 +149,11 @@ typedef struct arc_row_debug {
 
 /* arc_sample_options.flags */
 #define ARC_OPT_STEP_AUTOINC 0x1u /* after reading params[row].step, store step + 1 */
+/* filtered rows skip the direct selection (exact enumeration of the few ids
+ * above a provable floor) and take the threshold bisection over the whole
+ * row; both are exact, so tokens and survivor sets do not change -- a switch
+ * for cross-checking the two (arc_row_debug.passes tells which ran) */
+#define ARC_OPT_FORCE_BISECTION 0x2u
 
 /* Host struct; pass NULL for defaults. */
 typedef struct arc_sample_options {

@@ -16,7 +16,7 @@ from device_logits_sampling_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-def run(S, w, ld=None, ctas_per_row=0, max_hist_len=0, autoinc=False, params=None):
+def run(S, w, ld=None, ctas_per_row=0, max_hist_len=0, autoinc=False, params=None, force_bisection=False):
     import torch
 
     logits = S.logits_tensor(w, ld=ld)
@@ -26,7 +26,7 @@ def run(S, w, ld=None, ctas_per_row=0, max_hist_len=0, autoinc=False, params=Non
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     dbg = S.debug_tensor(w.B)
     S.sample_batch(logits, prm, out, hoff, hids, err_word=err, debug=dbg, ctas_per_row=ctas_per_row,
-                   max_hist_len=max_hist_len, autoinc=autoinc)
+                   max_hist_len=max_hist_len, autoinc=autoinc, force_bisection=force_bisection)
     torch.cuda.synchronize()
     return out.cpu().numpy(), S.debug_records(dbg), int(err.item()) & 0xFFFFFFFF
 
@@ -286,6 +286,33 @@ def test_distribution_matches_softmax(cuda_lib, kind):
     # and the individual tokens follow the oracle
     rows = list(range(0, B, 997))
     parity.check_batch(w, tokens, dbg, rows=rows)
+    # the threshold bisection draws the same token for every seed: the two
+    # exact selections are at total-variation distance 0
+    tokens_b, dbg_b, _ = run(cuda_lib, w, force_bisection=True)
+    assert np.array_equal(tokens_b, tokens)
+    if kind != "plain":
+        assert (dbg_b["passes"] >= 2).all() and (dbg["passes"] == 1).all()
+
+
+@pytest.mark.parametrize("name", ["mixed_quarters", "adversarial_ties", "penalized"])
+def test_enumeration_and_bisection_agree(cuda_lib, name):
+    """Exact enumeration of the few ids above the floor and threshold bisection
+    over the whole row select the same survivors and draw the same tokens;
+    the debug pass counts tell which path each filtered row took."""
+    w, _ = named(name)
+    mhl = 256 if w.hist_offsets is not None else 0
+    t1, d1, e1 = run(cuda_lib, w, max_hist_len=mhl)
+    t2, d2, e2 = run(cuda_lib, w, max_hist_len=mhl, force_bisection=True)
+    assert e1 == e2
+    assert np.array_equal(t1, t2)
+    for f in ("mode", "kappa_k", "iota_k", "kappa_r", "iota_r", "mass_r", "target"):
+        assert np.array_equal(d1[f], d2[f]), f
+    filtered = d1["mode"] == 2
+    assert (d2["passes"][filtered] >= 2).all()
+    assert (d2["passes"][~filtered] == d1["passes"][~filtered]).all()
+    direct = int((d1["passes"][filtered] == 1).sum())
+    print(f"{name}: filtered rows {int(filtered.sum())}, direct selection {direct}, "
+          f"bisection {int(filtered.sum()) - direct}")
 
 
 def test_graph_replay_reads_step_from_device(cuda_lib):
