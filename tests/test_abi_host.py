@@ -96,6 +96,12 @@ def test_bad_arguments_fail_before_any_cuda_call(lib):
     assert call_batch(lib, ws=None) == sampler.ARC_E_WORKSPACE
     assert call_batch(lib, ws=FAKE + 8) == sampler.ARC_E_ALIGN
     assert call_batch(lib, opts=sampler.Options(0x80, 0, 0, 0, None)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, opts=sampler.Options(0x4, 0, 0, 0, None)) == sampler.ARC_E_OPTION
+    # both defined flags together are a valid option set (checked without CUDA by the plan)
+    both = sampler.Options(sampler.ARC_OPT_STEP_AUTOINC | sampler.ARC_OPT_FORCE_BISECTION, 0, 0, 0, None)
+    geom = sampler.Geometry()
+    assert lib.arc_sample_plan(2, 1000, 1, 0, ctypes.byref(both), ctypes.byref(geom)) == sampler.ARC_OK
+    assert lib.arc_sample_workspace_bytes(2, 1000, 1, 0, ctypes.byref(both)) > 0
     assert call_batch(lib, opts=sampler.Options(0, 0, -1, 0, None)) == sampler.ARC_E_OPTION
     assert call_batch(lib, opts=sampler.Options(0, 0, 0, 5, None)) == sampler.ARC_E_OPTION
     g = lib.arc_sample_greedy
