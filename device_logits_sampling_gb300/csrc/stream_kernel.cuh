@@ -1008,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
     // the scan)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // the slice headers (warp 0) and the chunk tables (warps 1-7) load while
+    // the warp records (warp 0) and the chunk tables (warps 1-7) load while
     // the parameters do: nothing here waits for them
     if (warp == 0) {
         float v = -INFINITY;
