@@ -87,6 +87,37 @@ def test_drain_across_the_stamp_wrap(lib):
     assert got["stamp"].tolist() == [(1 << 32) - 1, 0, 1] and got["token"].tolist() == [1, 2, 3]
 
 
+def test_drain_waits_for_records_published_concurrently(lib):
+    """A writer thread publishes records (fields first, stamp last) while the
+    C drain, which runs without the interpreter lock, polls for them."""
+    import threading
+    import time
+
+    cap, n = 16, 200
+    ring = np.zeros(cap, dtype=decode.RECORD_DTYPE)
+    drained = []
+
+    def writer():
+        for i in range(n):
+            while len(drained) + cap <= i:  # never lap the reader
+                time.sleep(0)
+            slot = ring[i % cap]
+            slot["token"], slot["position"], slot["owner"] = i * 3, i, 5
+            ring["stamp"][i % cap] = i + 1
+            if i % 7 == 0:
+                time.sleep(0.0005)
+
+    t = threading.Thread(target=writer)
+    t.start()
+    first = 0
+    while first < n:
+        got = decode.ring_drain(ring.ctypes.data, cap, first, min(4, n - first), max_spins=1 << 30)
+        drained.extend(got["token"].tolist())
+        first += len(got)
+    t.join()
+    assert drained == [3 * i for i in range(n)]
+
+
 def test_commit_rejects_bad_arguments_before_any_cuda_call(lib):
     F = 0x1000  # never dereferenced: every check below fails first
     c = lib.arc_decode_commit
