@@ -27,8 +27,16 @@
 
 namespace arc {
 
+// The local histogram adds 64-bit masses as four pieces of pbits bits with
+// native 32-bit shared atomics (a 64-bit shared atomic add is a compare-and-
+// swap loop, which heavy ties turn into thousands of retries).  Masses are
+// below 2^(F+1) with F = 62 - ceil(log2 V), and a bin holds at most V ids, so
+// pbits = min(16, F - 30) keeps every piece's sum below 2^32 while four
+// pieces cover F + 1 bits, for every row the plan admits (V <= 2^20).
+constexpr int kPieces = 4;
+
 struct __align__(16) SampleShared {
-    uint64_t lhist[kBins];  // this CTA's histogram
+    uint32_t lhist[kBins * kPieces];  // this CTA's histogram: each bin's sum in kPieces 12-bit pieces
     uint64_t ghist[kBins];  // the cluster's histogram (every CTA adds into it)
     uint64_t cval[kCand];   // gathered candidates: id or mass
     uint32_t ckey[kCand];   //   and key
@@ -42,6 +50,7 @@ struct __align__(16) SampleShared {
 };
 
 constexpr uint32_t kErrInternal = ARC_ERR_INTERNAL;
+constexpr int kBatch = 8;  // rounds whose loads a pass issues together
 
 // Survivor predicate on the penalised logit z at id `idx`:
 // survive iff z > zt || (z == zt && idx < iota); iota == INT_MAX means z >= zt.
@@ -87,6 +96,7 @@ struct RowCtx {
     bool row_nan;
     // weights: w = ex2((z - m) * c), or [z == m] when m = +inf
     float m, c, scale;
+    int pbits;  // histogram piece width (see kPieces)
     bool infm;
     int par;           // exchange ring parity
     int passes;
@@ -114,8 +124,10 @@ struct RowCtx {
         return vmax[c * cps + ((v - c * vps) >> 5)] >= thr;
     }
 
-    __device__ __forceinline__ void load(int v, float (&z)[VEC]) const {
-        const uint4 raw = raw_vec(v);
+    __device__ __forceinline__ void load(int v, float (&z)[VEC]) const { unpack_patched(v, raw_vec(v), z); }
+
+    // vector v's logits from its raw 16 bytes, history penalties applied
+    __device__ __forceinline__ void unpack_patched(int v, const uint4& raw, float (&z)[VEC]) const {
         E::unpack(raw, z);
         if (HIST && has_patch) {
             const int l0 = v * VEC;
@@ -127,6 +139,37 @@ struct RowCtx {
                 for (int e = 0; e < VEC; ++e) {
                     const int li = l0 + e;
                     if ((bits >> e) & 1u) z[e] = patch[base + __popc(word & ((1u << (li & 31)) - 1u))];
+                }
+            }
+        }
+    }
+
+    // One pass over this thread's vectors v = j * kThreads + tid, j < rounds:
+    // the loads of kBatch rounds go out together (a pass over a row in global
+    // memory costs rounds / kBatch round trips, not rounds).  body(j, v, z)
+    // runs for the vectors with want(v); end(j) runs after round j in every
+    // thread (uniform, so it may hold warp collectives).
+    template <class Want, class Body, class End>
+    __device__ __forceinline__ void batched_pass(Want want, Body body, End end) const {
+        for (int j0 = 0; j0 < rounds; j0 += kBatch) {
+            uint4 raw[kBatch];
+            bool ok[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int v = (j0 + u) * kThreads + tid;
+                ok[u] = (j0 + u) < rounds && v < nv && want(v);
+                if (ok[u]) raw[u] = raw_vec(v);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (j0 + u < rounds) {
+                    const int v = (j0 + u) * kThreads + tid;
+                    if (ok[u]) {
+                        float z[VEC];
+                        unpack_patched(v, raw[u], z);
+                        body(j0 + u, v, z);
+                    }
+                    end(j0 + u);
                 }
             }
         }
@@ -248,12 +291,23 @@ struct RowCtx {
 
     __device__ __forceinline__ void lhist_add(const Window& W, uint32_t k, uint64_t wt) {
         if (k < W.klo || k > W.khi) return;
-        atomicAdd(reinterpret_cast<unsigned long long*>(&S.lhist[(W.khi - k) >> W.sh]),
-                  static_cast<unsigned long long>(wt));
+        uint32_t* h = &S.lhist[((W.khi - k) >> W.sh) * kPieces];
+        const uint64_t mask = (uint64_t{1} << pbits) - 1;
+#pragma unroll
+        for (int q = 0; q < kPieces; ++q) {
+            const uint32_t piece = static_cast<uint32_t>((wt >> (q * pbits)) & mask);
+            if (piece) atomicAdd(h + q, piece);
+        }
+    }
+    __device__ __forceinline__ uint64_t lhist_bin(int b) const {
+        uint64_t v = 0;
+#pragma unroll
+        for (int q = 0; q < kPieces; ++q) v += static_cast<uint64_t>(S.lhist[b * kPieces + q]) << (q * pbits);
+        return v;
     }
 
     __device__ __forceinline__ void lhist_clear() {
-        for (int b = tid; b < kBins; b += kThreads) S.lhist[b] = 0;
+        for (int b = tid; b < kBins * kPieces; b += kThreads) S.lhist[b] = 0;
         __syncthreads();
     }
 
@@ -275,7 +329,7 @@ struct RowCtx {
     __device__ __forceinline__ void push_hist() {
         if (ghist_zeroed >= epoch) xsync();
         for (int b = tid; b < kBins; b += kThreads) {
-            const uint64_t v = S.lhist[b];
+            const uint64_t v = lhist_bin(b);
             if (v)
                 for (int q = 0; q < s; ++q)
                     atomicAdd(reinterpret_cast<unsigned long long*>(cl.map_shared_rank(S.ghist, q) + b),
@@ -392,18 +446,15 @@ __device__ void pass_hist(Ctx& X, const Window& W, const Surv& D) {
     X.lhist_clear();
     const float zlo = Ctx::lo_float(W.klo), zhi = key_to_float(W.khi);
     const float thr = fmaxf(zlo, D.zt);
-    for (int j = 0; j < X.rounds; ++j) {
-        const int v = j * kThreads + X.tid;
-        if (v < X.nv && X.may_hold(v, thr)) {
-            float z[VEC];
-            X.load(v, z);
-            const int g0 = X.a0 + v * VEC;
+    X.batched_pass([&](int v) { return X.may_hold(v, thr); },
+                   [&](int, int v, const float(&z)[VEC]) {
+                       const int g0 = X.a0 + v * VEC;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e)
-                if (z[e] >= zlo && z[e] <= zhi && D.test(z[e], g0 + e))
-                    X.lhist_add(W, fkey(z[e]), MASS ? X.fix(X.weight(z[e])) : 1u);
-        }
-    }
+                       for (int e = 0; e < VEC; ++e)
+                           if (z[e] >= zlo && z[e] <= zhi && D.test(z[e], g0 + e))
+                               X.lhist_add(W, fkey(z[e]), MASS ? X.fix(X.weight(z[e])) : 1u);
+                   },
+                   [](int) {});
     X.passes++;
     __syncthreads();
 }
@@ -416,22 +467,19 @@ __device__ void pass_collect(Ctx& X, uint32_t lo, uint32_t hi, const Surv& D) {
     if (X.cand_zeroed >= X.epoch) X.xsync();
     const float zlo = Ctx::lo_float(lo), zhi = key_to_float(hi);
     const float thr = fmaxf(zlo, D.zt);
-    for (int j = 0; j < X.rounds; ++j) {
-        const int v = j * kThreads + X.tid;
-        if (v < X.nv && X.may_hold(v, thr)) {
-            float z[VEC];
-            X.load(v, z);
-            const int g0 = X.a0 + v * VEC;
+    X.batched_pass([&](int v) { return X.may_hold(v, thr); },
+                   [&](int, int v, const float(&z)[VEC]) {
+                       const int g0 = X.a0 + v * VEC;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                if (z[e] >= zlo && z[e] <= zhi && D.test(z[e], g0 + e)) {
-                    const uint32_t k = fkey(z[e]);
-                    if (k >= lo && k <= hi)
-                        X.push_cand(k, MASS ? X.fix(X.weight(z[e])) : static_cast<uint64_t>(g0 + e));
-                }
-            }
-        }
-    }
+                       for (int e = 0; e < VEC; ++e) {
+                           if (z[e] >= zlo && z[e] <= zhi && D.test(z[e], g0 + e)) {
+                               const uint32_t k = fkey(z[e]);
+                               if (k >= lo && k <= hi)
+                                   X.push_cand(k, MASS ? X.fix(X.weight(z[e])) : static_cast<uint64_t>(g0 + e));
+                           }
+                       }
+                   },
+                   [](int) {});
     X.passes++;
 }
 
@@ -442,24 +490,23 @@ __device__ void pass_mass(Ctx& X, int mode, const Surv& D, const Window& W) {
     constexpr int VEC = Ctx::VEC;
     if (HISTO) X.lhist_clear();
     const float zlo = Ctx::lo_float(W.klo), zhi = key_to_float(W.khi);
-    for (int j = 0; j < X.rounds; ++j) {
-        const int v = j * kThreads + X.tid;
-        uint64_t q = 0;
-        if (v < X.nv && (mode == kAll || X.may_hold(v, D.zt))) {
-            float z[VEC];
-            X.load(v, z);
-            const int g0 = X.a0 + v * VEC;
-            q = X.vec_mass(mode, z, g0, D);
-            if (HISTO && X.may_hold(v, zlo)) {
+    uint64_t q = 0;
+    X.batched_pass([&](int v) { return mode == kAll || X.may_hold(v, D.zt); },
+                   [&](int, int v, const float(&z)[VEC]) {
+                       const int g0 = X.a0 + v * VEC;
+                       q = X.vec_mass(mode, z, g0, D);
+                       if (HISTO && X.may_hold(v, zlo)) {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e)
-                    if (z[e] >= zlo && z[e] <= zhi && Ctx::in_domain(mode, D, z[e], g0 + e))
-                        X.lhist_add(W, fkey(z[e]), X.fix(X.weight(z[e])));
-            }
-        }
-        q = warp_sum_u64(q);
-        if (X.lane == 0) X.Wsum[j * kWarps + X.warp] = q;
-    }
+                           for (int e = 0; e < VEC; ++e)
+                               if (z[e] >= zlo && z[e] <= zhi && Ctx::in_domain(mode, D, z[e], g0 + e))
+                                   X.lhist_add(W, fkey(z[e]), X.fix(X.weight(z[e])));
+                       }
+                   },
+                   [&](int j) {
+                       const uint64_t t = warp_sum_u64(q);
+                       if (X.lane == 0) X.Wsum[j * kWarps + X.warp] = t;
+                       q = 0;
+                   });
     X.passes++;
 }
 
@@ -474,18 +521,17 @@ __device__ __forceinline__ int mass_mode(const Ctx& X, const Surv& D) {
 template <class Ctx>
 __device__ int tie_walk(Ctx& X, float zt, uint64_t need) {
     constexpr int VEC = Ctx::VEC;
-    for (int j = 0; j < X.rounds; ++j) {
-        const int v = j * kThreads + X.tid;
-        uint64_t q = 0;
-        if (v < X.nv && X.may_hold(v, zt)) {
-            float z[VEC];
-            X.load(v, z);
+    uint64_t q = 0;
+    X.batched_pass([&](int v) { return X.may_hold(v, zt); },
+                   [&](int, int, const float(&z)[VEC]) {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) q += (z[e] == zt) ? 1u : 0u;
-        }
-        q = warp_sum_u64(q);
-        if (X.lane == 0) X.Wsum[j * kWarps + X.warp] = q;
-    }
+                       for (int e = 0; e < VEC; ++e) q += (z[e] == zt) ? 1u : 0u;
+                   },
+                   [&](int j) {
+                       const uint64_t t = warp_sum_u64(q);
+                       if (X.lane == 0) X.Wsum[j * kWarps + X.warp] = t;
+                       q = 0;
+                   });
     X.passes++;
     X.publish_wsum_total(0);
     X.xsync();
@@ -619,11 +665,19 @@ __device__ bool select_mass(Ctx& X, Window W, const Surv& K, uint64_t tgt, float
             return true;
         }
         tgt -= r.before;
+        // no id in the bin weighs more than its top key: a bin whose mass is
+        // above kCand such weights holds more ids than a gather keeps (a run
+        // of ties, typically), so it is bisected without gathering
+        const uint64_t wtop = X.fix(X.weight(key_to_float(hi)));
+        const bool too_many = wtop == 0 || r.inbin / wtop > static_cast<uint64_t>(kCand);
         // gather the bin's ids (key, mass) into every CTA and find the largest
         // key whose mass at or above it reaches the target
-        pass_collect<Ctx, true>(X, lo, hi, K);
-        X.xsync();
-        const uint32_t got = X.S.ccount;
+        uint32_t got = UINT32_MAX;
+        if (!too_many) {
+            pass_collect<Ctx, true>(X, lo, hi, K);
+            X.xsync();
+            got = X.S.ccount;
+        }
         if (got <= static_cast<uint32_t>(kCand)) {
             const int nc = static_cast<int>(got);
             uint32_t best = 0;
@@ -644,7 +698,7 @@ __device__ bool select_mass(Ctx& X, Window W, const Surv& K, uint64_t tgt, float
             return true;
         }
         // too many ids: bisect the bin with another histogram pass
-        X.cand_clear();
+        if (!too_many) X.cand_clear();
         W.klo = lo;
         W.khi = hi;
         W.sh = max(0, W.sh - kBinBits);

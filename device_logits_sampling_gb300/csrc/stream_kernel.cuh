@@ -888,6 +888,7 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     X.m = m;
     X.c = st.cT;
     X.scale = st.scale;
+    X.pbits = min(16, a.F - 30);
     X.infm = st.infm;
     for (int b = tid; b < kBins; b += kThreads) KS.fb.ghist[b] = 0;
     if (tid == 0) {
@@ -1392,8 +1393,15 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                         }
                     }
                 };
+                // the gather stops once more ids than the selection holds are
+                // found (the threshold bisection then takes the row)
+                auto overflowed = [&]() {
+                    const uint32_t c = *reinterpret_cast<volatile const uint32_t*>(&SS.ccount);
+                    return __shfl_sync(0xFFFFFFFFu, c, 0) > static_cast<uint32_t>(kCandCap);
+                };
                 // single vectors: lane i reads entries i and i + 32 of each 64
                 for (int i0 = 0; i0 < nsg; i0 += 64) {
+                    if (i0 > 0 && overflowed()) break;
                     uint4 raw[2];
                     int vrow[2];
 #pragma unroll
@@ -1421,7 +1429,10 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                 }
                 // whole chunks
                 for (int r0 = 0; r0 < nw; r0 += kCollectU) {
-                    if (r0 > 0) stage_round(r0);
+                    if (r0 > 0) {
+                        if (overflowed()) break;  // (no copy of this warp is in flight here)
+                        stage_round(r0);
+                    }
                     cp_async_wait_all();
                     __syncwarp();
                     const int nst = min(kCollectU, nw - r0);
