@@ -11,6 +11,7 @@
 namespace {
 
 constexpr int kCommitThreads = 1024;
+constexpr uint32_t kMaxCapacity = 1u << 30;  // the "writing" stamp (two laps back) stays unambiguous
 
 struct CommitArgs {
     const int32_t* tokens;
@@ -32,6 +33,12 @@ struct CommitArgs {
 __device__ __forceinline__ void store_release_sys(uint32_t* p, uint32_t v) {
     asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void store_relaxed_sys(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's earlier stores before its later ones for every
+// observer, the host included.
+__device__ __forceinline__ void fence_acq_rel_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
 
 // One CTA: every row of the step, then the ring head.  The range checks come
 // before any write of the row; a refused row publishes a record with token -1.
@@ -51,6 +58,13 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
         faults |= bad;
         const uint64_t idx = head + static_cast<uint64_t>(r);
         arc_commit_record* rec = a.ring + (idx % a.capacity);
+        // a slot being rewritten first carries a "writing" stamp, two laps
+        // behind the new record (matches no record a reader can be waiting
+        // for, and reads as behind rather than as an overrun), so a host copy
+        // taken while the fields change is never confirmed by its second
+        // stamp read
+        store_relaxed_sys(&rec->stamp, static_cast<uint32_t>(idx + 1 - 2 * static_cast<uint64_t>(a.capacity)));
+        fence_acq_rel_sys();
         rec->token = bad ? -1 : tok;
         rec->position = pos;
         rec->owner = a.owners ? a.owners[r] : 0u;
@@ -72,7 +86,8 @@ int arc_decode_commit(const int32_t* tokens, int64_t B, int32_t V, int32_t* next
     if (tokens == nullptr || next_ids == nullptr || positions == nullptr || ring == nullptr ||
         head == nullptr)
         return ARC_E_NULL;
-    if (B <= 0 || V <= 0 || max_position <= 0 || capacity == 0 || static_cast<uint64_t>(B) > capacity)
+    if (B <= 0 || V <= 0 || max_position <= 0 || capacity == 0 || static_cast<uint64_t>(B) > capacity ||
+        capacity > kMaxCapacity)
         return ARC_E_SHAPE;
     CommitArgs a{tokens, B, V, next_ids, positions, max_position, owners, ring, capacity, head, fault_word};
     commit_kernel<<<1, kCommitThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
@@ -102,8 +117,9 @@ int64_t arc_ring_drain(const arc_commit_record* ring, uint32_t capacity, uint64_
         out[i].position = __atomic_load_n(&rec->position, __ATOMIC_RELAXED);
         out[i].owner = __atomic_load_n(&rec->owner, __ATOMIC_RELAXED);
         out[i].stamp = stamp;
-        // the slot may be rewritten by a later lap while being read: the
-        // stamp read again after the fields confirms the copy
+        // the slot may be rewritten by a later lap while being read: a writer
+        // replaces the stamp before it touches the fields (see commit_kernel),
+        // so the stamp read again after the fields confirms the copy
         std::atomic_thread_fence(std::memory_order_acquire);
         if (__atomic_load_n(&rec->stamp, __ATOMIC_RELAXED) != want) return ARC_E_RING_OVERRUN;
     }

@@ -20,11 +20,14 @@
  * The pages give no code for either; the record layout and the calls below
  * are this library's own.
  *
- * Ordering: arc_decode_commit is one kernel on the caller's stream.  Record
- * fields are stored before the record's stamp, and the stamp is stored with
- * system-scope release semantics, so a host that reads the stamp with acquire
- * semantics (arc_ring_drain does) and finds it matching sees the whole
- * record.  Every argument is a pointer or a size and the ring index lives in
+ * Ordering: arc_decode_commit is one kernel on the caller's stream.  A slot
+ * is rewritten as a sequence lock: its stamp first becomes a "writing" value
+ * (the new record's stamp minus twice the capacity, which no reader waits
+ * for), a system-scope fence follows, then the fields, and last the new
+ * stamp with system-scope release semantics.  A host that reads the stamp
+ * with acquire semantics (arc_ring_drain does) and finds it matching sees
+ * the whole record, and a copy taken while the slot was being rewritten
+ * fails its second stamp read.  Every argument is a pointer or a size and the ring index lives in
  * device memory (*head), so a commit captured into a CUDA graph publishes
  * fresh records on every replay.
  */
@@ -65,7 +68,7 @@ typedef struct arc_commit_record {
  *   owners        device [B] or NULL: owner tags copied into the records
  *   ring          device-visible address of `capacity` records in pinned,
  *                 mapped host memory (arc_ring_alloc gives both addresses)
- *   capacity      records in the ring, >= B
+ *   capacity      records in the ring, >= B and <= 2^30
  *   head          device uint64: records published by all earlier commits;
  *                 this call publishes records *head .. *head + B - 1, record
  *                 i at ring[i % capacity], and adds B

@@ -87,6 +87,69 @@ def test_drain_across_the_stamp_wrap(lib):
     assert got["stamp"].tolist() == [(1 << 32) - 1, 0, 1] and got["token"].tolist() == [1, 2, 3]
 
 
+def test_drain_never_confirms_a_slot_that_is_being_rewritten(lib):
+    """A slot in the middle of a rewrite (the "writing" stamp, two laps behind
+    the new record, with the new lap's fields already stored) is not a record
+    of either lap: the drain returns short instead of a mixed record."""
+    cap = 4
+    ring = np.zeros(cap, dtype=decode.RECORD_DTYPE)
+    for i in range(cap):  # lap 0 published
+        ring[i] = (10 + i, i, 7, i + 1)
+    new = cap + 1  # record 5 is being written into slot 1
+    ring[1]["token"], ring[1]["position"], ring[1]["owner"] = 99, 5, 8
+    ring[1]["stamp"] = (new + 1 - 2 * cap) % (1 << 32)
+    got = decode.ring_drain(ring.ctypes.data, cap, 0, cap, max_spins=50)
+    assert got["token"].tolist() == [10]  # record 1 is neither confirmed nor mixed
+    assert len(decode.ring_drain(ring.ctypes.data, cap, new, 1, max_spins=50)) == 0
+    ring[1]["stamp"] = new + 1  # the rewrite completes: record 1 is overrun, record 5 is readable
+    with pytest.raises(sampler.ArcError) as e:
+        decode.ring_drain(ring.ctypes.data, cap, 1, 1, max_spins=50)
+    assert e.value.rc == decode.ARC_E_RING_OVERRUN
+    assert decode.ring_drain(ring.ctypes.data, cap, new, 1)[0].tolist() == (99, 5, 8, new + 1)
+
+
+def test_drain_against_a_writer_that_laps_it(lib):
+    """A writer thread rewrites slots as the commit kernel does (writing stamp,
+    fields, new stamp) and laps the reader at will: every record the drain
+    returns is whole (its fields agree with its stamp); a lapped read is an
+    overrun, never a mixed record."""
+    import threading
+
+    cap, n = 8, 4000
+    ring = np.zeros(cap, dtype=decode.RECORD_DTYPE)
+    done = []
+
+    def writer():
+        for i in range(n):
+            slot = i % cap
+            ring["stamp"][slot] = (i + 1 - 2 * cap) % (1 << 32)
+            ring["token"][slot], ring["position"][slot], ring["owner"][slot] = 3 * i, i, i % 1000
+            ring["stamp"][slot] = i + 1
+        done.append(True)
+
+    t = threading.Thread(target=writer)
+    t.start()
+    seen = overruns = 0
+    first = 0
+    while not done or first < n:
+        try:
+            got = decode.ring_drain(ring.ctypes.data, cap, first, 4, max_spins=200)
+        except sampler.ArcError as e:
+            assert e.rc == decode.ARC_E_RING_OVERRUN
+            overruns += 1
+            first = max(first + 1, int(ring["stamp"].max()) - cap)  # skip ahead of the writer
+            continue
+        for r in got:
+            i = int(r["stamp"]) - 1
+            assert (int(r["token"]), int(r["position"]), int(r["owner"])) == (3 * i, i, i % 1000)
+        seen += len(got)
+        first += len(got)
+        if done and len(got) == 0:
+            break
+    t.join()
+    assert seen > 0
+
+
 def test_drain_waits_for_records_published_concurrently(lib):
     """A writer thread publishes records (fields first, stamp last) while the
     C drain, which runs without the interpreter lock, polls for them."""
