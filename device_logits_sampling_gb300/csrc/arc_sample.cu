@@ -30,6 +30,7 @@ struct Plan {
     int cs_off = 0;
     int cid_off = 0;
     int cv2_off = 0;
+    int cmv_off = -1;
     int clist_off = 0;
     int cand_off = 0;
     int sorted_off = 0;
@@ -115,9 +116,14 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     int64_t fb_patch = 0;
     if (has_hist) {
         const int64_t nwords = (fb_rounds * kThreads * vec + 31) / 32;
-        fb_patch = 2 * nwords * 4 + 2 * int64_t{cap} * 4;
+        fb_patch = r128(2 * nwords * 4 + 2 * int64_t{cap} * 4);
     }
-    const int64_t fin_smem = cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch;
+    // the chunk max vectors of a filtered row, when they fit in 16 KB (else
+    // the finish reads them from the logits)
+    const int64_t cmv_raw = s * kChunks * 16;
+    const int64_t cmv_bytes = cmv_raw <= 16384 ? r128(cmv_raw) : 0;
+    const int64_t fin_smem =
+        cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch + cmv_bytes;
     const int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
     if (fin_smem > limit || scan_smem > limit) return ARC_E_UNSUPPORTED;
     p.s = static_cast<int>(s);
@@ -135,6 +141,11 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     p.fb_wsum_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes);
     p.fb_patch_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum);
     p.fb_rounds = static_cast<int>(fb_rounds);
+    p.cmv_off = cmv_bytes ? static_cast<int>(fin_smem - cmv_bytes) : -1;
+    // every region holds 16-byte vectors or 8-byte words: starts must be 16-byte aligned
+    for (const int off : {p.cs_off, p.cid_off, p.cv2_off, p.clist_off, p.cand_off, p.sorted_off, p.stage_off,
+                          p.fb_wsum_off, p.fb_patch_off, p.cmv_off})
+        if (off >= 0 && off % 16 != 0) return ARC_E_UNSUPPORTED;
     p.fin_smem = static_cast<int>(fin_smem);
     p.slices = B * s;
     p.F = 62 - ceil_log2(V);
@@ -203,10 +214,10 @@ std::atomic<uint64_t> g_prep_fin[2][2];
 std::atomic<uint64_t> g_prep_argmax[2];
 
 // Scratch of arc_sample_batch_static, for callers that cannot allocate device
-// memory: one array per device context, created with the module; its address
-// is looked up once per device and cached here.
+// memory: one array per device context, created with the module.  Host code
+// sees only a stand-in symbol; its device address is looked up in the current
+// context at every call.
 __device__ __align__(256) unsigned char g_static_workspace[ARC_STATIC_WORKSPACE_BYTES];
-std::atomic<uintptr_t> g_static_workspace_addr[kMaxDevices];
 
 }  // namespace
 
@@ -329,6 +340,7 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.cs_off = p.cs_off;
     fa.cid_off = p.cid_off;
     fa.cv2_off = p.cv2_off;
+    fa.cmv_off = p.cmv_off;
     fa.clist_off = p.clist_off;
     fa.cand_off = p.cand_off;
     fa.sorted_off = p.sorted_off;
@@ -372,18 +384,13 @@ int arc_sample_batch_static(const void* logits, int64_t B, int64_t V, int64_t ld
     rc = check_options(opts);
     if (rc != ARC_OK) return rc;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ARC_E_CUDA;
-    uintptr_t addr = g_static_workspace_addr[dev].load(std::memory_order_acquire);
-    if (addr == 0) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) return ARC_E_CUDA;
-        addr = reinterpret_cast<uintptr_t>(p);
-        g_static_workspace_addr[dev].store(addr, std::memory_order_release);
-    }
+    // the array's address in the current context (never cached: a device
+    // reset or another context loads the module at another address)
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_static_workspace) != cudaSuccess || addr == nullptr) return ARC_E_CUDA;
     // a plan that needs more than the array is refused there (ARC_E_WORKSPACE)
-    return arc_sample_batch(logits, B, V, ld, dtype, params, hist_offsets, hist_ids, out, err_word,
-                            reinterpret_cast<void*>(addr), ARC_STATIC_WORKSPACE_BYTES, opts, stream);
+    return arc_sample_batch(logits, B, V, ld, dtype, params, hist_offsets, hist_ids, out, err_word, addr,
+                            ARC_STATIC_WORKSPACE_BYTES, opts, stream);
 }
 
 int arc_sample_greedy(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype, int32_t* out,

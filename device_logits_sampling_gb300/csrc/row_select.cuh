@@ -27,16 +27,14 @@
 
 namespace arc {
 
-// The local histogram adds 64-bit masses as four pieces of pbits bits with
-// native 32-bit shared atomics (a 64-bit shared atomic add is a compare-and-
-// swap loop, which heavy ties turn into thousands of retries).  Masses are
-// below 2^(F+1) with F = 62 - ceil(log2 V), and a bin holds at most V ids, so
-// pbits = min(16, F - 30) keeps every piece's sum below 2^32 while four
-// pieces cover F + 1 bits, for every row the plan admits (V <= 2^20).
-constexpr int kPieces = 4;
+// The local histogram keeps each bin's 64-bit sum as two 32-bit words updated
+// with native 32-bit shared atomics (a 64-bit shared atomic add is a
+// compare-and-swap loop, which heavy ties turn into long retry chains): the
+// low word adds the low half, and the high word the high half plus one for
+// every add that wrapped the low word, so the sum is exact in any order.
 
 struct __align__(16) SampleShared {
-    uint32_t lhist[kBins * kPieces];  // this CTA's histogram: each bin's sum in kPieces 12-bit pieces
+    uint32_t lhist[kBins * 2];  // this CTA's histogram: bin b's sum is lhist[2b] + 2^32 lhist[2b + 1]
     uint64_t ghist[kBins];  // the cluster's histogram (every CTA adds into it)
     uint64_t cval[kCand];   // gathered candidates: id or mass
     uint32_t ckey[kCand];   //   and key
@@ -96,7 +94,6 @@ struct RowCtx {
     bool row_nan;
     // weights: w = ex2((z - m) * c), or [z == m] when m = +inf
     float m, c, scale;
-    int pbits;  // histogram piece width (see kPieces)
     bool infm;
     int par;           // exchange ring parity
     int passes;
@@ -291,23 +288,18 @@ struct RowCtx {
 
     __device__ __forceinline__ void lhist_add(const Window& W, uint32_t k, uint64_t wt) {
         if (k < W.klo || k > W.khi) return;
-        uint32_t* h = &S.lhist[((W.khi - k) >> W.sh) * kPieces];
-        const uint64_t mask = (uint64_t{1} << pbits) - 1;
-#pragma unroll
-        for (int q = 0; q < kPieces; ++q) {
-            const uint32_t piece = static_cast<uint32_t>((wt >> (q * pbits)) & mask);
-            if (piece) atomicAdd(h + q, piece);
-        }
+        uint32_t* h = &S.lhist[((W.khi - k) >> W.sh) * 2];
+        const uint32_t lo = static_cast<uint32_t>(wt), hi = static_cast<uint32_t>(wt >> 32);
+        const uint32_t old = atomicAdd(h, lo);
+        const uint32_t carry = (old + lo < old) ? 1u : 0u;
+        if (hi + carry) atomicAdd(h + 1, hi + carry);
     }
     __device__ __forceinline__ uint64_t lhist_bin(int b) const {
-        uint64_t v = 0;
-#pragma unroll
-        for (int q = 0; q < kPieces; ++q) v += static_cast<uint64_t>(S.lhist[b * kPieces + q]) << (q * pbits);
-        return v;
+        return (static_cast<uint64_t>(S.lhist[2 * b + 1]) << 32) | S.lhist[2 * b];
     }
 
     __device__ __forceinline__ void lhist_clear() {
-        for (int b = tid; b < kBins * kPieces; b += kThreads) S.lhist[b] = 0;
+        for (int b = tid; b < kBins * 2; b += kThreads) S.lhist[b] = 0;
         __syncthreads();
     }
 

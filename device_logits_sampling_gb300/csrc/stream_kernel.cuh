@@ -33,8 +33,10 @@ namespace arc {
 constexpr int kVpt = 4;                  // 16-byte vectors per thread in a scan CTA
 constexpr int kChunks = kVpt * kWarps;   // chunks per slice summary (32-vector chunks)
 constexpr int kHdrBytes = kWarps * 16;   // per-warp records of a slice
-constexpr int kNoteBytes = 16;           // slice 0 of a min-p row: T ln(min_p) in fp64
-constexpr int kSummaryBytes = kHdrBytes + kChunks * 16 + kNoteBytes;
+constexpr int kEntryBytes = kChunks * 16;  // chunk entries of a slice
+// a slice summary: warp records, chunk entries, and (filtered rows) the raw
+// 16-byte vector holding each chunk's max
+constexpr int kSummaryBytes = kHdrBytes + 2 * kEntryBytes;
 constexpr int kMaxRowCtas = 128;         // slices per row at most
 constexpr int kCandCap = 1024;           // ids the direct selection holds
 constexpr int kCollectU = 8;             // chunks per warp in flight while gathering
@@ -76,6 +78,7 @@ struct FinishArgs {
     int cs_off;        //   chunk masses,
     int cid_off;       //   chunk max vectors,
     int cv2_off;       //   chunk second vector maxima,
+    int cmv_off;       //   chunk max vectors (-1: read from the logits instead),
     int clist_off;     //   per-warp candidate chunk lists,
     int cand_off;      //   candidates (key, id, mass),
     int sorted_off;    //   the candidates in (key desc, id asc) order,
@@ -126,8 +129,8 @@ static_assert(sizeof(ChunkEntry) == 16, "chunk entry size");
 __device__ __forceinline__ const ChunkEntry* chunk_table(const unsigned char* sm) {
     return reinterpret_cast<const ChunkEntry*>(sm + kHdrBytes);
 }
-__device__ __forceinline__ const double* slice_note(const unsigned char* sm) {
-    return reinterpret_cast<const double*>(sm + kHdrBytes + kChunks * 16);
+__device__ __forceinline__ const uint4* max_vectors(const unsigned char* sm) {
+    return reinterpret_cast<const uint4*>(sm + kHdrBytes + kEntryBytes);
 }
 
 // weight of z relative to a reference max mr (chunk or row): ex2((z - mr) c);
@@ -299,7 +302,6 @@ enum : uint32_t {
     kRowChunks = 2u,  // chunk table
     kRowMass = 4u,    // chunk masses
     kRowFiltered = 8u,  // chunk max vectors and second vector maxima
-    kRowNote = 16u,     // min-p rows: slice 0 writes T ln(min_p)
 };
 constexpr int kAmUnknown = INT_MAX;  // slice record of a row whose first max id the scan leaves open
 
@@ -356,7 +358,6 @@ __device__ __forceinline__ ScanRowInfo scan_row_info(const ScanArgs& a, int row,
         R.bits = kRowArgmax;
     } else {
         R.bits = kRowChunks | (md.need_mass ? kRowMass : 0u) | (md.filtered ? kRowFiltered : 0u);
-        if (md.filtered && md.minp_on) R.bits |= kRowNote;
         if (HIST) R.bits |= kRowArgmax;  // penalised rows keep their first max id
     }
     R.cT = (R.bits & kRowMass) ? __fdiv_rn(1.4426950408889634f, R.P.temperature) : 0.0f;
@@ -560,6 +561,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         // entry j as soon as its fields are known, by lane 8j (which holds the
         // chunk's mass): nothing per chunk stays live across the loop
         ChunkEntry* ch = reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes);
+        uint4* mvec = reinterpret_cast<uint4*>(mysum + kHdrBytes + kEntryBytes);
         const bool filtered = (bits & kRowFiltered) != 0;
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) {
@@ -569,6 +571,10 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
                 const unsigned holders = __ballot_sync(0xFFFFFFFFu, xs[j] == mj[j] && xs[j] > -INFINITY);
                 fl = holders ? __ffs(holders) - 1 : -1;
                 u2 = warp_max_nonan(lane == fl ? -INFINITY : xs[j]);
+                // the max's vector as loaded (history patches are applied by
+                // the reader), so that a chunk with one vector at or above a
+                // later floor needs no second read of the logits
+                if (lane == fl) mvec[j * kWarps + warp] = j == 0 ? d[0] : (j == 1 ? d[1] : (j == 2 ? d[2] : d[3]));
             }
             if (lane == 8 * j) {
                 ChunkEntry ce;
@@ -666,13 +672,6 @@ __global__ void __launch_bounds__(kThreads, HIST ? 4 : 8) scan_kernel(const Scan
     }
     const ScanRowInfo R = scan_row_info<HIST>(a, row, pw);
     scan_slice<DT, HIST>(a, d, row, cidx, R, sh, dyn);
-    // slice 0 of a min-p row: T ln(min_p) in fp64 for the finish kernel, by
-    // one thread after its slice (fp64 is slow on this part)
-    if (cidx == 0 && tid == 0 && (R.bits & kRowNote)) {
-        unsigned char* note = const_cast<unsigned char*>(
-            reinterpret_cast<const unsigned char*>(slice_note(summary_at(a.summaries, a.s, row, 0))));
-        *reinterpret_cast<double*>(note) = static_cast<double>(R.P.temperature) * log(static_cast<double>(R.P.min_p));
-    }
 }
 
 // ------------------------------------------------------------------ finish helpers
@@ -888,7 +887,6 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     X.m = m;
     X.c = st.cT;
     X.scale = st.scale;
-    X.pbits = min(16, a.F - 30);
     X.infm = st.infm;
     for (int b = tid; b < kBins; b += kThreads) KS.fb.ghist[b] = 0;
     if (tid == 0) {
@@ -1004,6 +1002,14 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
         hbeg = a.hist_off[row];
         hn = max(0, a.hist_off[row + 1] - hbeg);
     }
+    // min-p: T ln(min_p) in fp64 (slow on this part), by the thread that uses
+    // it, while the scan still runs
+    double tl = 0.0;
+    if (tid == 0 && P.min_p > 0.0f && P.min_p <= 1.0f && isfinite(P.temperature) && P.temperature > 0.0f &&
+        !(P.top_k == 1))
+        tl = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
+    // the finish needs the chunk max vectors (filtered rows)
+    const bool want_mv = a.cmv_off >= 0 && param_errors(P) == 0 && RowMode(P, a.V).filtered;
     // launched early behind the scan kernel: its summaries are complete and
     // visible after this (the parameters and history above are not written by
     // the scan)
@@ -1024,11 +1030,6 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
 #pragma unroll
         for (int u = 0; u < kLdR; ++u)
             if (lane + 32 * u < nrec) r[u] = rec(lane + 32 * u);
-        // min-p: T ln(min_p), computed in fp64 by the scan kernel (slice 0)
-        double tl = 0.0;
-        if (lane == 0 && P.min_p > 0.0f && P.min_p <= 1.0f && isfinite(P.temperature) && P.temperature > 0.0f &&
-            !(P.top_k == 1))
-            tl = *slice_note(summary_at(a.summaries, s, row, 0));
 #pragma unroll
         for (int u = 0; u < kLdR; ++u) {
             if (lane + 32 * u < nrec) {
@@ -1055,10 +1056,15 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
         constexpr int kStride = kThreads - 32;
         for (int g0 = tid - 32; g0 < nch; g0 += kLd * kStride) {
             ChunkEntry e[kLd];
+            uint4 mv[kLd];
 #pragma unroll
             for (int u = 0; u < kLd; ++u) {
                 const int gi = g0 + u * kStride;
-                if (gi < nch) e[u] = chunk_table(summary_at(a.summaries, s, row, gi / kChunks))[gi % kChunks];
+                if (gi < nch) {
+                    const unsigned char* sm = summary_at(a.summaries, s, row, gi / kChunks);
+                    e[u] = chunk_table(sm)[gi % kChunks];
+                    if (want_mv) mv[u] = max_vectors(sm)[gi % kChunks];
+                }
             }
 #pragma unroll
             for (int u = 0; u < kLd; ++u) {
@@ -1068,6 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                     cs[gi] = e[u].S;
                     cln[gi] = e[u].lane;
                     cu2[gi] = e[u].u2;
+                    if (want_mv) reinterpret_cast<uint4*>(dyn + a.cmv_off)[gi] = mv[u];
                 }
             }
         }
@@ -1413,7 +1420,9 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                             const int c = g / kChunks;
                             const int vs = (g % kChunks) * 32 + cln[g];
                             const int sn = min((c + 1) * a.L, a.V) - c * a.L;
-                            raw[u] = E::global_vec(rowp + static_cast<int64_t>(c) * a.L * E::kBytes, vs, sn, a.aligned);
+                            raw[u] = want_mv ? reinterpret_cast<const uint4*>(dyn + a.cmv_off)[g]
+                                             : E::global_vec(rowp + static_cast<int64_t>(c) * a.L * E::kBytes, vs,
+                                                             sn, a.aligned);
                             vrow[u] = c * Lv + vs;
                         }
                     }

@@ -37,7 +37,7 @@ ARC_ERR_INTERNAL = 0x40
 
 ARC_OPT_STEP_AUTOINC = 0x1
 ARC_OPT_FORCE_BISECTION = 0x2
-ARC_STATIC_WORKSPACE_BYTES = 8 << 20  # scratch compiled into the library (arc_sample_batch_static)
+ARC_STATIC_WORKSPACE_BYTES = 16 << 20  # scratch compiled into the library (arc_sample_batch_static)
 
 # arc_row_debug, 72 bytes
 ROW_DEBUG_DTYPE = np.dtype(

@@ -50,8 +50,8 @@
  *
  * Workspace: arc_sample_batch needs a caller-owned device workspace of
  * arc_sample_workspace_bytes() bytes, 16-byte aligned.  It carries one small
- * summary per row slice from the scan kernel to the finish kernel of the same
- * call; every byte the finish kernel uses is written earlier in that call, so
+ * summary per row slice (1,152 bytes) from the scan kernel to the finish
+ * kernel of the same call; every byte the finish kernel uses is written earlier in that call, so
  * the workspace needs no initial contents and keeps nothing between calls.
  * Calls that share a workspace must be ordered (same stream, or events);
  * calls that overlap on the GPU and share a workspace race.
@@ -235,20 +235,23 @@ int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history,
  * per-slice summaries go to a scratch array of ARC_STATIC_WORKSPACE_BYTES
  * compiled into the library (a static device array, one per device context,
  * created when the CUDA runtime loads the library's kernels); the library
- * never calls an allocator.  The first call on a device looks up the array's
- * address (cudaGetSymbolAddress, once per device) and sets the kernels'
- * attributes: make it before any stream capture that contains a call.
+ * never calls an allocator.  Every call looks the array's address up in the
+ * current context (cudaGetSymbolAddress, a host-side lookup), so a device
+ * reset or another context never sees a stale address.  The first call on a
+ * device sets the kernels' attributes: make it before any stream capture
+ * that contains a call.
  *
  * Limit: a shape whose workspace on this device (arc_sample_plan
- * workspace_bytes, B x slices-per-row x 656 bytes) exceeds
- * ARC_STATIC_WORKSPACE_BYTES returns ARC_E_WORKSPACE with nothing enqueued;
- * at V = 129,280 that admits B up to 799.  Nothing in the array needs to
- * start at zero: each call writes every byte it later uses.  Every call on
- * a device shares the one array, so calls that may overlap on the GPU
- * (different streams without an ordering between them, or concurrent host
- * threads) race: the caller must serialise them.
+ * workspace_bytes = B x slices-per-row x 1,152 bytes) exceeds
+ * ARC_STATIC_WORKSPACE_BYTES returns ARC_E_WORKSPACE with nothing enqueued.
+ * At V = 129,280 a row has 16 slices in bf16 and 32 in fp32, so B up to 910
+ * (bf16) or 455 (fp32) is accepted.  Nothing in the array needs to start at
+ * zero: each call writes every byte it later uses.  Every call on a device
+ * shares the one array, so calls that may overlap on the GPU (different
+ * streams without an ordering between them, or concurrent host threads)
+ * race: the caller must serialise them.
  */
-#define ARC_STATIC_WORKSPACE_BYTES (8u << 20)
+#define ARC_STATIC_WORKSPACE_BYTES (16u << 20)
 
 int arc_sample_batch_static(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,
                             arc_row_params* params, const int32_t* hist_offsets,

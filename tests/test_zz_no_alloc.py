@@ -50,17 +50,60 @@ def test_static_matches_workspace_call_two_calls_in_a_row(cuda_lib, name):
         assert np.array_equal(dbg, ref_dbg)
 
 
+def _largest_accepted(S, V, dtype):
+    """The largest B whose planned workspace fits the library's static array."""
+    lo, hi = 1, 1 << 16
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if S.plan(mid, V, dtype).workspace_bytes <= S.ARC_STATIC_WORKSPACE_BYTES:
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo
+
+
+def test_static_limits_are_the_documented_ones():
+    # B x slices-per-row x 1,152 B <= 16 MiB: 16 bf16 slices or 32 fp32 slices
+    # per row at V = 129,280 (host-only planning, no GPU)
+    S = sampler
+    S.load()
+    assert _largest_accepted(S, 129_280, workloads.DTYPE_BF16) == 910
+    assert _largest_accepted(S, 129_280, workloads.DTYPE_F32) == 455
+
+
 @pytest.mark.gpu
-def test_static_refuses_a_shape_beyond_its_scratch(cuda_lib):
+@pytest.mark.parametrize("dtype,B_max", [(workloads.DTYPE_BF16, 910), (workloads.DTYPE_F32, 455)])
+def test_static_at_its_limit_and_one_past_it(cuda_lib, dtype, B_max):
+    """The largest accepted batch matches arc_sample_batch token for token; one
+    more row is refused with nothing enqueued."""
     import torch
 
     S = cuda_lib
-    B, V = 1024, 129_280  # 1024 rows x 16 slices x 656 B > ARC_STATIC_WORKSPACE_BYTES
-    assert S.plan(B, V, workloads.DTYPE_BF16).workspace_bytes > S.ARC_STATIC_WORKSPACE_BYTES
-    logits = torch.zeros((B, V), dtype=torch.bfloat16, device="cuda")
+    V = 129_280
+    w = workloads.random_case(seed=77 + dtype, B=B_max, V=V, dtype=dtype)
+    ref_tok, ref_err, _ = _run(S, w, static=False)
+    tok, err, _ = _run(S, w, static=True)
+    assert np.array_equal(tok, ref_tok) and err == ref_err
+    B = B_max + 1
+    tdt = torch.bfloat16 if dtype == workloads.DTYPE_BF16 else torch.float32
+    logits = torch.zeros((B, V), dtype=tdt, device="cuda")
     prm = S.params_tensor(workloads.make_params(B))
     out = torch.full((B,), -7, dtype=torch.int32, device="cuda")
     rc = S.sample_batch_static(logits, prm, out, check=False)
     assert rc == sampler.ARC_E_WORKSPACE
     torch.cuda.synchronize()
     assert int((out != -7).sum().item()) == 0  # nothing was enqueued
+
+
+@pytest.mark.gpu
+def test_static_after_a_different_shape(cuda_lib):
+    """Calls of different shapes share the array: each matches arc_sample_batch."""
+    S = cuda_lib
+    shapes = [(40, 129_280, workloads.DTYPE_BF16), (6, 20_000, workloads.DTYPE_F32),
+              (300, 50_000, workloads.DTYPE_BF16)]
+    for i, (B, V, dt) in enumerate(shapes):
+        w = workloads.random_case(seed=500 + i, B=B, V=V, dtype=dt)
+        ref_tok, ref_err, ref_dbg = _run(S, w, static=False)
+        tok, err, dbg = _run(S, w, static=True)
+        assert np.array_equal(tok, ref_tok) and err == ref_err
+        assert np.array_equal(dbg, ref_dbg)
