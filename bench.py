@@ -7,10 +7,16 @@ mode dispatch, top-k / top-p / min-p, inverse-CDF draw).  Prints one JSON line.
 
 value: rows/s with the logits already resident in HBM; K launches are
 replayed back to back from CUDA graphs, cycling over input copies whose total
-is larger than L2, and timed with CUDA events on the launch stream.
+is larger than L2, and timed with CUDA events on the launch stream; the
+per-step time is the median over --repeats such regions (min and max beside).
+configs: the same measurement for each of the five synthetic workloads (the
+small fp32 batch, the single-row decode loop greedy and with the defaults,
+the mixed batch, the penalised batch, the tied fp32 batch), plus the cost of
+the design the library replaces: one D2H copy of the bench batch's logits.
 e2e: the same metric through the C ABI from pinned host buffers, with the
 host->device copy of the logits and parameters and the device->host read of
 the tokens inside every step.
+cpu_baseline: the fp64 oracle on every host core (and on one thread).
 --impl reference: the fp64 oracle on the host cores (a bounded sample of rows
 per step), the only CPU use of oracle/ besides the cpu_baseline leg.
 """
@@ -126,25 +132,75 @@ def rows_of_shard(B: int, world: int, rank: int) -> range:
     return range(rank * B, (rank + 1) * B)
 
 
-def cpu_baseline(seconds: float = 12.0) -> dict:
-    """The oracle as it stands on this host, over the first rows of the batch (row mix kept)."""
+def _oracle_rows(task):
+    """Worker of the host-core oracle pool: sample rows (logits, params, row index)."""
     import oracle
+
+    z, prm, rows = task
+    for zi, pi, r in zip(z, prm, rows):
+        oracle.sample_row(zi, pi, int(r))
+    return len(rows)
+
+
+def host_info() -> dict:
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+def oracle_rate(z, params, rows, workers: int, passes: int = 1) -> float:
+    """Rows per second of the fp64 oracle over `rows` of a batch (repeated `passes`
+    times), on `workers` host processes (spawn start: no state shared with CUDA);
+    pool start-up is outside the timed region."""
+    import multiprocessing as mp
+
+    rows = list(rows)
+    if workers <= 1:
+        t0 = time.perf_counter()
+        for _ in range(passes):
+            _oracle_rows((z[rows], params[rows], rows))
+        return passes * len(rows) / (time.perf_counter() - t0)
+    per = max(1, len(rows) // (workers * 2))
+    tasks = [(z[rows[i:i + per]], params[rows[i:i + per]], rows[i:i + per]) for i in range(0, len(rows), per)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        pool.map(_oracle_rows, tasks[:workers])  # warm the workers (imports)
+        t0 = time.perf_counter()
+        n = 0
+        for _ in range(passes):
+            n += sum(pool.map(_oracle_rows, tasks))
+        dt = time.perf_counter() - t0
+    return n / dt
+
+
+def cpu_baseline() -> dict:
+    """The oracle as it stands on this host: every host core over the whole
+    mixed batch (4 passes), and one thread over its first 48 rows."""
     from device_logits_sampling_gb300 import workloads
 
     w = workloads.mixed_batch()
     z = w.logits_f32()
-    t0 = time.perf_counter()
-    n = 0
-    while n < w.B and (n < 16 or time.perf_counter() - t0 < seconds):
-        oracle.sample_row(z[n], w.params[n], n)
-        n += 1
-    dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n} rows of the B=256 mixed batch (row%4 mix kept), fp64 numpy, one thread"}
+    info = host_info()
+    cores = info["nproc"] or 1
+    all_cores = oracle_rate(z, w.params, range(w.B), cores, passes=4)
+    one = oracle_rate(z, w.params, range(48), 1)
+    return {"value": all_cores, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"4 passes over the 256 rows of the B=256 mixed batch (row%4 mix kept), fp64 numpy, "
+                      f"{cores} processes",
+            "single_thread_value": one, "single_thread_sample": "first 48 rows of the same batch, one thread",
+            "cpu_model": info["cpu_model"], "nproc": info["nproc"]}
 
 
 def bench_reference(args) -> None:
     """--impl reference: the fp64 oracle on the host cores, K timed steps of a bounded row sample."""
+    import multiprocessing as mp
+
     ws, rank, _ = dist_setup()
     if rank != 0:
         return
@@ -153,26 +209,31 @@ def bench_reference(args) -> None:
 
     w = workloads.mixed_batch()
     z = w.logits_f32()
-    # size the per-step sample so K + W steps take about a minute
+    info = host_info()
+    cores = info["nproc"] or 1
+    # size the per-step sample so K + W steps take about a minute on every core
     t0 = time.perf_counter()
     for r in range(4):
         oracle.sample_row(z[r], w.params[r], r)
     per_row = (time.perf_counter() - t0) / 4
-    rows = int(max(1, min(w.B, 60.0 / max(1, args.steps + args.warmup) / per_row)))
-    rows = max(4, rows - rows % 4) if rows >= 4 else rows
+    rows = int(max(4, min(w.B, cores * 60.0 / max(1, args.steps + args.warmup) / per_row)))
+    rows -= rows % 4
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        per = max(1, rows // cores)
 
-    def step(i):
-        base = (i * rows) % w.B
-        for j in range(rows):
-            r = (base + j) % w.B
-            oracle.sample_row(z[r], w.params[r], r)
+        def step(i):
+            base = (i * rows) % w.B
+            idx = [(base + j) % w.B for j in range(rows)]
+            tasks = [(z[idx[a:a + per]], w.params[idx[a:a + per]], idx[a:a + per]) for a in range(0, rows, per)]
+            pool.map(_oracle_rows, tasks)
 
-    for i in range(args.warmup):
-        step(i)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(i)
-    dt = time.perf_counter() - t0
+        for i in range(args.warmup):
+            step(i)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step(i)
+        dt = time.perf_counter() - t0
     value = rows * args.steps / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws,
@@ -181,12 +242,100 @@ def bench_reference(args) -> None:
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "V": w.V, "logits_dtype": "bf16",
                    "rows_per_step": rows},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{rows} rows per step of the B=256 mixed batch, fp64 numpy, one thread"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} rows per step of the B=256 mixed batch, fp64 numpy, {cores} processes",
+                         "cpu_model": info["cpu_model"]},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line))
+
+
+def graph_steps(sampler, stream, bufs, call, n):
+    """A CUDA graph of n steps, step i sampling input copy i % len(bufs)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                call(bufs[i % len(bufs)])
+    return g
+
+
+def time_steps(stream, graphs, repeats):
+    """Per-step microseconds of `repeats` timed regions, each replaying `graphs`
+    once back to back, with CUDA events on the launch stream."""
+    import torch
+
+    steps = sum(n for _, n in graphs)
+    out = []
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for g, _ in graphs:
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e3 / steps)
+    return out
+
+
+def bench_config(sampler, workloads, name, peak, steps, repeats):
+    """One named workload: graph-replayed steps over rotating input copies
+    (more than L2 in total), per-step time median and min over `repeats`
+    regions; the share of filtered rows that took the direct selection."""
+    import numpy as np
+    import torch
+
+    w = getattr(workloads, name[0])(**name[1])
+    B, V = w.B, w.V
+    nbuf = max(2, min(NBUF, int(3 * 129e6 // (B * V * w.elem_bytes)) + 1))
+    bufs = [sampler.logits_tensor(w) for _ in range(nbuf)]
+    prm = sampler.params_tensor(w.params)
+    hoff, hids = sampler.history_tensors(w)
+    mhl = int(np.diff(w.hist_offsets).max()) if hoff is not None else 0
+    out = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ws = sampler.workspace_tensor(B, V, w.dtype, hoff is not None, max_hist_len=mhl)
+    dbg = sampler.debug_tensor(B)
+    st = torch.cuda.Stream()
+    autoinc = name[0] == "single_row_peaked"  # the decode loop: the step advances on device
+    with torch.cuda.stream(st):
+        sampler.sample_batch(bufs[0], prm, out, hoff, hids, workspace=ws, max_hist_len=mhl, debug=dbg, stream=st)
+    st.synchronize()
+    d = sampler.debug_records(dbg)
+
+    def call(x):
+        sampler.sample_batch(x, prm, out, hoff, hids, workspace=ws, max_hist_len=mhl, autoinc=autoinc, stream=st)
+
+    g = graph_steps(sampler, st, bufs, call, steps)
+    g.replay()
+    st.synchronize()
+    ts = time_steps(st, [(g, steps)], repeats)
+    med, mn = statistics.median(ts), min(ts)
+    alg = B * V * w.elem_bytes + B * 48 + B * 4 + (4 * int(w.hist_ids.size) + 4 * (B + 1) if hoff is not None else 0)
+    filt = d["mode"] == 2
+    rec = {"B": B, "V": V, "logits_dtype": "bf16" if w.dtype == workloads.DTYPE_BF16 else "f32",
+           "us_per_step_median": med, "us_per_step_min": mn, "rows_per_s": B / (med * 1e-6),
+           "achieved_gbs": alg / (med * 1e-6) / 1e9, "frac_of_measured_peak": alg / (med * 1e-6) / 1e9 / peak,
+           "alg_bytes": alg, "steps": steps, "repeats": repeats, "input_copies": nbuf,
+           "filtered_rows": int(filt.sum()), "direct_selection_rows": int(((d["passes"] == 1) & filt).sum())}
+    if autoinc:
+        rec["note"] = "decode loop: the step counter advances on device (ARC_OPT_STEP_AUTOINC)"
+    del bufs, ws
+    torch.cuda.empty_cache()
+    return w.name, rec
+
+
+CONFIGS = [  # the five synthetic workloads, in the order of the configuration list
+    ("small_fp32", {}),
+    ("single_row_peaked", {"greedy": True}),
+    ("single_row_peaked", {}),
+    ("mixed_batch", {}),
+    ("penalized_batch", {}),
+    ("adversarial_ties", {}),
+]
 
 
 def bench_gpu(args) -> None:
@@ -223,21 +372,13 @@ def bench_gpu(args) -> None:
     stream.synchronize()
     assert int(err.item()) == 0, hex(int(err.item()))
 
+    def call(x):
+        sampler.sample_batch(x, params, out, err_word=err, workspace=wspace, stream=stream)
+
     chunk = min(args.steps, 480)
-
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    sampler.sample_batch(bufs[i % NBUF], params, out, err_word=err, workspace=wspace,
-                                         stream=stream)
-        return g
-
-    g_main = capture(chunk)
-    rem = args.steps % chunk
-    g_rem = capture(rem) if rem else None
-    reps = args.steps // chunk
+    graphs = [(graph_steps(sampler, stream, bufs, call, chunk), chunk)] * (args.steps // chunk)
+    if args.steps % chunk:
+        graphs.append((graph_steps(sampler, stream, bufs, call, args.steps % chunk), args.steps % chunk))
 
     def barrier():
         if ws > 1:
@@ -245,35 +386,27 @@ def bench_gpu(args) -> None:
         torch.cuda.synchronize()
 
     # warm-up: W untimed steps
-    with torch.cuda.stream(stream):
-        gw = capture(args.warmup) if args.warmup else None
-        if gw is not None:
-            gw.replay()
+    gw = graph_steps(sampler, stream, bufs, call, args.warmup)
+    gw.replay()
     stream.synchronize()
 
     vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     clocks = ClockSampler(int(vis[local]) if local < len(vis) and vis[local].isdigit() else local)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    repeats = max(1, args.repeats)
     barrier()
     clocks.start()
     time.sleep(0.05)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g_main.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        e1.record(stream)
+    ts = time_steps(stream, graphs, repeats)
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
     assert int(err.item()) == 0, hex(int(err.item()))
+    us = statistics.median(ts)
     if ws > 1:
-        t = torch.tensor([ms], device="cuda")
+        t = torch.tensor([us], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_per_step = ms / args.steps
-    value = ws * B * args.steps / (ms / 1e3)
+        us = float(t.item())
+    ms_per_step = us * 1e-3
+    value = ws * B / (us * 1e-6)
 
     # ---- end to end through the C ABI from pinned host buffers
     host_logits = bufs[0].cpu().pin_memory()
@@ -325,6 +458,9 @@ def bench_gpu(args) -> None:
                 "ctas_per_row": geom.ctas_per_row, "launch": "CUDA graph, one launch per step",
                 "parallelism": f"rows sharded, {ws} independent rank(s)",
             },
+            "timing": {"repeats": repeats, "steps_per_repeat": args.steps,
+                       "us_per_step_median": statistics.median(ts), "us_per_step_min": min(ts),
+                       "us_per_step_max": max(ts)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": profiled_traffic(),
                          "peak_source": peak_src, "alg_bytes_per_launch": alg_bytes,
@@ -335,9 +471,34 @@ def bench_gpu(args) -> None:
                     "h2d_bytes_per_step": int(host_logits.numel() * host_logits.element_size()
                                               + host_params.numel()),
                     "d2h_bytes_per_step": int(B * 4)},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": KERNELS_PER_STEP * args.steps * repeats,
             "clocks": clk,
         }
+        if ws == 1 and not args.no_configs:
+            # the design the library replaces: the whole logits tensor to pinned host memory per step
+            host = torch.empty(bufs[0].shape, dtype=bufs[0].dtype).pin_memory()
+            d2h = []
+            for i in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    host.copy_(bufs[i % NBUF], non_blocking=True)
+                    e1.record(stream)
+                stream.synchronize()
+                d2h.append(e0.elapsed_time(e1))
+            nbytes = B * V * es
+            line["d2h_context"] = {"bytes": nbytes, "ms_median": statistics.median(d2h), "ms_min": min(d2h),
+                                   "gbs": nbytes / (statistics.median(d2h) * 1e-3) / 1e9,
+                                   "what": "one D2H copy of the B=256 bf16 logits into pinned host memory"}
+            del bufs, wspace
+            torch.cuda.empty_cache()
+            cfg = {}
+            for nm in CONFIGS:
+                steps = 1000 if nm[0] == "single_row_peaked" else (40 if nm[0] in ("penalized_batch", "adversarial_ties")
+                                                                   else 400)
+                key, rec = bench_config(sampler, workloads, nm, peak, steps, 5)
+                cfg[key] = rec
+            line["configs"] = cfg
         if ws == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line))
@@ -422,6 +583,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' figures")
+    ap.add_argument("--repeats", type=int, default=5, help="timed regions of K steps (median and min reported)")
     ap.add_argument("--decode-loop", action="store_true", help="time the decode-loop commit (separate JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:

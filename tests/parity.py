@@ -6,8 +6,11 @@
     the cutoff lies within 1e-6 * S_K of top_p * S_K (the cutoff may then move
     to the neighbouring distinct weight);
   * sampled tokens: identical to the oracle's draw over the GPU's survivor
-    set, except where the oracle's normalised CDF at the token boundary lies
-    within 1e-6 of u.
+    set, except that a different survivor is accepted when the oracle's
+    normalised CDF interval of that survivor, [C(before it), C(through it)),
+    comes within 1e-6 of u -- every CDF boundary between it and the oracle's
+    token then lies within 1e-6 of u (for bulk ids of mass ~1e-8 that can be
+    several ids; for typical ids it is the neighbouring survivor).
 Exempt cases are counted and returned so a test can report them.
 """
 from __future__ import annotations
@@ -57,6 +60,18 @@ def _neighbour_cutoffs(res):
     vals = np.unique(res.w[res.K])[::-1]
     j = int(np.nonzero(vals == res.tau)[0][0])
     return [vals[jj] for jj in (j - 1, j + 1) if 0 <= jj < vals.size]
+
+
+def token_within(R: np.ndarray, run: np.ndarray, S: float, tok: int, u: float) -> bool:
+    """True when survivor `tok`'s normalised CDF interval [C(tok-), C(tok)) lies
+    within REL of u: C(tok-) <= u + REL and C(tok) > u - REL (run: the oracle's
+    running mass over R in id order, S its total).  The oracle's own token
+    satisfies it with REL = 0."""
+    if not R[tok]:
+        return False
+    hi = run[tok] / S
+    lo = (run[tok - 1] if tok > 0 else 0.0) / S
+    return lo <= u + REL and hi > u - REL
 
 
 def check_row(r: int, res: "oracle.RowResult", tok: int, d, top_p: float, min_p: float, V: int) -> Report:
@@ -124,13 +139,9 @@ def check_row(r: int, res: "oracle.RowResult", tok: int, d, top_p: float, min_p:
     tok_o, run, S = oracle.inverse_cdf(res.w, Rg, u)
     assert Rg[tok], f"row {r}: token {tok} is not a survivor"
     if tok != tok_o:
-        idx = np.nonzero(Rg)[0]
-        k = int(np.searchsorted(idx, tok_o))
-        bounds = [run[tok_o] / S]
-        if k > 0:
-            bounds.append(run[idx[k - 1]] / S)
-        if not any(abs(b - u) <= REL for b in bounds):
-            raise AssertionError(f"row {r}: token gpu={tok} oracle={tok_o} u={u} cdf={bounds}")
+        if not token_within(Rg, run, S, tok, u):
+            raise AssertionError(f"row {r}: token gpu={tok} oracle={tok_o} u={u}: the GPU token's CDF interval "
+                                 f"is farther than {REL} from u")
         rep.token_exempt += 1
     return rep
 
