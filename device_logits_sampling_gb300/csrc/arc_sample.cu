@@ -2,6 +2,9 @@
 // geometry, per-device kernel attributes and one launch per call.
 #include <algorithm>
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -22,6 +25,7 @@ constexpr int kDefaultHist = 1024;  // history capacity when max_hist_len is 0
 constexpr int kAssumedSMs = 152;
 
 struct Plan {
+    bool cluster = false;   // one cluster_kernel launch (a cluster of s CTAs per row)
     int s = 1;              // slices per row
     int L = 0;              // logits per slice
     int hist_cap = 0;
@@ -78,14 +82,31 @@ int check_options(const arc_sample_options* o) {
 
 // Geometry: a row is cut into s slices of at most kVpt * kThreads 16-byte
 // vectors (one scan CTA each); small batches use more, smaller slices so that
-// every SM gets work.
+// every SM gets work.  A batch whose rows fit in clusters of at most 16 CTAs,
+// all resident at once (two per SM), takes the one-launch cluster kernel when
+// `allow_cluster`; an explicit ctas_per_row always takes the two kernels.
+constexpr int kClusterMax = 16;
+
 int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_options* o, int num_sms,
-              Plan& p) {
+              Plan& p, bool allow_cluster = true) {
     const int es = elem_bytes(dtype);
     const int vec = 16 / es;
     const int64_t slice_max = int64_t{kVpt} * kThreads * vec;
     int64_t s;
-    if (o != nullptr && o->ctas_per_row != 0) {
+    const bool automatic = o == nullptr || o->ctas_per_row == 0;
+    bool cluster = false;
+    if (automatic && allow_cluster) {
+        const int64_t s_min = (V + slice_max - 1) / slice_max;
+        const int64_t s_cap = std::max<int64_t>(1, V / 1024);
+        const int64_t fs =
+            std::max<int64_t>(s_min, std::min<int64_t>({int64_t{kClusterMax}, s_cap, 2 * int64_t{num_sms} / B}));
+        if (fs <= kClusterMax && B * fs <= 2 * int64_t{num_sms}) {
+            cluster = true;
+            s = fs;
+        }
+    }
+    if (cluster) {
+    } else if (!automatic) {
         s = o->ctas_per_row;
     } else {
         const int64_t s_min = (V + slice_max - 1) / slice_max;
@@ -97,7 +118,7 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     if (s * slice_max < V || s > kMaxRowCtas) return ARC_E_UNSUPPORTED;
     const int64_t per = (V + s - 1) / s;
     const int64_t L = ((per + vec - 1) / vec) * vec;
-    s = (V + L - 1) / L;  // no empty slice
+    s = (V + L - 1) / L;  // no empty slice (fewer CTAs in the cluster when rounding frees one)
     const int cap = has_hist ? ((o != nullptr && o->max_hist_len > 0) ? o->max_hist_len : kDefaultHist) : 0;
     int64_t scan_smem = 0;
     if (has_hist) {
@@ -124,8 +145,13 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     const int64_t cmv_bytes = cmv_raw <= 16384 ? r128(cmv_raw) : 0;
     const int64_t fin_smem =
         cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch + cmv_bytes;
-    const int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
-    if (fin_smem > limit || scan_smem > limit) return ARC_E_UNSUPPORTED;
+    int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
+    if (cluster) limit -= kSummaryBytes + static_cast<int64_t>(sizeof(ScanShared));
+    if (fin_smem > limit || scan_smem > limit) {
+        if (cluster) return make_plan(B, V, dtype, has_hist, o, num_sms, p, false);
+        return ARC_E_UNSUPPORTED;
+    }
+    p.cluster = cluster;
     p.s = static_cast<int>(s);
     p.L = static_cast<int>(L);
     p.hist_cap = cap;
@@ -149,7 +175,7 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     p.fin_smem = static_cast<int>(fin_smem);
     p.slices = B * s;
     p.F = 62 - ceil_log2(V);
-    p.ws_bytes = static_cast<size_t>(B * s) * kSummaryBytes;
+    p.ws_bytes = cluster ? 0 : static_cast<size_t>(B * s) * kSummaryBytes;
     return ARC_OK;
 }
 
@@ -174,13 +200,19 @@ template <class K>
 cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done, int carveout) {
     const uint64_t bit = uint64_t{1} << (dev & 63);
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemPerBlock - static_cast<int>(sizeof(KernelShared)) - 1024);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
-    if (e != cudaSuccess) return e;
+    // the largest dynamic shared memory a CTA of this kernel can have next to
+    // its static shared memory
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemPerBlock - static_cast<int>(fa.sharedSizeBytes));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // a refused attribute must not surface as a later launch error
+        return e;
+    }
     done.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
 }
@@ -209,7 +241,37 @@ cudaError_t launch_cluster(K kernel, int64_t grid, int s, int smem, cudaStream_t
     return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
+// Whether a cluster launch of this kernel and shape fits the device (cached;
+// asked once per device, kernel, cluster size and shared-memory size).
+template <class K>
+bool cluster_fits(K kernel, int dev, int dt, bool hist, int s, int smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int>, bool> known;
+    const auto key = std::make_tuple(dev, dt, hist ? 1 : 0, s, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = known.find(key);
+    if (it != known.end()) return it->second;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(s), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n >= 1;
+    if (!ok) (void)cudaGetLastError();
+    known[key] = ok;
+    return ok;
+}
+
 std::atomic<uint64_t> g_prep_scan[2][2];
+std::atomic<uint64_t> g_prep_cluster[2][2];
 std::atomic<uint64_t> g_prep_fin[2][2];
 std::atomic<uint64_t> g_prep_argmax[2];
 
@@ -257,7 +319,7 @@ int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history, co
     geom->smem_bytes = p.fin_smem;
     geom->grid_ctas = p.slices;
     geom->frac_bits = p.F;
-    geom->reserved = 0;
+    geom->launches = p.cluster ? 1 : 2;
     geom->workspace_bytes = static_cast<int64_t>(p.ws_bytes);
     return ARC_OK;
 }
@@ -301,6 +363,25 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     Plan p;
     rc = make_plan(B, V, dtype, has_hist, opts, num_sms_of(dev), p);
     if (rc != ARC_OK) return rc;
+    if (p.cluster) {
+        // the one-launch cluster kernel, when the device can schedule its clusters
+        const int dyn = std::max(p.scan_smem, p.fin_smem);
+        bool fits;
+        if (dtype == ARC_BF16)
+            fits = has_hist ? prepare(cluster_kernel<ARC_BF16, true>, dev, g_prep_cluster[1][1], 100) == cudaSuccess &&
+                                  cluster_fits(cluster_kernel<ARC_BF16, true>, dev, 1, true, p.s, dyn)
+                            : prepare(cluster_kernel<ARC_BF16, false>, dev, g_prep_cluster[1][0], 100) == cudaSuccess &&
+                                  cluster_fits(cluster_kernel<ARC_BF16, false>, dev, 1, false, p.s, dyn);
+        else
+            fits = has_hist ? prepare(cluster_kernel<ARC_F32, true>, dev, g_prep_cluster[0][1], 100) == cudaSuccess &&
+                                  cluster_fits(cluster_kernel<ARC_F32, true>, dev, 0, true, p.s, dyn)
+                            : prepare(cluster_kernel<ARC_F32, false>, dev, g_prep_cluster[0][0], 100) == cudaSuccess &&
+                                  cluster_fits(cluster_kernel<ARC_F32, false>, dev, 0, false, p.s, dyn);
+        if (!fits) {
+            rc = make_plan(B, V, dtype, has_hist, opts, num_sms_of(dev), p, false);
+            if (rc != ARC_OK) return rc;
+        }
+    }
     if (workspace_bytes < p.ws_bytes) return ARC_E_WORKSPACE;
 
     const int es = elem_bytes(dtype);
@@ -350,6 +431,18 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.fb_rounds = p.fb_rounds;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (p.cluster) {
+        const FusedArgs fu{sa, fa};
+        const int dyn = std::max(p.scan_smem, p.fin_smem);
+        cudaError_t e;
+        if (dtype == ARC_BF16)
+            e = has_hist ? launch_cluster(cluster_kernel<ARC_BF16, true>, B * p.s, p.s, dyn, st, fu)
+                         : launch_cluster(cluster_kernel<ARC_BF16, false>, B * p.s, p.s, dyn, st, fu);
+        else
+            e = has_hist ? launch_cluster(cluster_kernel<ARC_F32, true>, B * p.s, p.s, dyn, st, fu)
+                         : launch_cluster(cluster_kernel<ARC_F32, false>, B * p.s, p.s, dyn, st, fu);
+        return e == cudaSuccess ? ARC_OK : ARC_E_CUDA;
+    }
     auto go = [&](auto scan, auto fin, std::atomic<uint64_t>& done_s, std::atomic<uint64_t>& done_f) {
         cudaError_t err = prepare(scan, dev, done_s, has_hist ? 100 : 0);
         if (err == cudaSuccess) err = prepare(fin, dev, done_f, 100);

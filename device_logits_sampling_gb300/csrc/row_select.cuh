@@ -211,7 +211,10 @@ struct RowCtx {
 
     // ---------------------------------------------------------------- cluster exchange
     __device__ __forceinline__ void xsync() {
-        cl.sync();
+        if (s == 1)
+            __syncthreads();  // one CTA: every exchange stays in its own shared memory
+        else
+            cl.sync();
         epoch++;
     }
     __device__ __forceinline__ uint64_t xread(int r, int i) const {

@@ -437,7 +437,8 @@ __device__ __forceinline__ float warp_sum4(const float (&v)[4], int lane) {
 // as -inf): penalties, chunk table, per-warp records.
 template <int DT, bool HIST>
 __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[kVpt], int row, int cidx,
-                                           const ScanRowInfo& R, ScanShared& sh, unsigned char* patch_mem) {
+                                           const ScanRowInfo& R, ScanShared& sh, unsigned char* patch_mem,
+                                           unsigned char* mysum) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     static_assert(kVpt == 4, "warp_sum4 pairs the four vectors of a thread with lanes 0, 8, 16, 24");
@@ -516,7 +517,6 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
     }
     const bool wnan = __any_sync(0xFFFFFFFFu, vn != 0);
 
-    unsigned char* mysum = const_cast<unsigned char*>(summary_at(a.summaries, a.s, row, cidx));
     float wm = -INFINITY;
     int wam = -1;
     if (bits & kRowChunks) {
@@ -633,25 +633,18 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
     }
 }
 
-// One CTA per slice (grid: slices x rows, rows past 65,535 folded into z):
-// the row's parameter words and every 16-byte load of the slice are issued
-// first (they depend on nothing); the warps share nothing and meet at no
-// barrier (rows with history excepted), and registers stay few so that many
-// CTAs per SM keep enough bytes in flight.
+// One slice of one row: the row's parameter words and every 16-byte load of
+// the slice are issued first (they depend on nothing); the warps share
+// nothing and meet at no barrier (rows with history excepted), and registers
+// stay few so that many CTAs per SM keep enough bytes in flight.  The summary
+// goes to `mysum` (the workspace, or this CTA's shared memory in the cluster
+// kernel).
 template <int DT, bool HIST>
-__global__ void __launch_bounds__(kThreads, HIST ? 4 : 8) scan_kernel(const ScanArgs a) {
+__device__ __forceinline__ void scan_cta(const ScanArgs& a, int row, int cidx, ScanShared& sh, unsigned char* dyn,
+                                         unsigned char* mysum) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
-    extern __shared__ __align__(128) unsigned char dyn[];
-    __shared__ ScanShared sh;
-    // the finish kernel may be scheduled once every scan CTA is running; it
-    // waits (griddepcontrol.wait) for this grid to complete before reading
-    // the summaries
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
-    const int row = static_cast<int>(blockIdx.z * gridDim.y + blockIdx.y);
-    if (row >= a.B) return;  // the whole CTA, before any barrier
-    const int cidx = static_cast<int>(blockIdx.x);
     const int a0 = cidx * a.L;
     const int n = min(a0 + a.L, a.V) - a0;
     const int nv = (n + VEC - 1) / VEC;
@@ -671,7 +664,23 @@ __global__ void __launch_bounds__(kThreads, HIST ? 4 : 8) scan_kernel(const Scan
             d[j] = (v < nv) ? E::global_vec(sp, v, n, a.aligned) : ninf;
     }
     const ScanRowInfo R = scan_row_info<HIST>(a, row, pw);
-    scan_slice<DT, HIST>(a, d, row, cidx, R, sh, dyn);
+    scan_slice<DT, HIST>(a, d, row, cidx, R, sh, dyn, mysum);
+}
+
+// One CTA per slice (grid: slices x rows, rows past 65,535 folded into z).
+template <int DT, bool HIST>
+__global__ void __launch_bounds__(kThreads, HIST ? 4 : 8) scan_kernel(const ScanArgs a) {
+    extern __shared__ __align__(128) unsigned char dyn[];
+    __shared__ ScanShared sh;
+    // the finish kernel may be scheduled once every scan CTA is running; it
+    // waits (griddepcontrol.wait) for this grid to complete before reading
+    // the summaries
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int row = static_cast<int>(blockIdx.z * gridDim.y + blockIdx.y);
+    if (row >= a.B) return;  // the whole CTA, before any barrier
+    const int cidx = static_cast<int>(blockIdx.x);
+    scan_cta<DT, HIST>(a, row, cidx, sh, dyn,
+                       const_cast<unsigned char*>(summary_at(a.summaries, a.s, row, cidx)));
 }
 
 // ------------------------------------------------------------------ finish helpers
@@ -973,17 +982,19 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     st.err = err;
 }
 
-// One CTA per row.
-template <int DT, bool HIST>
-__global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_constant__ FinishArgs a) {
+// One row's finish by one CTA.  sum_at(c) is slice c's summary (the
+// workspace, or another CTA's shared memory in the cluster kernel); wait()
+// returns once every summary of the row is complete and visible; loaded()
+// runs after the summaries have been copied on chip (every thread of the CTA
+// calls both).
+template <int DT, bool HIST, class SumAt, class Wait, class Loaded>
+__device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelShared& KS, unsigned char* dyn,
+                                           SumAt sum_at, Wait wait, Loaded loaded) {
     using E = Elem<DT>;
     using Ctx = RowCtx<DT, HIST>;
     constexpr int VEC = E::kVec;
-    extern __shared__ __align__(128) unsigned char dyn[];
-    __shared__ KernelShared KS;
     FinishScratch& SS = KS.st;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = blockIdx.x;
     const int s = a.s;
     const int nch = s * kChunks;
     const char* rowp = static_cast<const char*>(a.logits) + static_cast<int64_t>(row) * a.ld * E::kBytes;
@@ -1010,10 +1021,9 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
         tl = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
     // the finish needs the chunk max vectors (filtered rows)
     const bool want_mv = a.cmv_off >= 0 && param_errors(P) == 0 && RowMode(P, a.V).filtered;
-    // launched early behind the scan kernel: its summaries are complete and
-    // visible after this (the parameters and history above are not written by
-    // the scan)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the summaries are complete and visible after this (the parameters and
+    // history above are not written by the scan)
+    wait();
 
     // the warp records (warp 0) and the chunk tables (warps 1-7) load while
     // the parameters do: nothing here waits for them
@@ -1023,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
         uint32_t f = 0;
         const int nrec = s * kWarps;
         auto rec = [&](int q) {
-            return reinterpret_cast<const WarpRecord*>(summary_at(a.summaries, s, row, q / kWarps))[q % kWarps];
+            return reinterpret_cast<const WarpRecord*>(sum_at(q / kWarps))[q % kWarps];
         };
         constexpr int kLdR = 4;  // records in flight per lane
         WarpRecord r[kLdR];
@@ -1061,7 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
             for (int u = 0; u < kLd; ++u) {
                 const int gi = g0 + u * kStride;
                 if (gi < nch) {
-                    const unsigned char* sm = summary_at(a.summaries, s, row, gi / kChunks);
+                    const unsigned char* sm = sum_at(gi / kChunks);
                     e[u] = chunk_table(sm)[gi % kChunks];
                     if (want_mv) mv[u] = max_vectors(sm)[gi % kChunks];
                 }
@@ -1088,6 +1098,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
     const float T = P.temperature;
     const int k = P.top_k;
     __syncthreads();
+    loaded();
 
     RowState st;
     st.m = SS.bf[0];
@@ -1648,6 +1659,51 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
         }
         if (a.flags & ARC_OPT_STEP_AUTOINC) a.params[row].step = P.step + 1;
     }
+}
+
+// One CTA per row, launched behind scan_kernel (programmatic dependent launch).
+template <int DT, bool HIST>
+__global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_constant__ FinishArgs a) {
+    extern __shared__ __align__(128) unsigned char dyn[];
+    __shared__ KernelShared KS;
+    const int row = blockIdx.x;
+    finish_row<DT, HIST>(
+        a, row, KS, dyn, [&](int c) { return summary_at(a.summaries, a.s, row, c); },
+        [] { asm volatile("griddepcontrol.wait;" ::: "memory"); }, [] {});
+}
+
+struct FusedArgs {
+    ScanArgs scan;
+    FinishArgs fin;
+};
+
+// Small batches in one launch: a thread-block cluster of s CTAs per row
+// (s <= 16).  Every CTA scans its slice into its own shared memory; after a
+// cluster barrier (release / acquire at cluster scope) CTA 0 of the cluster
+// reads the s summaries through distributed shared memory and finishes the
+// row, while the others wait at a second cluster barrier until those reads
+// are done, then exit.  No workspace, no second launch, no global round trip
+// for the summaries.
+template <int DT, bool HIST>
+__global__ void __launch_bounds__(kThreads, 2) cluster_kernel(const __grid_constant__ FusedArgs f) {
+    extern __shared__ __align__(128) unsigned char dyn[];
+    __shared__ KernelShared KS;
+    __shared__ ScanShared sh;
+    __shared__ __align__(16) unsigned char mysum[kSummaryBytes];
+    cg::cluster_group cl = cg::this_cluster();
+    const int s = static_cast<int>(cl.num_blocks());
+    const int rank = static_cast<int>(cl.block_rank());
+    const int row = static_cast<int>(blockIdx.x) / s;
+    scan_cta<DT, HIST>(f.scan, row, rank, sh, dyn, mysum);
+    if (rank != 0) {
+        cl.sync();  // the summaries are complete
+        cl.sync();  // CTA 0 has copied them
+        return;
+    }
+    // (the scan's shared memory is dead here: the finish reuses dyn)
+    finish_row<DT, HIST>(
+        f.fin, row, KS, dyn, [&](int c) { return static_cast<const unsigned char*>(cl.map_shared_rank(mysum, c)); },
+        [&] { cl.sync(); }, [&] { cl.sync(); });
 }
 
 }  // namespace arc

@@ -70,7 +70,7 @@ class Geometry(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("grid_ctas", ctypes.c_int64),
         ("frac_bits", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("launches", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
     ]
 

@@ -216,8 +216,10 @@ typedef struct arc_sample_geometry {
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int64_t grid_ctas;       /* total CTAs */
     int32_t frac_bits;       /* fixed-point fraction bits of the masses */
-    int32_t reserved;
-    int64_t workspace_bytes; /* workspace this geometry uses */
+    int32_t launches;        /* 1: one cluster kernel (a thread-block cluster of
+                                ctas_per_row CTAs per row, summaries combined in
+                                distributed shared memory); 2: scan + finish */
+    int64_t workspace_bytes; /* workspace this geometry uses (0 with one launch) */
 } arc_sample_geometry;
 
 int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history,

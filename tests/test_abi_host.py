@@ -115,13 +115,24 @@ def test_plan_geometry(lib):
     g = sampler.plan(256, workloads.VOCAB_V4, workloads.DTYPE_BF16)
     assert (g.ctas_per_row, g.slice_elems, g.grid_ctas, g.threads) == (16, 8080, 4096, 256)
     assert g.frac_bits == 62 - 17
-    # a single row is spread over many CTAs (latency), each with >= 1024 logits
+    assert g.launches == 2 and g.workspace_bytes == 256 * 16 * 1152
+    # a single row: one launch, a cluster of 16 CTAs sharing the row (their
+    # summaries combined in distributed shared memory, no workspace)
     g1 = sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16)
-    assert g1.ctas_per_row >= 32 and g1.slice_elems >= 1024
+    assert (g1.launches, g1.ctas_per_row, g1.grid_ctas, g1.workspace_bytes) == (1, 16, 16, 0)
+    # up to 19 such rows fit the GPU at once (16 CTAs each, two per SM); 20 take two launches
+    assert sampler.plan(19, workloads.VOCAB_V4, workloads.DTYPE_BF16).launches == 1
+    g20 = sampler.plan(20, workloads.VOCAB_V4, workloads.DTYPE_BF16)
+    assert g20.launches == 2 and g20.ctas_per_row >= 16
+    # an explicit slice count always takes the two kernels
+    assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16, ctas_per_row=32).launches == 2
+    # fp32 rows of 129,280 need 32 slices: more than a cluster holds
+    assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_F32).launches == 2
     # fp32 slices hold half as many logits
     assert sampler.plan(64, workloads.VOCAB_V4, workloads.DTYPE_F32).ctas_per_row == 32
-    # small vocabularies stay on one CTA
-    assert sampler.plan(4, 1024, workloads.DTYPE_F32).ctas_per_row == 1
+    # small vocabularies stay on one CTA (which scans and finishes its row)
+    g4 = sampler.plan(4, 1024, workloads.DTYPE_F32)
+    assert (g4.ctas_per_row, g4.launches) == (1, 1)
     # a forced geometry too small for the row is refused
     with pytest.raises(sampler.ArcError) as e:
         sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16, ctas_per_row=1)
@@ -138,7 +149,10 @@ def test_plan_geometry(lib):
     # the workspace covers every automatic geometry
     for B, V, dt in [(256, workloads.VOCAB_V4, 1), (1, workloads.VOCAB_V4, 1), (64, workloads.VOCAB_V4, 0)]:
         ws = sampler.workspace_bytes(B, V, dt)
-        assert ws >= sampler.plan(B, V, dt).workspace_bytes > 0
+        assert ws >= sampler.plan(B, V, dt).workspace_bytes and ws > 0
+        # and the two-kernel geometry the library falls back to when a device
+        # cannot schedule the cluster
+        assert ws >= sampler.plan(B, V, dt, ctas_per_row=sampler.plan(B, V, dt).ctas_per_row).workspace_bytes
     assert sampler.workspace_bytes(0, 10, 1) == 0
 
 

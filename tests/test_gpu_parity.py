@@ -360,3 +360,24 @@ def test_graph_replay_reads_step_from_device(cuda_lib):
     want = [oracle.draw_bits(5, 0, s) >> (53 - 12) for s in range(64)]  # uniform over 4096
     assert got == want
     assert len(set(got)) > 60
+
+
+@pytest.mark.parametrize("B,V,dtype,hist_len", [(1, 129_280, 1, 0), (4, 1024, 0, 0), (12, 30_011, 1, 64),
+                                                 (19, 129_280, 1, 0), (3, 131_072, 1, 0), (7, 4097, 0, 0)])
+def test_cluster_path_matches_two_kernels(cuda_lib, B, V, dtype, hist_len):
+    """Small batches take one launch: a cluster of CTAs per row, their slice
+    summaries combined through distributed shared memory.  With the same slices
+    the two-kernel path (scan, workspace, finish) gives the same tokens and the
+    same debug records, bit for bit; both match the oracle."""
+    S = cuda_lib
+    w = wl.random_case(seed=900 + B + V, B=B, V=V, dtype=dtype, ties=(V % 2 == 1), hist_len=hist_len)
+    g = S.plan(B, V, dtype, has_history=hist_len > 0, max_hist_len=hist_len)
+    assert g.launches == 1
+    t1, d1, e1 = run(S, w, max_hist_len=hist_len)
+    t2, d2, e2 = run(S, w, max_hist_len=hist_len, ctas_per_row=g.ctas_per_row)
+    assert S.plan(B, V, dtype, has_history=hist_len > 0, max_hist_len=hist_len,
+                  ctas_per_row=g.ctas_per_row).launches == 2
+    assert np.array_equal(t1, t2) and e1 == e2
+    assert np.array_equal(d1, d2)
+    rep = parity.check_batch(w, t1, d1)
+    assert rep.rows == B
