@@ -8,6 +8,6 @@ from .sampler import (  # noqa: F401
     MODE_FILTERED, MODE_GREEDY, MODE_INERT, MODE_INVALID,
     RowResult, apply_penalties, draw_bits, draw_many, inverse_cdf, params_valid,
     row_mode, sample_batch, sample_row, sample_row_u, splitmix64, top_k_mask,
-    top_p_cutoff, uniform,
+    top_logprobs, top_p_cutoff, uniform,
 )
 from . import decode_commit  # noqa: F401,E402

@@ -263,6 +263,49 @@ def sample_batch(logits_f32: np.ndarray, params: np.ndarray,
     return out
 
 
+def top_logprobs(z: np.ndarray, temperature: float, n: int) -> tuple[np.ndarray, np.ndarray]:
+    """The n most likely ids of a row and their log-probabilities.
+
+    Arc PR #222, section 3(b), names the top-n log-probability output as a
+    reader of the sampler's sort; the pages give no formula.  The reading here:
+      * order: (z desc, id asc) over the penalised logits z -- the order of the
+        top-k filter (temperature does not change it);
+      * value: log-softmax over every id at the row's sampling temperature,
+        before the top-k / top-p / min-p filters:
+            lp_i = (z_i - m) / T - ln(sum_j exp((z_j - m) / T)),  m = max z,
+        in fp64, with T = 1 for a greedy row (T == 0);
+      * -inf logits have lp = -inf; when the max is +inf, the +inf entries
+        share the mass (lp = -ln(count)) and the rest are -inf; a row with no
+        finite or +inf logit lists ids in ascending order with lp = -inf;
+      * n > V: the entries past V are (id -1, lp -inf).
+    Returns (ids int64[n], lp float64[n]).
+    """
+    z = np.asarray(z, dtype=np.float32)
+    V = int(z.size)
+    T = float(np.float32(temperature))
+    if not T > 0.0:
+        T = 1.0
+    zd = z.astype(np.float64)
+    order = np.lexsort((np.arange(V), -zd))
+    ids = np.full(n, -1, dtype=np.int64)
+    lp = np.full(n, -math.inf)
+    take = order[:min(n, V)]
+    ids[:take.size] = take
+    m = float(zd.max())
+    if m == -math.inf:
+        return ids, lp
+    if m == math.inf:
+        top = zd == math.inf
+        lse = math.log(float(top.sum()))
+        vals = np.where(top, -lse, -math.inf)
+    else:
+        with np.errstate(under="ignore"):
+            lse = math.log(float(np.sum(np.exp((zd - m) / T))))
+            vals = (zd - m) / T - lse
+    lp[:take.size] = vals[take]
+    return ids, lp
+
+
 def draw_many(w: np.ndarray, R: np.ndarray, u: np.ndarray) -> np.ndarray:
     """Inverse-CDF tokens for many uniforms over one fixed (w, R) (distribution tests)."""
     run = np.cumsum(np.where(R, w, 0.0))

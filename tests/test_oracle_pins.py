@@ -336,3 +336,72 @@ def test_mixed_workload_rows_use_the_stated_quarters():
     res = oracle.sample_batch(w.logits_f32(), w.params)
     for r in range(0, 8, 4):
         assert res[r].token == int(np.argmax(w.logits_f32()[r]))
+
+
+# ---------------------------------------------------------------- top-n log-probabilities
+def _brute_top_logprobs(z, T, n):
+    """Explicit sort of (id, value) pairs and probabilities summed with math.fsum."""
+    T = float(np.float32(T)) if float(np.float32(T)) > 0 else 1.0
+    pairs = sorted(range(len(z)), key=lambda i: (-float(z[i]), i))
+    m = max(float(v) for v in z)
+    e = [math.exp((float(v) - m) / T) if v != -math.inf else 0.0 for v in z]
+    tot = math.fsum(e)
+    out = []
+    for i in pairs[:n]:
+        out.append((i, math.log(e[i] / tot) if e[i] > 0 else -math.inf))
+    return out
+
+
+@pytest.mark.parametrize("ties", [False, True])
+def test_top_logprobs_brute_force_tiny(ties):
+    rng = np.random.default_rng(123 + ties)
+    for _ in range(200):
+        V = int(rng.integers(1, 13))
+        z = (rng.integers(-3, 4, size=V) if ties else rng.standard_normal(V) * 2).astype(np.float32)
+        if V > 2 and rng.random() < 0.2:
+            z[int(rng.integers(0, V))] = -np.inf
+        if not np.isfinite(z).any():
+            continue
+        T = float(rng.choice([0.0, 0.5, 1.0, 1.7]))
+        n = int(rng.integers(1, V + 3))
+        ids, lp = oracle.top_logprobs(z, T, n)
+        want = _brute_top_logprobs(z, T, n)
+        assert ids[:len(want)].tolist() == [i for i, _ in want]
+        for (i, v), g in zip(want, lp):
+            assert (v == -math.inf and g == -math.inf) or abs(g - v) <= 1e-12 * max(1.0, abs(v)), (v, g)
+        assert (ids[len(want):] == -1).all() and (lp[len(want):] == -math.inf).all()
+
+
+def test_top_logprobs_closed_forms():
+    # a flat row: every id has probability 1/V, listed in id order
+    ids, lp = oracle.top_logprobs(np.zeros(1000, dtype=np.float32), 0.7, 5)
+    assert ids.tolist() == [0, 1, 2, 3, 4] and np.allclose(lp, -math.log(1000), rtol=0, atol=1e-12)
+    # two levels: k ids at a, V - k at b
+    V, k, a, b = 500, 3, 2.0, -1.0
+    T = float(np.float32(0.8))  # the row parameter is an fp32 value
+    z = np.full(V, b, dtype=np.float32)
+    z[[7, 100, 42]] = a
+    ids, lp = oracle.top_logprobs(z, T, 5)
+    top = -math.log(k + (V - k) * math.exp((b - a) / T))
+    assert ids.tolist() == [7, 42, 100, 0, 1]
+    assert np.allclose(lp[:3], top, rtol=0, atol=1e-12)
+    assert np.allclose(lp[3:], (b - a) / T + top, rtol=0, atol=1e-12)
+    # a greedy row (T = 0) reports the distribution at T = 1
+    z = np.random.default_rng(3).standard_normal(64).astype(np.float32)
+    assert np.array_equal(oracle.top_logprobs(z, 0.0, 8)[1], oracle.top_logprobs(z, 1.0, 8)[1])
+    # +inf entries share all the mass
+    z[[5, 9]] = np.inf
+    ids, lp = oracle.top_logprobs(z, 1.0, 3)
+    assert ids[:2].tolist() == [5, 9] and np.allclose(lp[:2], -math.log(2)) and lp[2] == -math.inf
+
+
+def test_top_logprobs_are_a_distribution_in_sorted_order():
+    rng = np.random.default_rng(9)
+    z = (rng.standard_normal(3000) * 3).astype(np.float32)
+    ids, lp = oracle.top_logprobs(z, 0.9, 3000)
+    assert sorted(ids.tolist()) == list(range(3000))
+    assert np.all(np.diff(lp) <= 0)
+    assert abs(math.fsum(np.exp(lp)) - 1.0) <= 1e-12
+    # the ids are the top-k filter's set for every k
+    for k in (1, 17, 500):
+        assert set(ids[:k].tolist()) == set(np.nonzero(oracle.top_k_mask(z, k))[0].tolist())
