@@ -76,7 +76,8 @@ int check_options(const arc_sample_options* o) {
     if (o->flags & ~(ARC_OPT_STEP_AUTOINC | ARC_OPT_FORCE_BISECTION)) return ARC_E_OPTION;
     if (o->ctas_per_row < 0 || o->ctas_per_row > kMaxRowCtas) return ARC_E_OPTION;
     if (o->max_hist_len < 0 || o->max_hist_len > (1 << 20)) return ARC_E_OPTION;
-    if (o->reserved != 0) return ARC_E_OPTION;
+    if (o->top_n < 0 || o->top_n > ARC_MAX_TOP_N) return ARC_E_OPTION;
+    if (o->top_n > 0 && o->top_logprobs == nullptr) return ARC_E_OPTION;
     return ARC_OK;
 }
 
@@ -399,6 +400,7 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     sa.summaries = static_cast<unsigned char*>(workspace);
     sa.hist_cap = p.hist_cap;
     sa.aligned = aligned;
+    sa.top_n = opts ? opts->top_n : 0;
     FinishArgs fa;
     fa.logits = logits;
     fa.ld = ld;
@@ -412,6 +414,8 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.out = out;
     fa.err_word = err_word;
     fa.debug = opts ? opts->debug : nullptr;
+    fa.top_n = opts ? opts->top_n : 0;
+    fa.top_logprobs = (opts && opts->top_n > 0) ? opts->top_logprobs : nullptr;
     fa.summaries = static_cast<const unsigned char*>(workspace);
     fa.hist_cap = p.hist_cap;
     fa.F = p.F;

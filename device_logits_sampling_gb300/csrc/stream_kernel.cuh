@@ -54,6 +54,7 @@ struct ScanArgs {
     unsigned char* summaries;  // [B * s] x kSummaryBytes
     int hist_cap;
     int aligned;    // rows start on 16-byte boundaries: 16-byte loads
+    int top_n;      // > 0: every row records chunk masses, maxima and max vectors
 };
 
 struct FinishArgs {
@@ -69,6 +70,8 @@ struct FinishArgs {
     int32_t* out;
     uint32_t* err_word;
     arc_row_debug* debug;
+    int top_n;                       // > 0: write the row's top-n log-probabilities
+    arc_top_logprob* top_logprobs;   //   [B][top_n]
     const unsigned char* summaries;
     int hist_cap;
     int F;
@@ -360,7 +363,11 @@ __device__ __forceinline__ ScanRowInfo scan_row_info(const ScanArgs& a, int row,
         R.bits = kRowChunks | (md.need_mass ? kRowMass : 0u) | (md.filtered ? kRowFiltered : 0u);
         if (HIST) R.bits |= kRowArgmax;  // penalised rows keep their first max id
     }
-    R.cT = (R.bits & kRowMass) ? __fdiv_rn(1.4426950408889634f, R.P.temperature) : 0.0f;
+    // top-n log-probabilities: the masses at the row's temperature (1 for a
+    // greedy row) and the chunk maxima and max vectors of every row
+    if (a.top_n > 0 && R.rerr == 0) R.bits |= kRowChunks | kRowMass | kRowFiltered;
+    const float Tm = R.P.temperature > 0.0f ? R.P.temperature : 1.0f;
+    R.cT = (R.bits & kRowMass) ? __fdiv_rn(1.4426950408889634f, Tm) : 0.0f;
     return R;
 }
 
@@ -844,6 +851,48 @@ struct RowState {
     int token, passes;
 };
 
+// The selection context of one row held by one CTA, read from global memory.
+template <int DT, bool HIST>
+__device__ __forceinline__ void setup_row_ctx(RowCtx<DT, HIST>& X, const FinishArgs& a, int row, const char* rowp,
+                                              float* cm, const uint32_t* pbm, const uint32_t* pwp, const float* ppat,
+                                              bool has_patch, bool row_nan, float m, float c, float scale, bool infm,
+                                              unsigned char* dyn) {
+    constexpr int VEC = Elem<DT>::kVec;
+    X.s = 1;
+    X.rank = 0;
+    X.row = row;
+    X.tid = threadIdx.x;
+    X.lane = threadIdx.x & 31;
+    X.warp = threadIdx.x >> 5;
+    X.a0 = 0;
+    X.a1 = a.V;
+    X.n = a.V;
+    X.nv = (a.V + VEC - 1) / VEC;
+    X.nvf = a.V / VEC;
+    X.rounds = (X.nv + kThreads - 1) / kThreads;
+    X.data = reinterpret_cast<const unsigned char*>(rowp);
+    X.src_global = true;
+    X.src_aligned = a.aligned != 0;
+    X.vmax = cm;
+    X.vps = a.L / VEC;
+    X.cps = kChunks;
+    X.Wsum = reinterpret_cast<uint64_t*>(dyn + a.fb_wsum_off);
+    X.par = 0;
+    X.passes = 0;
+    X.epoch = 1;
+    X.ghist_zeroed = -1;
+    X.cand_zeroed = -1;
+    X.has_patch = has_patch;
+    X.row_nan = row_nan;
+    X.bm = pbm;
+    X.wp = pwp;
+    X.patch = ppat;
+    X.m = m;
+    X.c = c;
+    X.scale = scale;
+    X.infm = infm;
+}
+
 // Exact selection over the row in global memory by multi-way threshold
 // bisection (row_select.cuh), skipping every 32-vector chunk whose max lies
 // below a pass's threshold: the path for rows whose floor admits too many
@@ -864,39 +913,8 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     __syncthreads();
     cg::cluster_group cl = cg::this_cluster();
     Ctx X(KS.fb, cl);
-    X.s = 1;
-    X.rank = 0;
-    X.row = row;
-    X.tid = tid;
-    X.lane = lane;
-    X.warp = warp;
-    X.a0 = 0;
-    X.a1 = a.V;
-    X.n = a.V;
-    X.nv = (a.V + VEC - 1) / VEC;
-    X.nvf = a.V / VEC;
-    X.rounds = (X.nv + kThreads - 1) / kThreads;
-    X.data = reinterpret_cast<const unsigned char*>(rowp);
-    X.src_global = true;
-    X.src_aligned = a.aligned != 0;
-    X.vmax = cm;
-    X.vps = a.L / VEC;
-    X.cps = kChunks;
-    X.Wsum = reinterpret_cast<uint64_t*>(dyn + a.fb_wsum_off);
-    X.par = 0;
-    X.passes = 0;
-    X.epoch = 1;
-    X.ghist_zeroed = -1;
-    X.cand_zeroed = -1;
-    X.has_patch = has_patch;
-    X.row_nan = st.row_nan;
-    X.bm = pbm;
-    X.wp = pwp;
-    X.patch = ppat;
-    X.m = m;
-    X.c = st.cT;
-    X.scale = st.scale;
-    X.infm = st.infm;
+    setup_row_ctx<DT, HIST>(X, a, row, rowp, cm, pbm, pwp, ppat, has_patch, st.row_nan, m, st.cT, st.scale, st.infm,
+                            dyn);
     for (int b = tid; b < kBins; b += kThreads) KS.fb.ghist[b] = 0;
     if (tid == 0) {
         KS.fb.ccount = 0;
@@ -982,6 +1000,180 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     st.err = err;
 }
 
+// Top-n log-probabilities of one row (a.top_n > 0), after its token: the n
+// ids first in (z desc, id asc) order of the penalised logits and their
+// log-softmax at the row's temperature (1 for a greedy row).  The ids come
+// from the direct selection's floor (the n-th largest chunk max) and gather;
+// a row whose floor admits more ids than the selection holds takes the exact
+// top-k bisection with k = n.  ln(S) is the fp64 log of the chunk tables'
+// fixed-point total at the same temperature.
+template <int DT, bool HIST>
+__device__ __noinline__ void top_n_row(const FinishArgs& a, int row, const arc_row_params& P, bool valid,
+                                      const char* rowp, float m, bool row_nan, float cT, float scale, bool want_mv,
+                                      int hbeg, int hn, KernelShared& KS, unsigned char* dyn) {
+    using E = Elem<DT>;
+    using Ctx = RowCtx<DT, HIST>;
+    constexpr int VEC = E::kVec;
+    FinishScratch& SS = KS.st;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = a.top_n;
+    arc_top_logprob* out = a.top_logprobs + static_cast<size_t>(row) * n;
+    const int nch = a.s * kChunks;
+    float* cm = reinterpret_cast<float*>(dyn + a.cmax_off);
+    const float* cs = reinterpret_cast<const float*>(dyn + a.cs_off);
+    const int* cln = reinterpret_cast<const int*>(dyn + a.cid_off);
+    const float* cu2 = reinterpret_cast<const float*>(dyn + a.cv2_off);
+    const uint4* cmv = reinterpret_cast<const uint4*>(dyn + a.cmv_off);
+    __syncthreads();  // the row's selection is done with the shared scratch
+    if (!valid || !(m > -INFINITY)) {
+        // invalid parameters: (-1, -inf); no finite or +inf logit: every id
+        // ties at -inf, listed in id order
+        for (int j = tid; j < n; j += kThreads) out[j] = arc_top_logprob{(valid && j < a.V) ? j : -1, -INFINITY};
+        return;
+    }
+    const bool infm = m == INFINITY;
+    const float Tm = P.temperature > 0.0f ? P.temperature : 1.0f;
+    // the total mass: chunk masses rescaled to the row max, in units of 2^-F
+    {
+        const int cper = (nch + kThreads - 1) / kThreads;
+        uint64_t loc = 0;
+        for (int e = tid * cper; e < min(nch, tid * cper + cper); ++e) {
+            const float mj = cm[e], Sj = cs[e];
+            if (mj != -INFINITY && Sj != 0.0f) loc += __float2ull_rn(__fmul_rn(__fmul_rn(Sj, wrel(mj, m, cT)), scale));
+        }
+        const uint64_t tot = block_sum_u64(loc, SS.redu);
+        if (tid == 0) SS.bd[0] = log(static_cast<double>(tot)) - static_cast<double>(a.F) * 0.69314718055994530942;
+    }
+    // history patches of the whole row
+    const uint32_t* pbm = nullptr;
+    const uint32_t* pwp = nullptr;
+    const float* ppat = nullptr;
+    bool has_patch = false;
+    if (HIST && hn > 0) {
+        const int nwords_max = (a.fb_rounds * kThreads * VEC + 31) / 32;
+        uint32_t* bm = reinterpret_cast<uint32_t*>(dyn + a.fb_patch_off);
+        uint32_t* wp = bm + nwords_max;
+        uint32_t* cnt = wp + nwords_max;
+        float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
+        __syncthreads();
+        if (tid == 0) SS.bi[7] = 0;
+        const int distinct = build_patches<DT>(rowp, a.V, 0, a.V, (a.V + VEC - 1) / VEC, P, a.hist_ids + hbeg, hn, bm,
+                                               wp, cnt, pat, SS.red32, reinterpret_cast<uint32_t*>(&SS.bi[7]));
+        pbm = bm;
+        pwp = wp;
+        ppat = pat;
+        has_patch = distinct > 0;
+    }
+    uint64_t* cc = reinterpret_cast<uint64_t*>(dyn + a.cand_off);
+    for (int b = tid; b < kFloorHistWords; b += kThreads) reinterpret_cast<uint32_t*>(KS.fb.lhist)[b] = 0u;
+    if (tid == 0) SS.ccount = 0;
+    __syncthreads();
+    // floor: the n-th largest chunk max (every chunk max is an id at or above it)
+    float zf = -INFINITY;
+    bool fast = false;
+    if (!infm) {
+        auto wt = [&](float x) -> uint32_t { return x > -INFINITY ? 1u : 0u; };
+        fast = floor_hist(nch, [&](int e, float& x, uint32_t& w) { x = cm[e]; w = wt(x); }, m,
+                          static_cast<uint32_t>(n), reinterpret_cast<uint32_t*>(KS.fb.lhist), zf);
+        if (!fast) {
+            uint32_t edge = 0;
+            fast = floor_block(nch, [&](int e, uint32_t& key, uint32_t& w) { key = fkey(cm[e]); w = wt(cm[e]); },
+                               static_cast<uint32_t>(n), SS, edge);
+            if (fast) zf = Ctx::lo_float(edge);
+        }
+        fast = fast && zf > -INFINITY;
+    }
+    auto emit = [&](const float (&z)[VEC], int vrow, float thr) {
+        int cnt = 0;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cnt += (z[e] >= thr) ? 1 : 0;
+        if (cnt > 0) {
+            uint32_t pos = atomicAdd(&SS.ccount, static_cast<uint32_t>(cnt));
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                if (z[e] >= thr) {
+                    if (pos < static_cast<uint32_t>(kCandCap))
+                        cc[pos] = (static_cast<uint64_t>(fkey(z[e])) << 32) |
+                                  (0xFFFFFFFFu - static_cast<uint32_t>(vrow * VEC + e));
+                    ++pos;
+                }
+            }
+        }
+    };
+    if (fast) {
+        // ids >= zf from the chunks whose max reaches it: one vector (the max's)
+        // when the other vectors lie below zf, else all 32, one per lane
+        const int Lv = a.L / VEC;
+        const int wcap = (nch + kWarps - 1) / kWarps;
+        for (int g = warp * wcap; g < min(nch, warp * wcap + wcap); ++g) {
+            if (!(cm[g] >= zf)) continue;  // (warp-uniform)
+            const int c = g / kChunks;
+            const int sn = min((c + 1) * a.L, a.V) - c * a.L;
+            const char* sb = rowp + static_cast<int64_t>(c) * a.L * E::kBytes;
+            const bool single = cu2[g] < zf && cln[g] >= 0;
+            const int vs = (g % kChunks) * 32 + (single ? cln[g] : lane);
+            if (single && lane != 0) continue;
+            float z[VEC];
+            if (vs * VEC < sn) {
+                E::unpack(single && want_mv ? cmv[g] : E::global_vec(sb, vs, sn, a.aligned), z);
+                if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, c * Lv + vs, z);
+                emit(z, c * Lv + vs, zf);
+            }
+        }
+        __syncthreads();
+        fast = SS.ccount <= static_cast<uint32_t>(kCandCap);
+    }
+    if (!fast) {
+        // exact: the top-k set for k = n by threshold bisection, then its ids
+        __syncthreads();
+        cg::cluster_group cl = cg::this_cluster();
+        Ctx X(KS.fb, cl);
+        setup_row_ctx<DT, HIST>(X, a, row, rowp, cm, pbm, pwp, ppat, has_patch, row_nan, m, cT, scale, infm, dyn);
+        for (int b = tid; b < kBins; b += kThreads) KS.fb.ghist[b] = 0;
+        if (tid == 0) {
+            KS.fb.ccount = 0;
+            KS.fb.flags = 0;
+            SS.ccount = 0;
+        }
+        __syncthreads();
+        uint32_t err = 0;
+        const Surv K = select_topk(X, n, fkey(m), err);
+        __syncthreads();
+        X.batched_pass([&](int v) { return X.may_hold(v, K.zt); },
+                       [&](int, int v, const float(&z)[VEC]) {
+                           float zk[VEC];
+#pragma unroll
+                           for (int e = 0; e < VEC; ++e)  // (the row's tail vector pads past V with -inf)
+                               zk[e] = (v * VEC + e < a.V && K.test(z[e], v * VEC + e)) ? z[e] : NAN;
+                           emit(zk, v, -INFINITY);
+                       },
+                       [](int) {});
+        __syncthreads();
+    }
+    // rank by (key desc, id asc); the first n are written, the rest padded
+    const int nc = min(static_cast<int>(SS.ccount), kCandCap);
+    const double lnS = SS.bd[0];
+    for (int i = tid; i < nc; i += kThreads) {
+        const uint64_t vi = cc[i];
+        int rk = 0;
+#pragma unroll 8
+        for (int j = 0; j < nc; ++j) rk += (cc[j] > vi) ? 1 : 0;
+        if (rk < n) {
+            const float z = key_to_float(static_cast<uint32_t>(vi >> 32));
+            const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(vi));
+            float lp;
+            if (infm)
+                lp = z == INFINITY ? static_cast<float>(-lnS) : -INFINITY;
+            else if (z == -INFINITY)
+                lp = -INFINITY;
+            else
+                lp = static_cast<float>((static_cast<double>(z) - static_cast<double>(m)) / static_cast<double>(Tm) - lnS);
+            out[rk] = arc_top_logprob{id, lp};
+        }
+    }
+    for (int j = nc + tid; j < n; j += kThreads) out[j] = arc_top_logprob{-1, -INFINITY};
+}
+
 // One row's finish by one CTA.  sum_at(c) is slice c's summary (the
 // workspace, or another CTA's shared memory in the cluster kernel); wait()
 // returns once every summary of the row is complete and visible; loaded()
@@ -1020,7 +1212,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
         !(P.top_k == 1))
         tl = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
     // the finish needs the chunk max vectors (filtered rows)
-    const bool want_mv = a.cmv_off >= 0 && param_errors(P) == 0 && RowMode(P, a.V).filtered;
+    const bool want_mv = a.cmv_off >= 0 && param_errors(P) == 0 && (RowMode(P, a.V).filtered || a.top_n > 0);
     // the summaries are complete and visible after this (the parameters and
     // history above are not written by the scan)
     wait();
@@ -1105,7 +1297,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
     st.am = SS.bi[0];
     const uint32_t rflags = static_cast<uint32_t>(SS.bi[1]);
     st.row_nan = (rflags & ARC_ERR_NAN) != 0;
-    st.cT = md.greedy ? 0.0f : __fdiv_rn(1.4426950408889634f, T);
+    st.cT = (md.greedy && a.top_n == 0) ? 0.0f : __fdiv_rn(1.4426950408889634f, T > 0.0f ? T : 1.0f);
     st.scale = __uint_as_float(static_cast<uint32_t>(127 + a.F) << 23);
     st.infm = (st.m == INFINITY);
     st.zm = md.minp_on ? SS.bf[1] : -INFINITY;
@@ -1635,6 +1827,9 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
             }
         }
     }
+
+    if (a.top_n > 0)
+        top_n_row<DT, HIST>(a, row, P, mode >= 0, rowp, m, st.row_nan, cT, st.scale, want_mv, hbeg, hn, KS, dyn);
 
     // -------------------------------------------------------------- results
     if (tid == 0) {

@@ -57,9 +57,15 @@ class Options(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("ctas_per_row", ctypes.c_int32),
         ("max_hist_len", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("top_n", ctypes.c_int32),
         ("debug", ctypes.c_void_p),
+        ("top_logprobs", ctypes.c_void_p),
     ]
+
+
+# arc_top_logprob, 8 bytes
+TOP_LOGPROB_DTYPE = np.dtype([("id", "<i4"), ("logprob", "<f4")])
+ARC_MAX_TOP_N = 64
 
 
 class Geometry(ctypes.Structure):
@@ -180,9 +186,22 @@ def debug_records(t) -> np.ndarray:
     return t.cpu().numpy().view(ROW_DEBUG_DTYPE)
 
 
-def make_options(ctas_per_row=0, max_hist_len=0, autoinc=False, debug=None, force_bisection=False) -> Options:
+def make_options(ctas_per_row=0, max_hist_len=0, autoinc=False, debug=None, force_bisection=False,
+                 top_n=0, top_logprobs=None) -> Options:
     flags = (ARC_OPT_STEP_AUTOINC if autoinc else 0) | (ARC_OPT_FORCE_BISECTION if force_bisection else 0)
-    return Options(flags, int(ctas_per_row), int(max_hist_len), 0, _ptr(debug))
+    return Options(flags, int(ctas_per_row), int(max_hist_len), int(top_n), _ptr(debug), _ptr(top_logprobs))
+
+
+def top_logprobs_tensor(B: int, n: int, device="cuda"):
+    """Device output for top_n log-probabilities: arc_top_logprob [B][n] as bytes."""
+    import torch
+
+    return torch.zeros(B * n * TOP_LOGPROB_DTYPE.itemsize, dtype=torch.uint8, device=device)
+
+
+def top_logprobs_records(t, n: int) -> np.ndarray:
+    """Host view [B, n] of a top-n log-probability tensor (fields id, logprob)."""
+    return t.cpu().numpy().view(TOP_LOGPROB_DTYPE).reshape(-1, n)
 
 
 def workspace_bytes(B: int, V: int, dtype: int, has_history=False, ctas_per_row=0, max_hist_len=0) -> int:
@@ -204,7 +223,7 @@ def workspace_tensor(B: int, V: int, dtype: int, has_history=False, ctas_per_row
 
 def sample_batch(logits, params, out, hist_offsets=None, hist_ids=None, err_word=None, debug=None,
                  workspace=None, ctas_per_row=0, max_hist_len=0, autoinc=False, stream=None,
-                 check=True, force_bisection=False) -> int:
+                 check=True, force_bisection=False, top_n=0, top_logprobs=None) -> int:
     """arc_sample_batch on CUDA tensors: logits [B, V] (row stride >= V), params uint8
     [B*48], out int32 [B], optional CSR history (int32), err_word uint32 [1], debug uint8
     [B*72], workspace uint8 (zero-filled once; allocated here when None)."""
@@ -215,7 +234,7 @@ def sample_batch(logits, params, out, hist_offsets=None, hist_ids=None, err_word
     if workspace is None:
         workspace = workspace_tensor(B, V, _dtype_code(logits), hist_offsets is not None, ctas_per_row,
                                      max_hist_len, device=logits.device)
-    opts = make_options(ctas_per_row, max_hist_len, autoinc, debug, force_bisection)
+    opts = make_options(ctas_per_row, max_hist_len, autoinc, debug, force_bisection, top_n, top_logprobs)
     rc = load().arc_sample_batch(_ptr(logits), B, V, ld, _dtype_code(logits), _ptr(params),
                                  _ptr(hist_offsets), _ptr(hist_ids), _ptr(out), _ptr(err_word),
                                  _ptr(workspace), int(workspace.numel()), ctypes.byref(opts),
@@ -226,14 +245,15 @@ def sample_batch(logits, params, out, hist_offsets=None, hist_ids=None, err_word
 
 
 def sample_batch_static(logits, params, out, hist_offsets=None, hist_ids=None, err_word=None, debug=None,
-                        ctas_per_row=0, max_hist_len=0, autoinc=False, stream=None, check=True) -> int:
+                        ctas_per_row=0, max_hist_len=0, autoinc=False, stream=None, check=True,
+                        top_n=0, top_logprobs=None) -> int:
     """arc_sample_batch_static: as sample_batch, with the library's own scratch
     array instead of a workspace (nothing is allocated for the call)."""
     B, V = int(logits.shape[0]), int(logits.shape[1])
     ld = int(logits.stride(0)) if B > 1 else V
     if logits.stride(1) != 1:
         raise ValueError("logits rows must be contiguous")
-    opts = make_options(ctas_per_row, max_hist_len, autoinc, debug)
+    opts = make_options(ctas_per_row, max_hist_len, autoinc, debug, top_n=top_n, top_logprobs=top_logprobs)
     rc = load().arc_sample_batch_static(_ptr(logits), B, V, ld, _dtype_code(logits), _ptr(params),
                                         _ptr(hist_offsets), _ptr(hist_ids), _ptr(out), _ptr(err_word),
                                         ctypes.byref(opts), _stream(stream))

@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define ARC_SAMPLE_ABI_VERSION 1
+#define ARC_SAMPLE_ABI_VERSION 2
 
 /* logits element types */
 #define ARC_F32 0
@@ -155,13 +155,32 @@ typedef struct arc_row_debug {
  * for cross-checking the two (arc_row_debug.passes tells which ran) */
 #define ARC_OPT_FORCE_BISECTION 0x2u
 
+/*
+ * Top-n log-probabilities, one record per listed id (DEVICE memory, [B][top_n]).
+ * Arc PR #222, section 3(b): the top-n log-probability output reads the
+ * sampler's sort.  Row r lists the top_n ids first in (z desc, id asc) order
+ * of its penalised logits -- the top-k filter's order -- with
+ *     logprob = (z - max z) / T - ln(sum over every id of exp((z' - max z) / T))
+ * at the row's sampling temperature (T = 1 for a greedy row, T == 0), before
+ * the top-k / top-p / min-p filters.  -inf logits list logprob -inf; when the
+ * max is +inf the +inf ids share the mass; entries past V, and every entry of
+ * a row with invalid parameters, are (id -1, logprob -inf).
+ */
+typedef struct arc_top_logprob {
+    int32_t id;
+    float logprob;
+} arc_top_logprob;
+
+#define ARC_MAX_TOP_N 64
+
 /* Host struct; pass NULL for defaults. */
 typedef struct arc_sample_options {
     uint32_t flags;
     int32_t ctas_per_row;  /* slices (scan CTAs) per row: 0 = automatic, else 1..128 */
     int32_t max_hist_len;  /* upper bound on any row's history length; 0 = 1024 */
-    int32_t reserved;
+    int32_t top_n;         /* 0: off; 1..ARC_MAX_TOP_N: write top_logprobs */
     arc_row_debug* debug;  /* device [B] or NULL */
+    arc_top_logprob* top_logprobs;  /* device [B][top_n]; required when top_n > 0 */
 } arc_sample_options;
 
 /*

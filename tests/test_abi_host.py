@@ -49,7 +49,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.arc_sample_abi_version() == 1
+    assert lib.arc_sample_abi_version() == 2
     assert sampler.strerror(0) == "ok"
     for rc in range(-1, -9, -1):
         assert len(sampler.strerror(rc)) > 10 and "unknown" not in sampler.strerror(rc)
@@ -59,7 +59,8 @@ def test_abi_version_and_strerror(lib):
 def test_struct_layouts_match_header():
     assert workloads.ROW_PARAMS_DTYPE.itemsize == 48
     assert sampler.ROW_DEBUG_DTYPE.itemsize == 72
-    assert ctypes.sizeof(sampler.Options) == 24
+    assert ctypes.sizeof(sampler.Options) == 32
+    assert sampler.TOP_LOGPROB_DTYPE.itemsize == 8
     assert ctypes.sizeof(sampler.Geometry) == 40
     # field offsets of arc_row_params as laid out in the header
     off = {n: workloads.ROW_PARAMS_DTYPE.fields[n][1] for n in workloads.ROW_PARAMS_DTYPE.names}
@@ -103,7 +104,12 @@ def test_bad_arguments_fail_before_any_cuda_call(lib):
     assert lib.arc_sample_plan(2, 1000, 1, 0, ctypes.byref(both), ctypes.byref(geom)) == sampler.ARC_OK
     assert lib.arc_sample_workspace_bytes(2, 1000, 1, 0, ctypes.byref(both)) > 0
     assert call_batch(lib, opts=sampler.Options(0, 0, -1, 0, None)) == sampler.ARC_E_OPTION
-    assert call_batch(lib, opts=sampler.Options(0, 0, 0, 5, None)) == sampler.ARC_E_OPTION
+    # top-n log-probabilities: 1..64 ids, and an output pointer with them
+    assert call_batch(lib, opts=sampler.Options(0, 0, 0, 5, None, None)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, opts=sampler.Options(0, 0, 0, -1, None, FAKE)) == sampler.ARC_E_OPTION
+    assert call_batch(lib, opts=sampler.Options(0, 0, 0, 65, None, FAKE)) == sampler.ARC_E_OPTION
+    assert sampler.ARC_MAX_TOP_N == 64 and sampler.TOP_LOGPROB_DTYPE.itemsize == 8
+    assert lib.arc_sample_abi_version() == 2
     g = lib.arc_sample_greedy
     assert g(None, 2, 8, 8, 1, FAKE, None, None) == sampler.ARC_E_NULL
     assert g(FAKE, 2, 8, 4, 1, FAKE, None, None) == sampler.ARC_E_SHAPE

@@ -381,3 +381,87 @@ def test_cluster_path_matches_two_kernels(cuda_lib, B, V, dtype, hist_len):
     assert np.array_equal(d1, d2)
     rep = parity.check_batch(w, t1, d1)
     assert rep.rows == B
+
+
+def _check_top_logprobs(w, res, got, n):
+    """ids exact; log-probabilities within 2e-6 + 1e-6 |lp| of the fp64 oracle
+    (the fp32 chunk masses carry ~1e-7 relative error into ln S)."""
+    bad = 0
+    for r, rr in enumerate(res):
+        g = got[r]
+        if rr.mode == oracle.MODE_INVALID:
+            assert (g["id"] == -1).all() and np.isneginf(g["logprob"]).all(), r
+            continue
+        ids, lp = oracle.top_logprobs(rr.z, float(w.params[r]["temperature"]), n)
+        assert g["id"].tolist() == ids.tolist(), (r, g["id"][:8].tolist(), ids[:8].tolist())
+        fin = np.isfinite(lp)
+        assert np.array_equal(np.isfinite(g["logprob"]), fin), r
+        err = np.abs(g["logprob"][fin].astype(np.float64) - lp[fin])
+        bad += int((err > 2e-6 + 1e-6 * np.abs(lp[fin])).sum())
+    assert bad == 0, bad
+
+
+@pytest.mark.parametrize("name,n", [("small_fp32", 8), ("mixed_quarters", 5), ("penalized", 20),
+                                    ("adversarial_ties", 64)])
+def test_top_logprobs_match_the_oracle(cuda_lib, name, n):
+    """Top-n (id, log-probability) per row through the C ABI, next to the
+    sampled tokens, which the option leaves unchanged."""
+    import torch
+
+    S = cuda_lib
+    w, res = named(name)
+    mhl = 256 if w.hist_offsets is not None else 0
+    logits = S.logits_tensor(w)
+    prm = S.params_tensor(w.params)
+    hoff, hids = S.history_tensors(w)
+    out = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    tl = S.top_logprobs_tensor(w.B, n)
+    S.sample_batch(logits, prm, out, hoff, hids, max_hist_len=mhl, top_n=n, top_logprobs=tl)
+    torch.cuda.synchronize()
+    _check_top_logprobs(w, res, S.top_logprobs_records(tl, n), n)
+    base, _, _ = run(S, w, max_hist_len=mhl)
+    assert np.array_equal(out.cpu().numpy(), base)
+
+
+def test_top_logprobs_edge_rows(cuda_lib):
+    """Ragged V below n (padding), NaN, -inf, +inf and invalid rows, ties; one
+    launch (cluster) and two launches give the same records."""
+    import torch
+
+    S = cuda_lib
+    V, n = 3000, 16
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((8, V)).astype(np.float32)
+    z[1, :] = -np.inf
+    z[2, 17] = np.nan
+    z[3, [3, 77]] = np.inf
+    z[4, :] = np.round(z[4, :])  # heavy ties
+    z[5, :] = 0.0
+    p = wl.make_params(8)
+    p["seed"] = np.arange(8)
+    p[6]["temperature"] = -1.0  # invalid
+    p[7]["temperature"] = 0.0   # greedy: log-probabilities at T = 1
+    p[0]["top_k"] = 10
+    p[0]["temperature"] = 0.5
+    w = wl.Workload("edges", wl.DTYPE_F32, z, p)
+    res = oracle.sample_batch(w.logits_f32(), w.params)
+    for cpr in (0, 5):
+        logits = S.logits_tensor(w)
+        prm = S.params_tensor(w.params)
+        out = torch.zeros(8, dtype=torch.int32, device="cuda")
+        tl = S.top_logprobs_tensor(8, n)
+        S.sample_batch(logits, prm, out, ctas_per_row=cpr, top_n=n, top_logprobs=tl)
+        torch.cuda.synchronize()
+        _check_top_logprobs(w, res, S.top_logprobs_records(tl, n), n)
+    # fewer ids than n: the rest is (-1, -inf)
+    w2 = wl.random_case(seed=8, B=3, V=5, dtype=1)
+    res2 = oracle.sample_batch(w2.logits_f32(), w2.params)
+    logits = S.logits_tensor(w2)
+    prm = S.params_tensor(w2.params)
+    out = torch.zeros(3, dtype=torch.int32, device="cuda")
+    tl = S.top_logprobs_tensor(3, 8)
+    S.sample_batch(logits, prm, out, top_n=8, top_logprobs=tl)
+    torch.cuda.synchronize()
+    got = S.top_logprobs_records(tl, 8)
+    _check_top_logprobs(w2, res2, got, 8)
+    assert (got["id"][:, 5:] == -1).all()
