@@ -38,7 +38,6 @@ struct Plan {
     int clist_off = 0;
     int cand_off = 0;
     int sorted_off = 0;
-    int stage_off = 0;
     int fb_wsum_off = 0;
     int fb_patch_off = 0;
     int fb_rounds = 0;
@@ -131,7 +130,7 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     const int64_t cs_bytes = 3 * cmax_bytes;  // masses, max ids, second largest logits
     const int64_t clist_bytes = r128((s * kChunks + kWarps) * 4);
     const int64_t cand_bytes = r128(int64_t{kCandCap} * 16);
-    const int64_t stage_bytes = int64_t{kWarps} * kCollectU * 32 * 16 + cand_bytes;  // + sorted candidates
+    const int64_t stage_bytes = cand_bytes;  // the candidates in rank order
     const int64_t nv_row = (V + vec - 1) / vec;
     const int64_t fb_rounds = (nv_row + kThreads - 1) / kThreads;
     const int64_t fb_wsum = r128(fb_rounds * kWarps * 8);
@@ -163,14 +162,13 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     p.cv2_off = static_cast<int>(3 * cmax_bytes);
     p.clist_off = static_cast<int>(cmax_bytes + cs_bytes);
     p.cand_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes);
-    p.stage_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes);
-    p.sorted_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + int64_t{kWarps} * kCollectU * 32 * 16);
+    p.sorted_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes);
     p.fb_wsum_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes);
     p.fb_patch_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum);
     p.fb_rounds = static_cast<int>(fb_rounds);
     p.cmv_off = cmv_bytes ? static_cast<int>(fin_smem - cmv_bytes) : -1;
     // every region holds 16-byte vectors or 8-byte words: starts must be 16-byte aligned
-    for (const int off : {p.cs_off, p.cid_off, p.cv2_off, p.clist_off, p.cand_off, p.sorted_off, p.stage_off,
+    for (const int off : {p.cs_off, p.cid_off, p.cv2_off, p.clist_off, p.cand_off, p.sorted_off,
                           p.fb_wsum_off, p.fb_patch_off, p.cmv_off})
         if (off >= 0 && off % 16 != 0) return ARC_E_UNSUPPORTED;
     p.fin_smem = static_cast<int>(fin_smem);
@@ -429,7 +427,6 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.clist_off = p.clist_off;
     fa.cand_off = p.cand_off;
     fa.sorted_off = p.sorted_off;
-    fa.stage_off = p.stage_off;
     fa.fb_wsum_off = p.fb_wsum_off;
     fa.fb_patch_off = p.fb_patch_off;
     fa.fb_rounds = p.fb_rounds;

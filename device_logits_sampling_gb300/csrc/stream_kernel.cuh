@@ -39,7 +39,6 @@ constexpr int kEntryBytes = kChunks * 16;  // chunk entries of a slice
 constexpr int kSummaryBytes = kHdrBytes + 2 * kEntryBytes;
 constexpr int kMaxRowCtas = 128;         // slices per row at most
 constexpr int kCandCap = 1024;           // ids the direct selection holds
-constexpr int kCollectU = 8;             // chunks per warp in flight while gathering
 
 struct ScanArgs {
     const void* logits;
@@ -85,7 +84,6 @@ struct FinishArgs {
     int clist_off;     //   per-warp candidate chunk lists,
     int cand_off;      //   candidates (key, id, mass),
     int sorted_off;    //   the candidates in (key desc, id asc) order,
-    int stage_off;     //   gather staging (kWarps x kCollectU x 32 vectors),
     int fb_wsum_off;   //   per-(round, warp) masses,
     int fb_patch_off;  //   row patch tables
     int fb_rounds;     // rounds of a whole row
@@ -108,6 +106,7 @@ struct FinishScratch {
     uint64_t bu[8];
     float bf[8];
     uint32_t ccount;  // candidates gathered
+    uint32_t nwhole;  // chunks listed for a whole read
     uint32_t fc[2][kWarps][4];  // floor search partial counts
     double bd[2];
 };
@@ -1284,7 +1283,10 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
     // the floor histogram and the candidate counter start at zero (filtered
     // rows), cleared while the summaries load
     for (int b = tid; b < kFloorHistWords; b += kThreads) reinterpret_cast<uint32_t*>(KS.fb.lhist)[b] = 0u;
-    if (tid == 0) SS.ccount = 0;  // candidates gathered (filtered rows)
+    if (tid == 0) {
+        SS.ccount = 0;  // candidates gathered (filtered rows)
+        SS.nwhole = 0;
+    }
     uint32_t rerr = param_errors(P);
     const RowMode md(P, a.V);
     const float T = P.temperature;
@@ -1524,11 +1526,11 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
             // (the candidate counter was cleared with the summaries)
             fast = fast && zf > -INFINITY && !(a.flags & ARC_OPT_FORCE_BISECTION);
 
-            // gather the ids >= zf as (key, id, mass): each warp takes the chunks
-            // of its eighth whose max is >= zf, stages up to kCollectU of them at a
-            // time in shared memory with 16-byte asynchronous copies (all in
-            // flight together); the ids found take slots from one counter, one
-            // atomic per warp and element position
+            // gather the ids >= zf as (key, id): every thread takes a contiguous run
+            // of chunk entries; a chunk whose other vectors lie below zf ("single")
+            // gives the ids of its max's vector, taken from the summary, and any
+            // other chunk at or above zf is listed; after one barrier the warps read
+            // the listed chunks from the logits, 32 vectors (one per lane) each
             // candidates as one 64-bit value: key << 32 | (2^32 - 1 - id), so
             // that a larger value ranks first by (z desc, id asc)
             uint64_t* cc = reinterpret_cast<uint64_t*>(dyn + a.cand_off);
@@ -1538,58 +1540,12 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
             int nc = 0;
             if (fast) {
                 const int Lv = a.L / VEC;
-                uint4* stage = reinterpret_cast<uint4*>(dyn + a.stage_off) + warp * (kCollectU * 32);
-                int* wl = reinterpret_cast<int*>(dyn + a.clist_off) + warp * ((nch + kWarps - 1) / kWarps);
-                // classify this warp's chunks (a contiguous eighth of the table,
-                // read without bank conflicts) at or above zf: "single" when the
-                // other vectors lie below zf (only the max's vector can hold ids
-                // >= zf), else "whole"; lists from both ends of wl
-                const int wcap = (nch + kWarps - 1) / kWarps;
-                const unsigned below = (1u << lane) - 1u;
-                int nsg = 0, nw = 0;
-                const int gw0 = warp * wcap, gw1 = min(nch, gw0 + wcap);
-                for (int b0 = gw0; b0 < gw1; b0 += 32) {
-                    const int g = b0 + lane;
-                    const bool in = g < gw1 && cm[g] >= zf;
-                    const bool single = in && cu2[g] < zf && cln[g] >= 0;
-                    const unsigned bs = __ballot_sync(0xFFFFFFFFu, single);
-                    const unsigned bw = __ballot_sync(0xFFFFFFFFu, in && !single);
-                    if (single) wl[nsg + __popc(bs & below)] = g;
-                    if (in && !single) wl[wcap - 1 - (nw + __popc(bw & below))] = g;
-                    nsg += __popc(bs);
-                    nw += __popc(bw);
-                }
-                __syncwarp();
-                const uint4 ninf = (DT == ARC_BF16) ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
-                                                    : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
-                // whole chunks, up to kCollectU per round, staged by 16-byte
-                // asynchronous copies; the first round goes out before the singles
-                auto stage_round = [&](int r0) {
-#pragma unroll
-                    for (int u = 0; u < kCollectU; ++u) {
-                        if (r0 + u < nw) {
-                            const int g = wl[wcap - 1 - (r0 + u)];
-                            const int c = g / kChunks;
-                            const int vs = (g % kChunks) * 32 + lane;
-                            const int sn = min((c + 1) * a.L, a.V) - c * a.L;
-                            const char* sb = rowp + static_cast<int64_t>(c) * a.L * E::kBytes;
-                            uint4* dst = stage + u * 32 + lane;
-                            if (a.aligned && (vs + 1) * VEC <= sn)
-                                cp_async16(dst, sb + static_cast<size_t>(vs) * 16);
-                            else
-                                *dst = (vs * VEC < sn) ? E::global_vec(sb, vs, sn, false) : ninf;
-                        }
-                    }
-                };
-                stage_round(0);
-                // ids found take slots from one shared counter: one atomic per lane
-                // that found any (few lanes of a chunk do)
-                auto emit = [&](bool valid, const float (&z)[VEC], int vrow) {
+                int* whole = reinterpret_cast<int*>(dyn + a.clist_off);  // listed chunks
+                // the ids of a vector >= zf take slots from one shared counter
+                auto emit = [&](const float (&z)[VEC], int vrow) {
                     int cnt = 0;
-                    if (valid) {
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
-                    }
+                    for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
                     if (cnt > 0) {
                         uint32_t pos = atomicAdd(&SS.ccount, static_cast<uint32_t>(cnt));
 #pragma unroll
@@ -1603,65 +1559,66 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                         }
                     }
                 };
-                // the gather stops once more ids than the selection holds are
-                // found (the threshold bisection then takes the row)
-                auto overflowed = [&]() {
-                    const uint32_t c = *reinterpret_cast<volatile const uint32_t*>(&SS.ccount);
-                    return __shfl_sync(0xFFFFFFFFu, c, 0) > static_cast<uint32_t>(kCandCap);
-                };
-                // single vectors: lane i reads entries i and i + 32 of each 64
-                for (int i0 = 0; i0 < nsg; i0 += 64) {
-                    if (i0 > 0 && overflowed()) break;
-                    uint4 raw[2];
-                    int vrow[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = i0 + u * 32 + lane;
-                        vrow[u] = -1;
-                        if (i < nsg) {
-                            const int g = wl[i];
-                            const int c = g / kChunks;
-                            const int vs = (g % kChunks) * 32 + cln[g];
-                            const int sn = min((c + 1) * a.L, a.V) - c * a.L;
-                            raw[u] = want_mv ? reinterpret_cast<const uint4*>(dyn + a.cmv_off)[g]
-                                             : E::global_vec(rowp + static_cast<int64_t>(c) * a.L * E::kBytes, vs,
-                                                             sn, a.aligned);
-                            vrow[u] = c * Lv + vs;
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
+                for (int g = ce0; g < ce1; ++g) {
+                    if (!(cm[g] >= zf)) continue;
+                    const int c = g / kChunks;
+                    if (cu2[g] < zf && cln[g] >= 0) {
+                        const int vs = (g % kChunks) * 32 + cln[g];
+                        const int sn = min((c + 1) * a.L, a.V) - c * a.L;
                         float z[VEC];
-                        if (vrow[u] >= 0) {
-                            E::unpack(raw[u], z);
-                            if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, vrow[u], z);
-                        }
-                        emit(vrow[u] >= 0, z, vrow[u]);
+                        E::unpack(want_mv ? reinterpret_cast<const uint4*>(dyn + a.cmv_off)[g]
+                                          : E::global_vec(rowp + static_cast<int64_t>(c) * a.L * E::kBytes, vs, sn,
+                                                          a.aligned),
+                                  z);
+                        if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, c * Lv + vs, z);
+                        emit(z, c * Lv + vs);
+                    } else {
+                        whole[atomicAdd(&SS.nwhole, 1u)] = g;
                     }
-                }
-                // whole chunks
-                for (int r0 = 0; r0 < nw; r0 += kCollectU) {
-                    if (r0 > 0) {
-                        if (overflowed()) break;  // (no copy of this warp is in flight here)
-                        stage_round(r0);
-                    }
-                    cp_async_wait_all();
-                    __syncwarp();
-                    const int nst = min(kCollectU, nw - r0);
-                    for (int u = 0; u < nst; ++u) {
-                        const int g = wl[wcap - 1 - (r0 + u)];
-                        const int c = g / kChunks;
-                        const int vs = (g % kChunks) * 32 + lane;
-                        float z[VEC];
-                        E::unpack(stage[u * 32 + lane], z);
-                        // padding vectors past the slice read as -inf and take no patch
-                        if (HIST && has_patch && vs * VEC < min((c + 1) * a.L, a.V) - c * a.L)
-                            apply_patches<VEC>(pbm, pwp, ppat, c * Lv + vs, z);
-                        emit(true, z, c * Lv + vs);
-                    }
-                    __syncwarp();  // the stage is refilled next round
                 }
                 __syncthreads();
+                const int nw = static_cast<int>(SS.nwhole);
+                // a listed chunk holds at least two ids >= zf (its max and its
+                // second vector max): a list that cannot fit is not read
+                if (nw > 0 && SS.ccount + 2u * static_cast<uint32_t>(nw) <= static_cast<uint32_t>(kCandCap)) {
+                    // warp w reads listed chunks w, w + 8, ...: up to four in flight per lane
+                    constexpr int kU = 4;
+                    for (int i0 = warp; i0 < nw; i0 += kU * kWarps) {
+                        const uint32_t got = *reinterpret_cast<volatile const uint32_t*>(&SS.ccount);
+                        if (__shfl_sync(0xFFFFFFFFu, got, 0) > static_cast<uint32_t>(kCandCap)) break;
+                        uint4 raw[kU];
+                        int vr[kU];
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            const int i = i0 + u * kWarps;
+                            vr[u] = -1;
+                            if (i < nw) {
+                                const int g = whole[i];
+                                const int c = g / kChunks;
+                                const int vs = (g % kChunks) * 32 + lane;
+                                const int sn = min((c + 1) * a.L, a.V) - c * a.L;
+                                if (vs * VEC < sn) {  // padding vectors past the slice hold no id
+                                    raw[u] = E::global_vec(rowp + static_cast<int64_t>(c) * a.L * E::kBytes, vs, sn,
+                                                           a.aligned);
+                                    vr[u] = c * Lv + vs;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            if (vr[u] >= 0) {
+                                float z[VEC];
+                                E::unpack(raw[u], z);
+                                if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, vr[u], z);
+                                emit(z, vr[u]);
+                            }
+                        }
+                    }
+                    __syncthreads();
+                } else if (nw > 0) {
+                    SS.ccount = kCandCap + 1;  // (every thread stores the same value)
+                    __syncthreads();
+                }
                 nc = static_cast<int>(SS.ccount);
                 fast = nc <= kCandCap;
             }
