@@ -558,15 +558,19 @@ __device__ int tie_walk(Ctx& X, float zt, uint64_t need) {
     return pos;
 }
 
-// Exact top-k survivor set: the first k ids by (z desc, id asc).
+// Exact top-k survivor set: the first k ids by (z desc, id asc).  zhint, when
+// finite, is a known lower bound of the k-th largest logit: the first window
+// starts there.
 template <class Ctx>
-__device__ Surv select_topk(Ctx& X, int k, uint32_t Km, uint32_t& err) {
+__device__ Surv select_topk(Ctx& X, int k, uint32_t Km, uint32_t& err, float zhint = -INFINITY) {
     const Surv all{-INFINITY, INT_MAX};
     uint64_t tgt = static_cast<uint64_t>(k);
-    // first window: 2^23 keys (one binade) below the max, widened 16x while it
-    // holds fewer than k ids
+    // first window: from the hint, else 2^23 keys (one binade) below the max,
+    // widened 16x while it holds fewer than k ids
     uint32_t width = 1u << 23;
-    Window W = Ctx::make_window(Km > width - 1 ? Km - (width - 1) : 0u, Km);
+    const bool hinted = zhint > -INFINITY && zhint <= key_to_float(Km);
+    Window W = hinted ? Ctx::make_window(fkey(zhint), Km)
+                      : Ctx::make_window(Km > width - 1 ? Km - (width - 1) : 0u, Km);
     bool first = true;
     while (true) {
         pass_hist<Ctx, false>(X, W, all);

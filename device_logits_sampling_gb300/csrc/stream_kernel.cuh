@@ -422,21 +422,39 @@ __device__ __forceinline__ float warp_max_nonan(float v) {
     return r;
 }
 
-// Four warp sums at once: lane l ends with the sum over the warp of
-// v[2 * bit4(l) + bit3(l)] (lanes 0, 8, 16, 24 hold sums 0..3).
-__device__ __forceinline__ float warp_sum4(const float (&v)[4], int lane) {
-    const bool h = (lane & 16) != 0;
-    float a0 = h ? v[2] : v[0], a1 = h ? v[3] : v[1];
-    const float s0 = h ? v[0] : v[2], s1 = h ? v[1] : v[3];
-    a0 = __fadd_rn(a0, __shfl_xor_sync(0xFFFFFFFFu, s0, 16));
-    a1 = __fadd_rn(a1, __shfl_xor_sync(0xFFFFFFFFu, s1, 16));
-    const bool q = (lane & 8) != 0;
-    float b = q ? a1 : a0;
-    const float t = q ? a0 : a1;
-    b = __fadd_rn(b, __shfl_xor_sync(0xFFFFFFFFu, t, 8));
+// NV warp sums at once (NV a power of two <= 32): lane l ends with the sum
+// over the warp of v[l / (32 / NV)] (lanes 0, 32/NV, 2*32/NV, ... hold sums
+// 0, 1, 2, ...).  Each halving step keeps the half of the values that the
+// lane's bit selects and adds the partner's copy of it.
+template <int NV>
+__device__ __forceinline__ float warp_sum_n(const float (&v)[NV], int lane) {
+    float a[NV];
 #pragma unroll
-    for (int d = 4; d > 0; d >>= 1) b = __fadd_rn(b, __shfl_xor_sync(0xFFFFFFFFu, b, d));
+    for (int i = 0; i < NV; ++i) a[i] = v[i];
+    int d = 16;
+#pragma unroll
+    for (int h = NV / 2; h >= 1; h /= 2, d /= 2) {
+        const bool up = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float keep = up ? a[i + h] : a[i];
+            const float send = up ? a[i] : a[i + h];
+            a[i] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, d));
+        }
+    }
+    float b = a[0];
+#pragma unroll
+    for (; d > 0; d /= 2) b = __fadd_rn(b, __shfl_xor_sync(0xFFFFFFFFu, b, d));
     return b;
+}
+
+// The j-th of a thread's vectors, for a j the compiler cannot see.
+__device__ __forceinline__ uint4 pick(const uint4 (&d)[kVpt], int j) {
+    uint4 r = d[0];
+#pragma unroll
+    for (int i = 1; i < kVpt; ++i)
+        if (j == i) r = d[i];
+    return r;
 }
 
 // One slice, its vectors already in registers (vectors past the slice read
@@ -447,7 +465,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
                                            unsigned char* mysum) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
-    static_assert(kVpt == 4, "warp_sum4 pairs the four vectors of a thread with lanes 0, 8, 16, 24");
+    constexpr int kSumLanes = 32 / kVpt;  // lane kSumLanes * j holds chunk j's mass
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int a0 = cidx * a.L;
     const int n = min(a0 + a.L, a.V) - a0;  // > 0: the plan makes no empty slice
@@ -562,7 +580,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
                     sl[j] = l;
                 }
             }
-            S = warp_sum4(sl, lane);
+            S = warp_sum_n<kVpt>(sl, lane);
         }
         // entry j as soon as its fields are known, by lane 8j (which holds the
         // chunk's mass): nothing per chunk stays live across the loop
@@ -580,9 +598,9 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
                 // the max's vector as loaded (history patches are applied by
                 // the reader), so that a chunk with one vector at or above a
                 // later floor needs no second read of the logits
-                if (lane == fl) mvec[j * kWarps + warp] = j == 0 ? d[0] : (j == 1 ? d[1] : (j == 2 ? d[2] : d[3]));
+                if (lane == fl) mvec[j * kWarps + warp] = d[j];
             }
-            if (lane == 8 * j) {
+            if (lane == kSumLanes * j) {
                 ChunkEntry ce;
                 ce.m = mj[j];
                 ce.S = S;
@@ -591,7 +609,9 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
                 ch[j * kWarps + warp] = ce;
             }
         }
-        wm = fmaxf(fmaxf(mj[0], mj[1]), fmaxf(mj[2], mj[3]));
+        wm = mj[0];
+#pragma unroll
+        for (int j = 1; j < kVpt; ++j) wm = fmaxf(wm, mj[j]);
         wam = wm > -INFINITY ? kAmUnknown : -1;
     }
     if (bits & kRowArgmax) {
@@ -614,7 +634,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         if (wc != 0xFFFFFFFFu) {
             const int jw = static_cast<int>(wc >> 5), lw = static_cast<int>(wc & 31u);
             if (lane == lw) {
-                const uint4 dv = jw == 0 ? d[0] : (jw == 1 ? d[1] : (jw == 2 ? d[2] : d[3]));
+                const uint4 dv = pick(d, jw);
                 float z[VEC];
                 E::unpack(dv, z);
                 if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, jw * kThreads + tid, z);
@@ -924,7 +944,28 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     uint32_t err = st.err;
     Surv K{-INFINITY, INT_MAX};
     if (md.topk_on) {
-        K = select_topk(X, P.top_k, Km, err);
+        // every chunk max and every second vector max of a chunk is an id at or
+        // above itself: the k-th largest of them bounds the k-th largest logit
+        // from below and narrows the first histogram window
+        float zhint = -INFINITY;
+        if (isfinite(m)) {
+            const float* cu2 = reinterpret_cast<const float*>(dyn + a.cv2_off);
+            const int nch = a.s * kChunks;
+            uint32_t* fh = reinterpret_cast<uint32_t*>(KS.fb.lhist);
+            for (int b = tid; b < kFloorHistWords; b += kThreads) fh[b] = 0u;
+            __syncthreads();
+            float zh = -INFINITY;
+            floor_hist(2 * nch,
+                       [&](int e, float& x, uint32_t& w) {
+                           x = e < nch ? cm[e] : cu2[e - nch];
+                           w = (x > -INFINITY && x < INFINITY) ? 1u : 0u;
+                           if (w == 0u) x = m;
+                       },
+                       m, static_cast<uint32_t>(P.top_k), fh, zh);
+            zhint = zh;
+            __syncthreads();
+        }
+        K = select_topk(X, P.top_k, Km, err, zhint);
         st.kap_k = (K.zt == -INFINITY && K.ge_form()) ? 0u : fkey(K.zt);
         st.iot_k = K.ge_form() ? a.V : K.iota;
     }
