@@ -35,6 +35,7 @@ struct Plan {
     int cid_off = 0;
     int cv2_off = 0;
     int cmv_off = -1;
+    int cwide_off = -1;
     int clist_off = 0;
     int cand_off = 0;
     int sorted_off = 0;
@@ -143,8 +144,10 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     // the finish reads them from the logits)
     const int64_t cmv_raw = s * kChunks * 16;
     const int64_t cmv_bytes = cmv_raw <= 16384 ? r128(cmv_raw) : 0;
+    // and the wide entries of top-k rows with a large k, under the same bound
+    const int64_t cwide_bytes = cmv_bytes;
     const int64_t fin_smem =
-        cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch + cmv_bytes;
+        cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch + cmv_bytes + cwide_bytes;
     int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
     if (cluster) limit -= kSummaryBytes + static_cast<int64_t>(sizeof(ScanShared));
     if (fin_smem > limit || scan_smem > limit) {
@@ -166,10 +169,11 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     p.fb_wsum_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes);
     p.fb_patch_off = static_cast<int>(cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum);
     p.fb_rounds = static_cast<int>(fb_rounds);
-    p.cmv_off = cmv_bytes ? static_cast<int>(fin_smem - cmv_bytes) : -1;
+    p.cmv_off = cmv_bytes ? static_cast<int>(fin_smem - cmv_bytes - cwide_bytes) : -1;
+    p.cwide_off = cwide_bytes ? static_cast<int>(fin_smem - cwide_bytes) : -1;
     // every region holds 16-byte vectors or 8-byte words: starts must be 16-byte aligned
     for (const int off : {p.cs_off, p.cid_off, p.cv2_off, p.clist_off, p.cand_off, p.sorted_off,
-                          p.fb_wsum_off, p.fb_patch_off, p.cmv_off})
+                          p.fb_wsum_off, p.fb_patch_off, p.cmv_off, p.cwide_off})
         if (off >= 0 && off % 16 != 0) return ARC_E_UNSUPPORTED;
     p.fin_smem = static_cast<int>(fin_smem);
     p.slices = B * s;
@@ -424,6 +428,7 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.cid_off = p.cid_off;
     fa.cv2_off = p.cv2_off;
     fa.cmv_off = p.cmv_off;
+    fa.cwide_off = p.cwide_off;
     fa.clist_off = p.clist_off;
     fa.cand_off = p.cand_off;
     fa.sorted_off = p.sorted_off;

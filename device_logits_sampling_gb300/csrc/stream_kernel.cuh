@@ -34,11 +34,13 @@ constexpr int kVpt = 4;                  // 16-byte vectors per thread in a scan
 constexpr int kChunks = kVpt * kWarps;   // chunks per slice summary (32-vector chunks)
 constexpr int kHdrBytes = kWarps * 16;   // per-warp records of a slice
 constexpr int kEntryBytes = kChunks * 16;  // chunk entries of a slice
+constexpr int kWideK = 64;               // top-k rows with larger k record more per chunk (see WideEntry)
 // a slice summary: warp records, chunk entries, and (filtered rows) the raw
 // 16-byte vector holding each chunk's max
-constexpr int kSummaryBytes = kHdrBytes + 2 * kEntryBytes;
+constexpr int kSummaryBytes = kHdrBytes + 3 * kEntryBytes;
 constexpr int kMaxRowCtas = 128;         // slices per row at most
-constexpr int kCandCap = 1024;           // ids the direct selection holds
+constexpr int kCandCap = 2048;           // ids the direct selection holds
+constexpr int kRankMax = 256;            // candidates ranked by counting; more are sorted
 
 struct ScanArgs {
     const void* logits;
@@ -81,6 +83,7 @@ struct FinishArgs {
     int cid_off;       //   chunk max vectors,
     int cv2_off;       //   chunk second vector maxima,
     int cmv_off;       //   chunk max vectors (-1: read from the logits instead),
+    int cwide_off;     //   wide entries of top-k rows with large k (-1: none),
     int clist_off;     //   per-warp candidate chunk lists,
     int cand_off;      //   candidates (key, id, mass),
     int sorted_off;    //   the candidates in (key desc, id asc) order,
@@ -133,6 +136,18 @@ __device__ __forceinline__ const ChunkEntry* chunk_table(const unsigned char* sm
 }
 __device__ __forceinline__ const uint4* max_vectors(const unsigned char* sm) {
     return reinterpret_cast<const uint4*>(sm + kHdrBytes + kEntryBytes);
+}
+// Top-k rows with k > kWideK: the third and fourth largest vector maxima of a
+// chunk and the lanes of its second and third, so that the k-th largest of
+// the four maxima per chunk bounds the k-th logit from below and a chunk
+// whose fourth is below that floor is read as at most three known vectors.
+struct __align__(16) WideEntry {
+    float u3, u4;
+    int lane2, lane3;  // -1 when none
+};
+static_assert(sizeof(WideEntry) == 16, "wide entry size");
+__device__ __forceinline__ const WideEntry* wide_entries(const unsigned char* sm) {
+    return reinterpret_cast<const WideEntry*>(sm + kHdrBytes + 2 * kEntryBytes);
 }
 
 // weight of z relative to a reference max mr (chunk or row): ex2((z - mr) c);
@@ -586,7 +601,9 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         // chunk's mass): nothing per chunk stays live across the loop
         ChunkEntry* ch = reinterpret_cast<ChunkEntry*>(mysum + kHdrBytes);
         uint4* mvec = reinterpret_cast<uint4*>(mysum + kHdrBytes + kEntryBytes);
+        WideEntry* wide = reinterpret_cast<WideEntry*>(mysum + kHdrBytes + 2 * kEntryBytes);
         const bool filtered = (bits & kRowFiltered) != 0;
+        const bool wide_row = filtered && R.P.top_k > kWideK && R.P.top_k < a.V;
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) {
             int fl = -1;
@@ -607,6 +624,24 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
                 ce.lane = fl;
                 ce.u2 = u2;
                 ch[j * kWarps + warp] = ce;
+            }
+        }
+        if (wide_row) {
+            // per chunk: the vectors holding the largest and second largest
+            // maxima (by position), then the third and fourth largest maxima
+#pragma unroll
+            for (int j = 0; j < kVpt; ++j) {
+                const float x = xs[j];
+                const unsigned h1 = __ballot_sync(0xFFFFFFFFu, x == mj[j] && x > -INFINITY);
+                const int fl = h1 ? __ffs(h1) - 1 : -1;
+                const float u2 = warp_max_nonan(lane == fl ? -INFINITY : x);
+                const unsigned h2 = __ballot_sync(0xFFFFFFFFu, lane != fl && x == u2 && u2 > -INFINITY);
+                const int fl2 = h2 ? __ffs(h2) - 1 : -1;
+                const float u3 = warp_max_nonan((lane == fl || lane == fl2) ? -INFINITY : x);
+                const unsigned h3 = __ballot_sync(0xFFFFFFFFu, lane != fl && lane != fl2 && x == u3 && u3 > -INFINITY);
+                const int fl3 = h3 ? __ffs(h3) - 1 : -1;
+                const float u4 = warp_max_nonan((lane == fl || lane == fl2 || lane == fl3) ? -INFINITY : x);
+                if (lane == 0) wide[j * kWarps + warp] = WideEntry{u3, u4, fl2, fl3};
             }
         }
         wm = mj[0];
@@ -1214,6 +1249,114 @@ __device__ __noinline__ void top_n_row(const FinishArgs& a, int row, const arc_r
     for (int j = nc + tid; j < n; j += kThreads) out[j] = arc_top_logprob{-1, -INFINITY};
 }
 
+// The direct selection after the ranking, over the candidates in sorted order
+// (sk, sid, sm: keys, ids, fixed-point masses): K = the first nk, the top-p
+// cutoff, min-p, the survivors' mass and the draw in id order.  Thread t holds
+// sorted positions [POS t, POS t + POS): POS = 4 covers 1,024 candidates, 8
+// covers 2,048 (kept apart, so that the common case carries no extra work).
+template <int POS>
+__device__ __forceinline__ void sorted_select(const FinishArgs& a, const arc_row_params& P, const RowMode& md,
+                                              RowState& st, FinishScratch& SS, const uint32_t* sk, const int* sid,
+                                              const uint64_t* sm, int nk, float zm, const Surv& K) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        // thread t holds sorted positions [POS t, POS t + POS), read once as
+        // 16-byte vectors (kCandCap = POS kThreads: always inside the arrays)
+        static_assert(POS % 4 == 0 && POS * kThreads <= kCandCap, "sorted positions per thread");
+        const int p0 = POS * tid;
+        uint32_t tk[POS];
+        int ti[POS];
+        uint64_t tm[POS];
+#pragma unroll
+        for (int h = 0; h < POS / 4; ++h) {
+            const uint4 kv = reinterpret_cast<const uint4*>(sk)[(POS / 4) * tid + h];
+            const int4 iv = reinterpret_cast<const int4*>(sid)[(POS / 4) * tid + h];
+            const ulonglong2 m0 = reinterpret_cast<const ulonglong2*>(sm)[(POS / 2) * tid + 2 * h];
+            const ulonglong2 m1 = reinterpret_cast<const ulonglong2*>(sm)[(POS / 2) * tid + 2 * h + 1];
+            tk[4 * h] = kv.x, tk[4 * h + 1] = kv.y, tk[4 * h + 2] = kv.z, tk[4 * h + 3] = kv.w;
+            ti[4 * h] = iv.x, ti[4 * h + 1] = iv.y, ti[4 * h + 2] = iv.z, ti[4 * h + 3] = iv.w;
+            tm[4 * h] = m0.x, tm[4 * h + 1] = m0.y, tm[4 * h + 2] = m1.x, tm[4 * h + 3] = m1.y;
+        }
+        uint64_t lk = 0;
+#pragma unroll
+        for (int q = 0; q < POS; ++q) lk += (p0 + q < nk) ? tm[q] : 0u;
+        uint64_t tot_k;
+        // (the barrier after the ranking follows every earlier use of SS.redu)
+        const uint64_t inc_k = block_scan_u64(lk, SS.redu, tot_k, /*fresh=*/true);
+        st.mass_k = md.topk_on ? tot_k : st.S_all;
+        bool found = false;
+        float zp = -INFINITY;
+        if (md.topp_on) {
+            // first sorted position whose running mass reaches ceil(p * mass_k)
+            if (tid == 0)
+                SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(st.mass_k)));
+            __syncthreads();
+            const uint64_t tgt = max(SS.bu[5], uint64_t{1});
+            uint64_t run = inc_k - lk;
+            if (run < tgt && inc_k >= tgt) {
+#pragma unroll
+                for (int q = 0; q < POS; ++q) {
+                    const uint64_t mq = (p0 + q < nk) ? tm[q] : 0u;
+                    if (mq != 0 && run < tgt && run + mq >= tgt) SS.bi[5] = p0 + q;
+                    run += mq;
+                }
+            }
+            __syncthreads();
+            if (SS.bi[5] >= 0) {
+                found = true;
+                zp = key_to_float(sk[SS.bi[5]]);
+            }
+            if (!found && !md.minp_on && !md.topk_on) st.err |= kErrInternal;  // the floor guarantees it
+        }
+        const float zx = found ? fmaxf(zp, zm) : zm;
+        const Surv R = (zx > K.zt) ? Surv{zx, INT_MAX} : K;
+        st.kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
+        st.iot_r = R.ge_form() ? a.V : R.iota;
+        // survivors: a prefix [0, ns) of the sorted order
+        int nsv = nk;
+        if (!(zx > K.zt)) {
+            // R is K: its positions are [0, nk) and its mass the scan's total
+            st.mass_r = tot_k;
+        } else {
+            // the survivors' mass and their count, in one reduction
+            uint64_t lr = 0;
+            int first_out = nk;
+#pragma unroll
+            for (int q = POS - 1; q >= 0; --q) {
+                const int pp = p0 + q;
+                if (pp < nk) {
+                    if (R.test(key_to_float(tk[q]), ti[q]))
+                        lr += tm[q];
+                    else
+                        first_out = pp;
+                }
+            }
+            lr = warp_sum_u64(lr);
+            first_out = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, static_cast<unsigned>(first_out)));
+            if (lane == 0) {
+                SS.fc[1][warp][0] = static_cast<uint32_t>(lr);
+                SS.fc[1][warp][1] = static_cast<uint32_t>(lr >> 32);
+                SS.fc[1][warp][2] = static_cast<uint32_t>(first_out);
+            }
+            __syncthreads();
+            uint64_t mr = 0;
+            for (int v = 0; v < kWarps; ++v) {
+                mr += (static_cast<uint64_t>(SS.fc[1][v][1]) << 32) | SS.fc[1][v][0];
+                nsv = min(nsv, static_cast<int>(SS.fc[1][v][2]));
+            }
+            st.mass_r = mr;
+        }
+        st.target = scale_by_u(st.rbits, st.mass_r);
+        // the draw in id order: each survivor sums the survivors with smaller ids
+        for (int pp = tid; pp < nsv; pp += kThreads) {
+            const int ip = sid[pp];
+            const uint64_t mp = sm[pp];
+            uint64_t before = 0;
+#pragma unroll 8
+            for (int qq = 0; qq < nsv; ++qq) before += (sid[qq] < ip) ? sm[qq] : 0u;
+            if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
+        }
+}
+
 // One row's finish by one CTA.  sum_at(c) is slice c's summary (the
 // workspace, or another CTA's shared memory in the cluster kernel); wait()
 // returns once every summary of the row is complete and visible; loaded()
@@ -1253,6 +1396,9 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
         tl = static_cast<double>(P.temperature) * log(static_cast<double>(P.min_p));
     // the finish needs the chunk max vectors (filtered rows)
     const bool want_mv = a.cmv_off >= 0 && param_errors(P) == 0 && (RowMode(P, a.V).filtered || a.top_n > 0);
+    // a top-k row with a large k: the wide entries too
+    const bool want_wide = want_mv && a.cwide_off >= 0 && RowMode(P, a.V).filtered && P.top_k > kWideK &&
+                           P.top_k < a.V;
     // the summaries are complete and visible after this (the parameters and
     // history above are not written by the scan)
     wait();
@@ -1299,6 +1445,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
         for (int g0 = tid - 32; g0 < nch; g0 += kLd * kStride) {
             ChunkEntry e[kLd];
             uint4 mv[kLd];
+            WideEntry we[kLd];
 #pragma unroll
             for (int u = 0; u < kLd; ++u) {
                 const int gi = g0 + u * kStride;
@@ -1306,6 +1453,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                     const unsigned char* sm = sum_at(gi / kChunks);
                     e[u] = chunk_table(sm)[gi % kChunks];
                     if (want_mv) mv[u] = max_vectors(sm)[gi % kChunks];
+                    if (want_wide) we[u] = wide_entries(sm)[gi % kChunks];
                 }
             }
 #pragma unroll
@@ -1317,6 +1465,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                     cln[gi] = e[u].lane;
                     cu2[gi] = e[u].u2;
                     if (want_mv) reinterpret_cast<uint4*>(dyn + a.cmv_off)[gi] = mv[u];
+                    if (want_wide) reinterpret_cast<WideEntry*>(dyn + a.cwide_off)[gi] = we[u];
                 }
             }
         }
@@ -1548,17 +1697,31 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                     return !(x > -INFINITY) ? 0u
                                             : (md.topk_on ? 1u : static_cast<uint32_t>(fixq(wrel(x, m, cT)) >> sh));
                 };
+                // wide top-k rows: the four largest vector maxima of every chunk
+                // (distinct ids), so that a k beyond the chunk count still has a floor
+                const int nv_floor = want_wide ? 4 * nch : nch;
+                const WideEntry* cw = reinterpret_cast<const WideEntry*>(dyn + a.cwide_off);
+                auto val = [&](int e) -> float {
+                    if (e < nch) return cm[e];
+                    if (e < 2 * nch) return cu2[e - nch];
+                    return e < 3 * nch ? cw[e - 2 * nch].u3 : cw[e - 3 * nch].u4;
+                };
                 fast = isfinite(m) &&
-                       floor_hist(nch, [&](int e, float& x, uint32_t& w) { x = cm[e]; w = wt(x); }, m, tgt,
-                                  reinterpret_cast<uint32_t*>(KS.fb.lhist), zf);
+                       floor_hist(nv_floor,
+                                  [&](int e, float& x, uint32_t& w) {
+                                      x = val(e);
+                                      w = (x < INFINITY) ? wt(x) : 0u;
+                                      if (w == 0u) x = m;
+                                  },
+                                  m, tgt, reinterpret_cast<uint32_t*>(KS.fb.lhist), zf);
                 if (!fast) {
                     auto kw = [&](int e, uint32_t& key, uint32_t& w) {
-                        const float x = cm[e];
-                        key = fkey(x);
-                        w = wt(x);
+                        const float x = val(e);
+                        key = fkey(x < INFINITY ? x : -INFINITY);
+                        w = (x < INFINITY) ? wt(x) : 0u;
                     };
                     uint32_t edge = 0;
-                    fast = floor_block(nch, kw, tgt, SS, edge);
+                    fast = floor_block(nv_floor, kw, tgt, SS, edge);
                     if (fast) zf = Ctx::lo_float(edge);
                 }
             } else {
@@ -1600,10 +1763,36 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                         }
                     }
                 };
+                const WideEntry* cw = reinterpret_cast<const WideEntry*>(dyn + a.cwide_off);
                 for (int g = ce0; g < ce1; ++g) {
                     if (!(cm[g] >= zf)) continue;
                     const int c = g / kChunks;
-                    if (cu2[g] < zf && cln[g] >= 0) {
+                    if (want_wide && cu2[g] >= zf && cw[g].u4 < zf && cln[g] >= 0) {
+                        // at most three vectors hold ids >= zf: the max's (from the
+                        // summary), the second's and, when its max reaches zf, the third's
+                        const WideEntry wg = cw[g];
+                        const int sn = min((c + 1) * a.L, a.V) - c * a.L;
+                        const char* sb = rowp + static_cast<int64_t>(c) * a.L * E::kBytes;
+                        const int vb = (g % kChunks) * 32;
+                        const int v1 = vb + cln[g], v2 = vb + wg.lane2, v3 = wg.u3 >= zf ? vb + wg.lane3 : -1;
+                        uint4 r1 = want_mv ? reinterpret_cast<const uint4*>(dyn + a.cmv_off)[g]
+                                           : E::global_vec(sb, v1, sn, a.aligned);
+                        const uint4 r2 = E::global_vec(sb, v2, sn, a.aligned);
+                        uint4 r3 = r2;
+                        if (v3 >= vb) r3 = E::global_vec(sb, v3, sn, a.aligned);
+                        float z[VEC];
+                        E::unpack(r1, z);
+                        if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, c * Lv + v1, z);
+                        emit(z, c * Lv + v1);
+                        E::unpack(r2, z);
+                        if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, c * Lv + v2, z);
+                        emit(z, c * Lv + v2);
+                        if (v3 >= vb) {
+                            E::unpack(r3, z);
+                            if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, c * Lv + v3, z);
+                            emit(z, c * Lv + v3);
+                        }
+                    } else if (cu2[g] < zf && cln[g] >= 0) {
                         const int vs = (g % kChunks) * 32 + cln[g];
                         const int sn = min((c + 1) * a.L, a.V) - c * a.L;
                         float z[VEC];
@@ -1666,19 +1855,48 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
 
             if (fast) {
                 // ------------------------------------------------------ direct selection
-                // rank every candidate by (key desc, id asc) into sorted arrays
+                // every candidate in (key desc, id asc) order into sorted arrays:
+                // few are ranked by counting, more by a bitonic sort of the
+                // 64-bit values (padded with zeros, which rank last)
                 uint32_t* sk = reinterpret_cast<uint32_t*>(dyn + a.sorted_off);
                 int* sid = reinterpret_cast<int*>(sk + kCandCap);
                 uint64_t* sm = reinterpret_cast<uint64_t*>(sid + kCandCap);
-                for (int i = tid; i < nc; i += kThreads) {
-                    const uint64_t vi = cc[i];
-                    int rk = 0;
+                if (nc <= kRankMax) {
+                    for (int i = tid; i < nc; i += kThreads) {
+                        const uint64_t vi = cc[i];
+                        int rk = 0;
 #pragma unroll 8
-                    for (int j = 0; j < nc; ++j) rk += (cc[j] > vi) ? 1 : 0;
-                    const uint32_t ki = static_cast<uint32_t>(vi >> 32);
-                    sk[rk] = ki;
-                    sid[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(vi));
-                    sm[rk] = fixq(weight_of(key_to_float(ki)));
+                        for (int j = 0; j < nc; ++j) rk += (cc[j] > vi) ? 1 : 0;
+                        const uint32_t ki = static_cast<uint32_t>(vi >> 32);
+                        sk[rk] = ki;
+                        sid[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(vi));
+                        sm[rk] = fixq(weight_of(key_to_float(ki)));
+                    }
+                } else {
+                    int n2 = kRankMax;
+                    while (n2 < nc) n2 <<= 1;
+                    for (int i = nc + tid; i < n2; i += kThreads) cc[i] = 0;
+                    __syncthreads();
+                    for (int size = 2; size <= n2; size <<= 1) {
+                        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                            for (int i = tid; i < (n2 >> 1); i += kThreads) {
+                                const int lo = (i / stride) * 2 * stride + (i % stride), hi = lo + stride;
+                                const uint64_t x = cc[lo], y = cc[hi];
+                                if ((x < y) == ((lo & size) == 0)) {  // descending where lo & size == 0
+                                    cc[lo] = y;
+                                    cc[hi] = x;
+                                }
+                            }
+                            __syncthreads();
+                        }
+                    }
+                    for (int i = tid; i < nc; i += kThreads) {
+                        const uint64_t vi = cc[i];
+                        const uint32_t ki = static_cast<uint32_t>(vi >> 32);
+                        sk[i] = ki;
+                        sid[i] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(vi));
+                        sm[i] = fixq(weight_of(key_to_float(ki)));
+                    }
                 }
                 if (tid == 0) {
                     SS.bi[5] = -1;
@@ -1718,101 +1936,10 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                         st.target = target;
                     }
                 } else {
-                    // thread t holds sorted positions [4t, 4t + 4), read once as 16-byte
-                    // vectors (kCandCap = 4 kThreads: always inside the arrays)
-                    const int p0 = 4 * tid;
-                    uint32_t tk[4];
-                    int ti[4];
-                    uint64_t tm[4];
-                    {
-                        const uint4 kv = reinterpret_cast<const uint4*>(sk)[tid];
-                        const int4 iv = reinterpret_cast<const int4*>(sid)[tid];
-                        const ulonglong2 m0 = reinterpret_cast<const ulonglong2*>(sm)[2 * tid];
-                        const ulonglong2 m1 = reinterpret_cast<const ulonglong2*>(sm)[2 * tid + 1];
-                        tk[0] = kv.x, tk[1] = kv.y, tk[2] = kv.z, tk[3] = kv.w;
-                        ti[0] = iv.x, ti[1] = iv.y, ti[2] = iv.z, ti[3] = iv.w;
-                        tm[0] = m0.x, tm[1] = m0.y, tm[2] = m1.x, tm[3] = m1.y;
-                    }
-                    static_assert(kCandCap == 4 * kThreads, "four sorted positions per thread");
-                    uint64_t lk = 0;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) lk += (p0 + q < nk) ? tm[q] : 0u;
-                    uint64_t tot_k;
-                    // (the barrier after the ranking follows every earlier use of SS.redu)
-                    const uint64_t inc_k = block_scan_u64(lk, SS.redu, tot_k, /*fresh=*/true);
-                    st.mass_k = md.topk_on ? tot_k : st.S_all;
-                    bool found = false;
-                    float zp = -INFINITY;
-                    if (md.topp_on) {
-                        // first sorted position whose running mass reaches ceil(p * mass_k)
-                        if (tid == 0)
-                            SS.bu[5] = static_cast<uint64_t>(ceil(static_cast<double>(P.top_p) * static_cast<double>(st.mass_k)));
-                        __syncthreads();
-                        const uint64_t tgt = max(SS.bu[5], uint64_t{1});
-                        uint64_t run = inc_k - lk;
-                        if (run < tgt && inc_k >= tgt) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const uint64_t mq = (p0 + q < nk) ? tm[q] : 0u;
-                                if (mq != 0 && run < tgt && run + mq >= tgt) SS.bi[5] = p0 + q;
-                                run += mq;
-                            }
-                        }
-                        __syncthreads();
-                        if (SS.bi[5] >= 0) {
-                            found = true;
-                            zp = key_to_float(sk[SS.bi[5]]);
-                        }
-                        if (!found && !md.minp_on && !md.topk_on) st.err |= kErrInternal;  // the floor guarantees it
-                    }
-                    const float zx = found ? fmaxf(zp, zm) : zm;
-                    const Surv R = (zx > K.zt) ? Surv{zx, INT_MAX} : K;
-                    st.kap_r = (R.zt == -INFINITY && R.ge_form()) ? 0u : fkey(R.zt);
-                    st.iot_r = R.ge_form() ? a.V : R.iota;
-                    // survivors: a prefix [0, ns) of the sorted order
-                    int nsv = nk;
-                    if (!(zx > K.zt)) {
-                        // R is K: its positions are [0, nk) and its mass the scan's total
-                        st.mass_r = tot_k;
-                    } else {
-                        // the survivors' mass and their count, in one reduction
-                        uint64_t lr = 0;
-                        int first_out = nk;
-#pragma unroll
-                        for (int q = 3; q >= 0; --q) {
-                            const int pp = p0 + q;
-                            if (pp < nk) {
-                                if (R.test(key_to_float(tk[q]), ti[q]))
-                                    lr += tm[q];
-                                else
-                                    first_out = pp;
-                            }
-                        }
-                        lr = warp_sum_u64(lr);
-                        first_out = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, static_cast<unsigned>(first_out)));
-                        if (lane == 0) {
-                            SS.fc[1][warp][0] = static_cast<uint32_t>(lr);
-                            SS.fc[1][warp][1] = static_cast<uint32_t>(lr >> 32);
-                            SS.fc[1][warp][2] = static_cast<uint32_t>(first_out);
-                        }
-                        __syncthreads();
-                        uint64_t mr = 0;
-                        for (int v = 0; v < kWarps; ++v) {
-                            mr += (static_cast<uint64_t>(SS.fc[1][v][1]) << 32) | SS.fc[1][v][0];
-                            nsv = min(nsv, static_cast<int>(SS.fc[1][v][2]));
-                        }
-                        st.mass_r = mr;
-                    }
-                    st.target = scale_by_u(st.rbits, st.mass_r);
-                    // the draw in id order: each survivor sums the survivors with smaller ids
-                    for (int pp = tid; pp < nsv; pp += kThreads) {
-                        const int ip = sid[pp];
-                        const uint64_t mp = sm[pp];
-                        uint64_t before = 0;
-#pragma unroll 8
-                        for (int qq = 0; qq < nsv; ++qq) before += (sid[qq] < ip) ? sm[qq] : 0u;
-                        if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
-                    }
+                    if (nc <= 4 * kThreads)
+                        sorted_select<4>(a, P, md, st, SS, sk, sid, sm, nk, zm, K);
+                    else
+                        sorted_select<8>(a, P, md, st, SS, sk, sid, sm, nk, zm, K);
                 }
                 __syncthreads();
                 st.token = SS.bi[6];

@@ -63,16 +63,16 @@ def _largest_accepted(S, V, dtype):
 
 
 def test_static_limits_are_the_documented_ones():
-    # B x slices-per-row x 1,152 B <= 16 MiB: 16 bf16 slices or 32 fp32 slices
+    # B x slices-per-row x 1,664 B <= 16 MiB: 16 bf16 slices or 32 fp32 slices
     # per row at V = 129,280 (host-only planning, no GPU)
     S = sampler
     S.load()
-    assert _largest_accepted(S, 129_280, workloads.DTYPE_BF16) == 910
-    assert _largest_accepted(S, 129_280, workloads.DTYPE_F32) == 455
+    assert _largest_accepted(S, 129_280, workloads.DTYPE_BF16) == 630
+    assert _largest_accepted(S, 129_280, workloads.DTYPE_F32) == 315
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("dtype,B_max", [(workloads.DTYPE_BF16, 910), (workloads.DTYPE_F32, 455)])
+@pytest.mark.parametrize("dtype,B_max", [(workloads.DTYPE_BF16, 630), (workloads.DTYPE_F32, 315)])
 def test_static_at_its_limit_and_one_past_it(cuda_lib, dtype, B_max):
     """The largest accepted batch matches arc_sample_batch token for token; one
     more row is refused with nothing enqueued."""
