@@ -338,6 +338,22 @@ CONFIGS = [  # the five synthetic workloads, in the order of the configuration l
 ]
 
 
+def bench_only_config(args) -> None:
+    """--only-config NAME: one synthetic workload's record (for profiling one
+    configuration's kernels), K steps, one timed region."""
+    import torch
+
+    from device_logits_sampling_gb300 import sampler, workloads
+
+    torch.cuda.set_device(0)
+    sampler.load()
+    peak = measured_peaks().get("hbm_gbs") or 6800.0
+    kw = {"greedy": True} if args.only_config == "single_row_peaked_greedy" else {}
+    name = "single_row_peaked" if args.only_config.startswith("single_row_peaked") else args.only_config
+    key, rec = bench_config(sampler, workloads, (name, kw), peak, max(1, args.steps), max(1, args.repeats))
+    print(json.dumps({"workload": key, **rec}))
+
+
 def bench_gpu(args) -> None:
     import numpy as np
     import torch
@@ -585,11 +601,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' figures")
     ap.add_argument("--repeats", type=int, default=5, help="timed regions of K steps (median and min reported)")
+    ap.add_argument("--only-config", default=None,
+                    help="time one synthetic workload only (small_fp32, single_row_peaked[_greedy], mixed_batch, "
+                         "penalized_batch, adversarial_ties) and print its record")
     ap.add_argument("--decode-loop", action="store_true", help="time the decode-loop commit (separate JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.decode_loop:
+    if args.only_config:
+        bench_only_config(args)
+    elif args.decode_loop:
         bench_decode_loop(args)
     elif args.impl == "reference":
         bench_reference(args)
