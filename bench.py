@@ -526,8 +526,10 @@ def bench_decode_loop(args) -> None:
     """--decode-loop: the decode step after sampling (arc_decode_commit into a
     pinned host ring).  Times, with CUDA events over graph replays on the
     mixed B=256 batch, one step of sampling alone, one step of sampling
-    followed by the commit, and the commit alone; the host drains every
-    record of the timed replays afterwards and checks their count and owners."""
+    followed by the commit kernel, the commit kernel alone, and sampling with
+    the commit folded into its finish (arc_sample_batch_commit); the host
+    drains every record of the timed replays afterwards and checks their
+    count and owners."""
     import numpy as np
     import torch
 
@@ -542,10 +544,10 @@ def bench_decode_loop(args) -> None:
     ids = torch.zeros(B, dtype=torch.int32, device="cuda")
     pos = torch.zeros(B, dtype=torch.int32, device="cuda")
     owners = torch.arange(B, dtype=torch.int32, device="cuda")
-    head = torch.zeros(1, dtype=torch.int64, device="cuda")
+    head = torch.zeros(2, dtype=torch.int64, device="cuda")  # [1]: the folded commit's arrival count
     fault = torch.zeros(1, dtype=torch.int32, device="cuda")
     n = max(1, args.steps)
-    ring = decode.Ring(B * (n * 3 + args.warmup * 3 + 8))
+    ring = decode.Ring(B * (n * 4 + args.warmup * 4 + 8))
     s = torch.cuda.Stream()
 
     def timed(fn):
@@ -571,23 +573,30 @@ def bench_decode_loop(args) -> None:
         sampler.sample_batch(bufs[i], prm, out, workspace=ws, autoinc=True, stream=s)
 
     def commit():
-        decode.decode_commit(out, ids, pos, 1 << 30, V, ring, head, owners=owners, fault_word=fault, stream=s)
+        decode.decode_commit(out, ids, pos, 1 << 30, V, ring, head[:1], owners=owners, fault_word=fault, stream=s)
 
     def both(i):
         sample(i)
         commit()
 
+    def folded(i):
+        decode.sample_and_commit(bufs[i], prm, out, ids, pos, 1 << 30, ring, head, owners=owners, fault_word=fault,
+                                 workspace=ws, autoinc=True, stream=s)
+
     t_sample = timed(sample)
     t_both = timed(both)
     t_commit = timed(lambda i: commit())
-    published = int(head.item())
+    t_folded = timed(folded)
+    published = int(head[0].item())
+    assert int(head[1].item()) == 0
     recs = ring.drain(published, max_spins=1 << 20)
     assert len(recs) == published and int(fault.item()) == 0
     assert np.array_equal(recs["owner"], np.tile(np.arange(B), published // B))
     print(json.dumps({
         "metric": "decode step after sampling: sample + commit into a pinned host ring", "unit": "us",
         "B": B, "V": V, "sample_us": t_sample, "sample_and_commit_us": t_both, "commit_alone_us": t_commit,
-        "commit_added_us": t_both - t_sample, "records_drained": published, "higher_is_better": False,
+        "commit_added_us": t_both - t_sample, "sample_with_folded_commit_us": t_folded,
+        "folded_commit_added_us": t_folded - t_sample, "records_drained": published, "higher_is_better": False,
     }))
     ring.close()
 

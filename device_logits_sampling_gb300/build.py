@@ -1,7 +1,9 @@
 """Build the sampling library in-tree for sm_103a (GB300).
 
-Produces device_logits_sampling_gb300/_lib/libarcsample.so from csrc/ with
-one nvcc invocation.  Runs on any host with nvcc (no GPU needed).
+Produces device_logits_sampling_gb300/_lib/libarcsample.so from csrc/: one
+nvcc process per translation unit, all at once (the four kernel sets
+dominate the build), then one link.  Runs on any host with nvcc (no GPU
+needed).
 """
 from __future__ import annotations
 
@@ -16,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libarcsample.so")
-SOURCES = [os.path.join(CSRC, "arc_sample.cu"), os.path.join(CSRC, "arc_decode.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("kernels_bf16.cu", "kernels_bf16_hist.cu", "kernels_f32.cu",
+                                            "kernels_f32_hist.cu", "arc_sample.cu", "arc_decode.cu")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,20 +33,33 @@ def nvcc_path() -> str:
 def build(verbose: bool = False, extra: list[str] | None = None, out: str | None = None) -> str:
     os.makedirs(LIBDIR, exist_ok=True)
     target = out or LIB
-    cmd = [
-        nvcc_path(), *ARCH, "-O3", "-std=c++17", "-lineinfo",
-        "-Xcompiler", "-fPIC", "-shared", "-I", INCLUDE, "-I", CSRC,
-        "-Xptxas", "-v" if verbose else "-O3",
-        *(extra or []),
-        "-o", target + ".tmp", *SOURCES,
-    ]
-    res = subprocess.run(cmd, capture_output=True, text=True)
+    objdir = target + ".obj"
+    os.makedirs(objdir, exist_ok=True)
+    nvcc = nvcc_path()
+    common = [*ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
+              "-Xptxas", "-v" if verbose else "-O3", *(extra or [])]
+    jobs = []
+    for src in SOURCES:
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
+        cmd = [nvcc, *common, "-c", "-o", obj, src]
+        jobs.append((cmd, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)))
+    failed = None
+    for cmd, _, proc in jobs:
+        so, se = proc.communicate()
+        if proc.returncode != 0 and failed is None:
+            failed = (proc.returncode, cmd, so + se)
+        elif verbose:
+            sys.stderr.write(se)
+    if failed is not None:
+        sys.stderr.write(failed[2])
+        raise RuntimeError(f"nvcc failed ({failed[0]}): {' '.join(failed[1])}")
+    link = [nvcc, *ARCH, "-shared", "-o", target + ".tmp", *[obj for _, obj, _ in jobs]]
+    res = subprocess.run(link, capture_output=True, text=True)
     if res.returncode != 0:
         sys.stderr.write(res.stdout + res.stderr)
-        raise RuntimeError(f"nvcc failed ({res.returncode}): {' '.join(cmd)}")
-    if verbose:
-        sys.stderr.write(res.stderr)
+        raise RuntimeError(f"nvcc link failed ({res.returncode}): {' '.join(link)}")
     os.replace(target + ".tmp", target)
+    shutil.rmtree(objdir, ignore_errors=True)
     return target
 
 

@@ -7,11 +7,11 @@
 
 #include "arc_decode.h"
 #include "arc_sample.h"
+#include "commit_row.cuh"
 
 namespace {
 
 constexpr int kCommitThreads = 1024;
-constexpr uint32_t kMaxCapacity = 1u << 30;  // the "writing" stamp (two laps back) stays unambiguous
 
 struct CommitArgs {
     const int32_t* tokens;
@@ -27,49 +27,14 @@ struct CommitArgs {
     uint32_t* fault_word;
 };
 
-// System-scope release store of a record's stamp: the record's other fields,
-// stored before it by this thread, are visible to a host that reads the
-// stamp with acquire semantics.
-__device__ __forceinline__ void store_release_sys(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void store_relaxed_sys(uint32_t* p, uint32_t v) {
-    asm volatile("st.relaxed.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Orders this thread's earlier stores before its later ones for every
-// observer, the host included.
-__device__ __forceinline__ void fence_acq_rel_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
-
 // One CTA: every row of the step, then the ring head.  The range checks come
 // before any write of the row; a refused row publishes a record with token -1.
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_constant__ CommitArgs a) {
     const uint64_t head = *a.head;  // read by every thread before thread 0 advances it
     uint32_t faults = 0;
-    for (int64_t r = threadIdx.x; r < a.B; r += kCommitThreads) {
-        const int32_t tok = a.tokens[r];
-        const int32_t pos = a.positions[r];
-        uint32_t bad = 0;
-        if (tok < 0 || tok >= a.V) bad |= ARC_COMMIT_BAD_TOKEN;
-        if (pos < 0 || pos >= a.max_position) bad |= ARC_COMMIT_BAD_POSITION;
-        if (bad == 0) {
-            a.next_ids[r] = tok;
-            a.positions[r] = pos + 1;
-        }
-        faults |= bad;
-        const uint64_t idx = head + static_cast<uint64_t>(r);
-        arc_commit_record* rec = a.ring + (idx % a.capacity);
-        // a slot being rewritten first carries a "writing" stamp, two laps
-        // behind the new record (matches no record a reader can be waiting
-        // for, and reads as behind rather than as an overrun), so a host copy
-        // taken while the fields change is never confirmed by its second
-        // stamp read
-        store_relaxed_sys(&rec->stamp, static_cast<uint32_t>(idx + 1 - 2 * static_cast<uint64_t>(a.capacity)));
-        fence_acq_rel_sys();
-        rec->token = bad ? -1 : tok;
-        rec->position = pos;
-        rec->owner = a.owners ? a.owners[r] : 0u;
-        store_release_sys(&rec->stamp, static_cast<uint32_t>(idx + 1));
-    }
+    for (int64_t r = threadIdx.x; r < a.B; r += kCommitThreads)
+        faults |= arc::commit_row(a.tokens[r], r, head + static_cast<uint64_t>(r), a.V, a.next_ids, a.positions,
+                                  a.max_position, a.owners, a.ring, a.capacity);
     if (faults && a.fault_word) atomicOr(a.fault_word, faults);
     __syncthreads();  // every thread has read *head
     if (threadIdx.x == 0) *a.head = head + static_cast<uint64_t>(a.B);
@@ -87,7 +52,7 @@ int arc_decode_commit(const int32_t* tokens, int64_t B, int32_t V, int32_t* next
         head == nullptr)
         return ARC_E_NULL;
     if (B <= 0 || V <= 0 || max_position <= 0 || capacity == 0 || static_cast<uint64_t>(B) > capacity ||
-        capacity > kMaxCapacity)
+        capacity > ARC_RING_MAX_CAPACITY)
         return ARC_E_SHAPE;
     CommitArgs a{tokens, B, V, next_ids, positions, max_position, owners, ring, capacity, head, fault_word};
     commit_kernel<<<1, kCommitThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);

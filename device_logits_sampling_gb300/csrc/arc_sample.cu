@@ -13,14 +13,14 @@
 #include "arc_decode.h"
 #include "arc_sample.h"
 #include "argmax_kernel.cuh"
-#include "stream_kernel.cuh"
+#include "kernel_set.cuh"
+#include "launch_util.cuh"
 
 namespace {
 
 using namespace arc;
 
 constexpr int kMaxDevices = 64;
-constexpr int kSmemPerBlock = 232448;         // 227 KB opt-in limit of sm_100-class GPUs
 constexpr int kDefaultHist = 1024;  // history capacity when max_hist_len is 0
 constexpr int kAssumedSMs = 152;
 
@@ -193,89 +193,6 @@ int num_sms_of(int dev) {
     return v;
 }
 
-// Function attributes are set once per (device, kernel): the first call on a
-// device must come before any stream capture that contains a call.
-// `carveout` is the preferred shared-memory share of the SM's L1/shared
-// storage in percent: 0 for the streaming kernels, which use (almost) no
-// shared memory and keep more loads in flight with a larger L1, 100 for
-// the kernels that stage rows or penalty tables in shared memory.
-template <class K>
-cudaError_t prepare(K kernel, int dev, std::atomic<uint64_t>& done, int carveout) {
-    const uint64_t bit = uint64_t{1} << (dev & 63);
-    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    // the largest dynamic shared memory a CTA of this kernel can have next to
-    // its static shared memory
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemPerBlock - static_cast<int>(fa.sharedSizeBytes));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();  // a refused attribute must not surface as a later launch error
-        return e;
-    }
-    done.fetch_or(bit, std::memory_order_acq_rel);
-    return cudaSuccess;
-}
-
-template <class K, class A>
-cudaError_t launch_cluster(K kernel, int64_t grid, int s, int smem, cudaStream_t st, const A& args,
-                           bool early = false) {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    // early: the kernel may start before the previous kernel on the stream has
-    // finished (programmatic dependent launch); it waits for that kernel's
-    // results with griddepcontrol.wait before reading them
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = early ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args);
-}
-
-// Whether a cluster launch of this kernel and shape fits the device (cached;
-// asked once per device, kernel, cluster size and shared-memory size).
-template <class K>
-bool cluster_fits(K kernel, int dev, int dt, bool hist, int s, int smem) {
-    static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int, int>, bool> known;
-    const auto key = std::make_tuple(dev, dt, hist ? 1 : 0, s, smem);
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = known.find(key);
-    if (it != known.end()) return it->second;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(s), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    const bool ok = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n >= 1;
-    if (!ok) (void)cudaGetLastError();
-    known[key] = ok;
-    return ok;
-}
-
-std::atomic<uint64_t> g_prep_scan[2][2];
-std::atomic<uint64_t> g_prep_cluster[2][2];
-std::atomic<uint64_t> g_prep_fin[2][2];
 std::atomic<uint64_t> g_prep_argmax[2];
 
 // Scratch of arc_sample_batch_static, for callers that cannot allocate device
@@ -347,9 +264,16 @@ size_t arc_sample_workspace_bytes(int64_t B, int64_t V, int32_t dtype, int32_t h
     return p.ws_bytes;
 }
 
-int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype, arc_row_params* params,
-                     const int32_t* hist_offsets, const int32_t* hist_ids, int32_t* out, uint32_t* err_word,
-                     void* workspace, size_t workspace_bytes, const arc_sample_options* opts, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// arc_sample_batch, with each row's decode-loop commit folded into its finish
+// when `commit` is given (arc_sample_batch_commit).
+int sample_impl(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype, arc_row_params* params,
+                const int32_t* hist_offsets, const int32_t* hist_ids, int32_t* out, uint32_t* err_word,
+                void* workspace, size_t workspace_bytes, const arc_sample_options* opts,
+                const arc_commit_target* commit, void* stream) {
     int rc = check_common(logits, B, V, ld, dtype, out);
     if (rc != ARC_OK) return rc;
     if (params == nullptr) return ARC_E_NULL;
@@ -371,15 +295,11 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
         const int dyn = std::max(p.scan_smem, p.fin_smem);
         bool fits;
         if (dtype == ARC_BF16)
-            fits = has_hist ? prepare(cluster_kernel<ARC_BF16, true>, dev, g_prep_cluster[1][1], 100) == cudaSuccess &&
-                                  cluster_fits(cluster_kernel<ARC_BF16, true>, dev, 1, true, p.s, dyn)
-                            : prepare(cluster_kernel<ARC_BF16, false>, dev, g_prep_cluster[1][0], 100) == cudaSuccess &&
-                                  cluster_fits(cluster_kernel<ARC_BF16, false>, dev, 1, false, p.s, dyn);
+            fits = has_hist ? KernelSet<ARC_BF16, true>::cluster_ok(p.s, dyn, dev)
+                            : KernelSet<ARC_BF16, false>::cluster_ok(p.s, dyn, dev);
         else
-            fits = has_hist ? prepare(cluster_kernel<ARC_F32, true>, dev, g_prep_cluster[0][1], 100) == cudaSuccess &&
-                                  cluster_fits(cluster_kernel<ARC_F32, true>, dev, 0, true, p.s, dyn)
-                            : prepare(cluster_kernel<ARC_F32, false>, dev, g_prep_cluster[0][0], 100) == cudaSuccess &&
-                                  cluster_fits(cluster_kernel<ARC_F32, false>, dev, 0, false, p.s, dyn);
+            fits = has_hist ? KernelSet<ARC_F32, true>::cluster_ok(p.s, dyn, dev)
+                            : KernelSet<ARC_F32, false>::cluster_ok(p.s, dyn, dev);
         if (!fits) {
             rc = make_plan(B, V, dtype, has_hist, opts, num_sms_of(dev), p, false);
             if (rc != ARC_OK) return rc;
@@ -435,40 +355,53 @@ int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32
     fa.fb_wsum_off = p.fb_wsum_off;
     fa.fb_patch_off = p.fb_patch_off;
     fa.fb_rounds = p.fb_rounds;
+    fa.commit = commit ? *commit : arc_commit_target{};
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
     if (p.cluster) {
         const FusedArgs fu{sa, fa};
         const int dyn = std::max(p.scan_smem, p.fin_smem);
-        cudaError_t e;
         if (dtype == ARC_BF16)
-            e = has_hist ? launch_cluster(cluster_kernel<ARC_BF16, true>, B * p.s, p.s, dyn, st, fu)
-                         : launch_cluster(cluster_kernel<ARC_BF16, false>, B * p.s, p.s, dyn, st, fu);
+            e = has_hist ? KernelSet<ARC_BF16, true>::launch_fused(fu, B, p.s, dyn, st)
+                         : KernelSet<ARC_BF16, false>::launch_fused(fu, B, p.s, dyn, st);
         else
-            e = has_hist ? launch_cluster(cluster_kernel<ARC_F32, true>, B * p.s, p.s, dyn, st, fu)
-                         : launch_cluster(cluster_kernel<ARC_F32, false>, B * p.s, p.s, dyn, st, fu);
-        return e == cudaSuccess ? ARC_OK : ARC_E_CUDA;
+            e = has_hist ? KernelSet<ARC_F32, true>::launch_fused(fu, B, p.s, dyn, st)
+                         : KernelSet<ARC_F32, false>::launch_fused(fu, B, p.s, dyn, st);
+    } else if (dtype == ARC_BF16) {
+        e = has_hist ? KernelSet<ARC_BF16, true>::launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st)
+                     : KernelSet<ARC_BF16, false>::launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st);
+    } else {
+        e = has_hist ? KernelSet<ARC_F32, true>::launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st)
+                     : KernelSet<ARC_F32, false>::launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st);
     }
-    auto go = [&](auto scan, auto fin, std::atomic<uint64_t>& done_s, std::atomic<uint64_t>& done_f) {
-        cudaError_t err = prepare(scan, dev, done_s, has_hist ? 100 : 0);
-        if (err == cudaSuccess) err = prepare(fin, dev, done_f, 100);
-        if (err != cudaSuccess) return err;
-        // slices x rows; rows past 65,535 fold into z (grid y is 16-bit)
-        const unsigned gy = static_cast<unsigned>(std::min<int64_t>(B, 65535));
-        const unsigned gz = static_cast<unsigned>((B + gy - 1) / gy);
-        scan<<<dim3(static_cast<unsigned>(p.s), gy, gz), kThreads, p.scan_smem, st>>>(sa);
-        err = cudaGetLastError();
-        if (err == cudaSuccess) err = launch_cluster(fin, B, 1, p.fin_smem, st, fa, /*early=*/true);
-        return err;
-    };
-    cudaError_t e;
-    if (dtype == ARC_BF16)
-        e = has_hist ? go(scan_kernel<ARC_BF16, true>, finish_kernel<ARC_BF16, true>, g_prep_scan[1][1], g_prep_fin[1][1])
-                     : go(scan_kernel<ARC_BF16, false>, finish_kernel<ARC_BF16, false>, g_prep_scan[1][0], g_prep_fin[1][0]);
-    else
-        e = has_hist ? go(scan_kernel<ARC_F32, true>, finish_kernel<ARC_F32, true>, g_prep_scan[0][1], g_prep_fin[0][1])
-                     : go(scan_kernel<ARC_F32, false>, finish_kernel<ARC_F32, false>, g_prep_scan[0][0], g_prep_fin[0][0]);
     return e == cudaSuccess ? ARC_OK : ARC_E_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int arc_sample_batch(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype, arc_row_params* params,
+                     const int32_t* hist_offsets, const int32_t* hist_ids, int32_t* out, uint32_t* err_word,
+                     void* workspace, size_t workspace_bytes, const arc_sample_options* opts, void* stream) {
+    return sample_impl(logits, B, V, ld, dtype, params, hist_offsets, hist_ids, out, err_word, workspace,
+                       workspace_bytes, opts, nullptr, stream);
+}
+
+int arc_sample_batch_commit(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,
+                            arc_row_params* params, const int32_t* hist_offsets, const int32_t* hist_ids,
+                            int32_t* out, uint32_t* err_word, void* workspace, size_t workspace_bytes,
+                            const arc_sample_options* opts, const arc_commit_target* commit, void* stream) {
+    if (commit == nullptr || commit->next_ids == nullptr || commit->positions == nullptr ||
+        commit->ring == nullptr || commit->head == nullptr)
+        return ARC_E_NULL;
+    if (reinterpret_cast<uintptr_t>(commit->head) % 8 != 0) return ARC_E_ALIGN;
+    if (commit->max_position <= 0 || commit->capacity == 0 || commit->capacity > ARC_RING_MAX_CAPACITY ||
+        B > static_cast<int64_t>(commit->capacity))
+        return ARC_E_SHAPE;
+    return sample_impl(logits, B, V, ld, dtype, params, hist_offsets, hist_ids, out, err_word, workspace,
+                       workspace_bytes, opts, commit, stream);
 }
 
 int arc_sample_batch_static(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,

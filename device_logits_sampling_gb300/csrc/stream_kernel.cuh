@@ -26,6 +26,7 @@
 
 #include <climits>
 
+#include "commit_row.cuh"
 #include "row_select.cuh"
 
 namespace arc {
@@ -90,6 +91,7 @@ struct FinishArgs {
     int fb_wsum_off;   //   per-(round, warp) masses,
     int fb_patch_off;  //   row patch tables
     int fb_rounds;     // rounds of a whole row
+    arc_commit_target commit;  // decode-loop commit of each row after its token (ring NULL: none)
 };
 
 // One warp's share of a slice, as the scan kernel summarises it: each warp
@@ -961,7 +963,7 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     using Ctx = RowCtx<DT, HIST>;
     constexpr int VEC = E::kVec;
     FinishScratch& SS = KS.st;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const float T = P.temperature;
     const float m = st.m, zm = st.zm;
     __syncthreads();
@@ -1362,6 +1364,27 @@ __device__ __forceinline__ void sorted_select(const FinishArgs& a, const arc_row
 // returns once every summary of the row is complete and visible; loaded()
 // runs after the summaries have been copied on chip (every thread of the CTA
 // calls both).
+// The decode-loop commit of this CTA's row as record head[0] + row (the
+// commit of arc_decode.h, one row per CTA).  Every CTA reads head[0] before
+// its acquire-release arrival on head[1]; the CTA that arrives last has seen
+// every other arrival, so its advance of head[0] by B follows every read of
+// it, and it leaves head[1] at 0 for the next call.
+__device__ __forceinline__ void commit_own_row(const FinishArgs& a, int row, int32_t tok) {
+    const arc_commit_target& c = a.commit;
+    unsigned long long* head = reinterpret_cast<unsigned long long*>(c.head);
+    unsigned long long h, n;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(h) : "l"(head) : "memory");
+    const uint32_t bad = commit_row(tok, row, h + static_cast<unsigned long long>(row), a.V, c.next_ids, c.positions,
+                                    c.max_position, c.owners, c.ring, c.capacity);
+    if (bad != 0 && c.fault_word != nullptr) atomicOr(c.fault_word, bad);
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(n) : "l"(head + 1) : "memory");
+    if (n == static_cast<unsigned long long>(a.B) - 1ull) {
+        asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" ::"l"(head + 1) : "memory");
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(head), "l"(h + static_cast<unsigned long long>(a.B))
+                     : "memory");
+    }
+}
+
 template <int DT, bool HIST, class SumAt, class Wait, class Loaded>
 __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelShared& KS, unsigned char* dyn,
                                            SumAt sum_at, Wait wait, Loaded loaded) {
@@ -1978,6 +2001,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
             dbg.target = st.target;
         }
         if (a.flags & ARC_OPT_STEP_AUTOINC) a.params[row].step = P.step + 1;
+        if (a.commit.ring != nullptr) commit_own_row(a, row, st.token);
     }
 }
 

@@ -32,6 +32,33 @@ def decode_commit(tokens, next_ids, positions, max_position: int, V: int, ring: 
     return rc
 
 
+def sample_and_commit(logits, params, out, next_ids, positions, max_position: int, ring: "Ring", head,
+                      owners=None, fault_word=None, hist_offsets=None, hist_ids=None, err_word=None, debug=None,
+                      workspace=None, ctas_per_row=0, max_hist_len=0, autoinc=False, stream=None,
+                      check: bool = True) -> int:
+    """arc_sample_batch_commit: sample_batch's arguments plus the commit's;
+    head is int64 [2] (records published; rows committed in the running call,
+    0 between calls)."""
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    ld = int(logits.stride(0)) if B > 1 else V
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    if workspace is None:
+        workspace = sampler.workspace_tensor(B, V, sampler._dtype_code(logits), hist_offsets is not None,
+                                             ctas_per_row, max_hist_len, device=logits.device)
+    ptr = sampler._ptr
+    opts = sampler.make_options(ctas_per_row, max_hist_len, autoinc, debug)
+    tgt = sampler.CommitTarget(ptr(next_ids), ptr(positions), ptr(owners), ring.device, ptr(head),
+                               ptr(fault_word), int(max_position), ring.capacity)
+    rc = sampler.load().arc_sample_batch_commit(ptr(logits), B, V, ld, sampler._dtype_code(logits), ptr(params),
+                                                ptr(hist_offsets), ptr(hist_ids), ptr(out), ptr(err_word),
+                                                ptr(workspace), int(workspace.numel()), ctypes.byref(opts),
+                                                ctypes.byref(tgt), sampler._stream(stream))
+    if check and rc != sampler.ARC_OK:
+        raise sampler.ArcError(rc)
+    return rc
+
+
 def stream_idle(stream=None) -> int:
     """1 when every piece of work on the stream has retired, 0 while some has
     not, < 0 on a (possibly asynchronous) CUDA error.  Never blocks."""

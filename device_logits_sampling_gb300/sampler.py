@@ -81,6 +81,20 @@ class Geometry(ctypes.Structure):
     ]
 
 
+class CommitTarget(ctypes.Structure):
+    """arc_commit_target (arc_decode.h), 56 bytes."""
+    _fields_ = [
+        ("next_ids", ctypes.c_void_p),
+        ("positions", ctypes.c_void_p),
+        ("owners", ctypes.c_void_p),
+        ("ring", ctypes.c_void_p),
+        ("head", ctypes.c_void_p),
+        ("fault_word", ctypes.c_void_p),
+        ("max_position", ctypes.c_int32),
+        ("capacity", ctypes.c_uint32),
+    ]
+
+
 _lib = None
 
 # exported symbol -> (restype, argtypes)
@@ -107,6 +121,11 @@ SIGNATURES = {
     "arc_decode_commit": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "arc_sample_batch_commit": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(Options), ctypes.POINTER(CommitTarget),
+        ctypes.c_void_p]),
     "arc_ring_drain": (ctypes.c_int64, [
         ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint64]),
     "arc_stream_idle": (ctypes.c_int, [ctypes.c_void_p]),

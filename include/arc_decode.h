@@ -20,6 +20,10 @@
  * The pages give no code for either; the record layout and the calls below
  * are this library's own.
  *
+ * The commit runs either as its own kernel after the sampler
+ * (arc_decode_commit) or inside the sampler's per-row finish
+ * (arc_sample_batch_commit), with the same checks, record and ordering.
+ *
  * Ordering: arc_decode_commit is one kernel on the caller's stream.  A slot
  * is rewritten as a sequence lock: its stamp first becomes a "writing" value
  * (the new record's stamp minus twice the capacity, which no reader waits
@@ -36,6 +40,8 @@
 
 #include <stddef.h>
 #include <stdint.h>
+
+#include "arc_sample.h"
 
 #ifdef __cplusplus
 extern "C" {
@@ -55,6 +61,9 @@ typedef struct arc_commit_record {
 
 /* return codes of the calls below besides the ARC_E_* codes of arc_sample.h */
 #define ARC_E_RING_OVERRUN (-9) /* the ring was overwritten before it was drained */
+
+/* the largest ring: a slot's "writing" stamp, two laps behind, stays unambiguous */
+#define ARC_RING_MAX_CAPACITY (1u << 30)
 
 /*
  * Commit one step: row r of tokens[0 .. B) becomes record number *head + r.
@@ -82,6 +91,40 @@ int arc_decode_commit(const int32_t* tokens, int64_t B, int32_t V, int32_t* next
                       int32_t* positions, int32_t max_position, const uint32_t* owners,
                       arc_commit_record* ring, uint32_t capacity, uint64_t* head,
                       uint32_t* fault_word, void* stream);
+
+/* The commit's arguments for arc_sample_batch_commit (56 bytes). */
+typedef struct arc_commit_target {
+    int32_t* next_ids;          /* as in arc_decode_commit */
+    int32_t* positions;         /* as in arc_decode_commit */
+    const uint32_t* owners;     /* as in arc_decode_commit (NULL: owner 0) */
+    arc_commit_record* ring;    /* as in arc_decode_commit */
+    uint64_t* head;             /* device, TWO words: head[0] as arc_decode_commit's
+                                   *head; head[1] the rows of the running call that
+                                   have committed: 0 before the first call, and
+                                   every call leaves it 0 */
+    uint32_t* fault_word;       /* as in arc_decode_commit (NULL: none) */
+    int32_t max_position;       /* as in arc_decode_commit */
+    uint32_t capacity;          /* as in arc_decode_commit */
+} arc_commit_target;
+
+/*
+ * arc_sample_batch followed by arc_decode_commit, without the commit's own
+ * launch: the CTA that finishes row r commits row r right after it writes
+ * out[r] (same checks, same record, same sequence-locked publication), and
+ * the last row to commit advances head[0] by B.  Sampling arguments, results
+ * and return codes are arc_sample_batch's; tokens = out, B and V are the
+ * sampler's.  Afterwards out, next_ids, positions, the ring, head[0] and the
+ * fault word hold exactly what arc_sample_batch then arc_decode_commit on the
+ * same stream would leave.  Calls that share a head must not overlap (as for
+ * arc_decode_commit).  Extra host checks, before any CUDA call: commit,
+ * next_ids, positions, ring and head non-NULL (ARC_E_NULL), head 8-byte
+ * aligned (ARC_E_ALIGN), max_position > 0 and B <= capacity <=
+ * ARC_RING_MAX_CAPACITY (ARC_E_SHAPE).
+ */
+int arc_sample_batch_commit(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,
+                            arc_row_params* params, const int32_t* hist_offsets, const int32_t* hist_ids,
+                            int32_t* out, uint32_t* err_word, void* workspace, size_t workspace_bytes,
+                            const arc_sample_options* opts, const arc_commit_target* commit, void* stream);
 
 /*
  * Host only, no CUDA call: copy records first .. first + count - 1 of `ring`

@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == sorted(["arc_sample_batch", "arc_sample_batch_static", "arc_sample_greedy",
+    assert names == sorted(["arc_sample_batch", "arc_sample_batch_static", "arc_sample_batch_commit",
+                            "arc_sample_greedy",
                             "arc_sample_plan", "arc_sample_workspace_bytes", "arc_sample_strerror",
                             "arc_sample_abi_version",
                             "arc_decode_commit", "arc_ring_drain", "arc_stream_idle", "arc_ring_alloc",
@@ -62,6 +63,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(sampler.Options) == 32
     assert sampler.TOP_LOGPROB_DTYPE.itemsize == 8
     assert ctypes.sizeof(sampler.Geometry) == 40
+    assert ctypes.sizeof(sampler.CommitTarget) == 56
     # field offsets of arc_row_params as laid out in the header
     off = {n: workloads.ROW_PARAMS_DTYPE.fields[n][1] for n in workloads.ROW_PARAMS_DTYPE.names}
     assert off["temperature"] == 0 and off["top_k"] == 4 and off["flags"] == 28

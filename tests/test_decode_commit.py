@@ -6,6 +6,8 @@ the commit after the sampler record for record against the oracle, refused
 rows, and a sample + commit step captured in a CUDA graph and replayed with
 the host draining the ring without any CUDA call.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -192,6 +194,31 @@ def test_commit_rejects_bad_arguments_before_any_cuda_call(lib):
     assert c(F, 2, 10, F, F, 5, None, None, 8, F, None, None) == -1  # ring NULL
     assert c(F, 2, 10, F, F, 5, None, F, 8, None, None, None) == -1  # head NULL
     assert lib.arc_ring_drain(None, 4, 0, 1, None, 1) == -1
+
+
+def _commit_call(lib, tgt, B=2, logits=0x1000):
+    F = 0x1000
+    opts = sampler.make_options()
+    t = ctypes.byref(tgt) if tgt is not None else None
+    return lib.arc_sample_batch_commit(logits, B, 8, 8, 1, F, None, None, F, None, F, 1 << 20, ctypes.byref(opts),
+                                       t, None)
+
+
+def test_sample_and_commit_rejects_bad_arguments_before_any_cuda_call(lib):
+    F = 0x1000
+    T = sampler.CommitTarget
+    assert _commit_call(lib, None) == -1                                   # no commit target
+    assert _commit_call(lib, T(None, F, None, F, F, None, 5, 8)) == -1     # next_ids NULL
+    assert _commit_call(lib, T(F, None, None, F, F, None, 5, 8)) == -1     # positions NULL
+    assert _commit_call(lib, T(F, F, None, None, F, None, 5, 8)) == -1     # ring NULL
+    assert _commit_call(lib, T(F, F, None, F, None, None, 5, 8)) == -1     # head NULL
+    assert _commit_call(lib, T(F, F, None, F, F + 4, None, 5, 8)) == -4    # head not 8-byte aligned
+    assert _commit_call(lib, T(F, F, None, F, F, None, 0, 8)) == -2        # max_position <= 0
+    assert _commit_call(lib, T(F, F, None, F, F, None, 5, 1)) == -2        # capacity < B
+    assert _commit_call(lib, T(F, F, None, F, F, None, 5, (1 << 30) + 1)) == -2  # capacity too large
+    # then the sampler's own checks
+    assert _commit_call(lib, T(F, F, None, F, F, None, 5, 8), logits=None) == -1
+    assert _commit_call(lib, T(F, F, None, F, F, None, 5, 8), B=0) == -2
     assert "overwritten" in sampler.strerror(decode.ARC_E_RING_OVERRUN)
 
 
@@ -321,3 +348,69 @@ def test_captured_sample_and_commit_replay_drained_from_the_host(cuda_lib):
     assert len(ring.drain(1, max_spins=1000)) == 0
     ring.close()
     ring_e.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,B", [("mixed_quarters", 256), ("small_fp32", 4), ("single_row_peaked", 1)])
+def test_commit_folded_into_the_sampler_matches_sample_then_commit(cuda_lib, name, B):
+    """arc_sample_batch_commit over several steps (step advanced on device, some
+    rows running out of positions, one row with invalid parameters) leaves the
+    same tokens, next ids, positions, ring, head and fault word as
+    arc_sample_batch followed by arc_decode_commit, and both match the oracle
+    commit of the sampled tokens.  The single-row batch takes the one-launch
+    cluster path, the others the two-kernel path."""
+    import torch
+    from device_logits_sampling_gb300 import workloads as wl
+
+    w = wl.NAMED[name]()
+    B = min(B, w.B)
+    V, N, maxp = w.V, 5, 3
+    logits = sampler.logits_tensor(w)[:B]
+    params = w.params[:B].copy()
+    if B > 2:
+        params["temperature"][2] = -1.0  # invalid: token -1, refused as BAD_TOKEN
+    pos0 = (np.arange(B) % 4).astype(np.int32)  # rows at 3 are refused from the first step on
+    owners0 = (1000 + np.arange(B)).astype(np.int32)
+    cap = 3 * B + 5
+
+    def run(fused):
+        prm = sampler.params_tensor(params)
+        out = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+        ws = sampler.workspace_tensor(B, V, w.dtype)
+        ids = torch.full((B,), 5, dtype=torch.int32, device="cuda")
+        pos = torch.tensor(pos0, device="cuda")
+        owners = torch.tensor(owners0, device="cuda")
+        head = torch.tensor([7, 0], dtype=torch.int64, device="cuda")  # records wrap the ring
+        fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ring = decode.Ring(cap)
+        toks, states = [], []
+        for _ in range(N):
+            if fused:
+                decode.sample_and_commit(logits, prm, out, ids, pos, maxp, ring, head, owners=owners,
+                                         fault_word=fault, workspace=ws, autoinc=True)
+            else:
+                sampler.sample_batch(logits, prm, out, workspace=ws, autoinc=True)
+                decode.decode_commit(out, ids, pos, maxp, V, ring, head[:1], owners=owners, fault_word=fault)
+            torch.cuda.synchronize()
+            toks.append(out.cpu().numpy().copy())
+            states.append((ids.cpu().numpy().copy(), pos.cpu().numpy().copy(), ring.records().copy(),
+                           head.cpu().numpy().copy(), int(fault.item())))
+        ring.close()
+        return toks, states
+
+    t_sep, s_sep = run(False)
+    t_fus, s_fus = run(True)
+    ring_o = oc.empty_ring(cap)
+    ids_o, pos_o, head_o, fault_o = [5] * B, pos0.tolist(), 7, 0
+    for step in range(N):
+        assert np.array_equal(t_fus[step], t_sep[step])
+        ids_o, pos_o, ring_o, head_o, fault_o = oc.commit(t_sep[step].tolist(), V, ids_o, pos_o, maxp,
+                                                          owners0.tolist(), head_o, cap, ring_o, fault_o)
+        for st in (s_sep[step], s_fus[step]):
+            ids, pos, recs, head, fault = st
+            assert ids.tolist() == ids_o and pos.tolist() == pos_o
+            assert np.array_equal(recs, oc.as_records(ring_o))
+            assert int(head[0]) == head_o and fault == fault_o
+        assert int(s_fus[step][3][1]) == 0  # the arrival count is back at 0 after every call
+    if B > 2:
+        assert fault_o == oc.BAD_TOKEN | oc.BAD_POSITION
