@@ -39,15 +39,15 @@ METRIC = "sampled rows/s and achieved HBM GB/s (% of GB300 roofline) at B=256, V
 NBUF = 6  # input copies cycled per step: 6 x 66 MB > L2
 PROFILE = os.path.join(ROOT, "profiles", "scan_finish_mixed_quarters_B256.md")
 KERNELS_PER_STEP = 2  # scan_kernel + finish_kernel
-KERNEL_SOURCES = ["arc_sample.cu", "stream_kernel.cuh", "row_select.cuh", "arc_device.cuh"]
+CSRC = os.path.join(ROOT, "device_logits_sampling_gb300", "csrc")
 
 
 def kernel_hash() -> str:
     """Hash of the kernel sources' code: comments and layout do not count, so a
     profile stays matched to the build it measured until the code changes."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "device_logits_sampling_gb300", "csrc", f), encoding="utf-8") as fh:
+    for f in sorted(x for x in os.listdir(CSRC) if x.endswith((".cu", ".cuh"))):
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
         src = re.sub(r"//[^\n]*", " ", src)
