@@ -2,7 +2,6 @@
 // and the host side of the ring it publishes into.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdint>
 
 #include "arc_decode.h"
@@ -54,6 +53,7 @@ int arc_decode_commit(const int32_t* tokens, int64_t B, int32_t V, int32_t* next
     if (B <= 0 || V <= 0 || max_position <= 0 || capacity == 0 || static_cast<uint64_t>(B) > capacity ||
         capacity > ARC_RING_MAX_CAPACITY)
         return ARC_E_SHAPE;
+    if (reinterpret_cast<uintptr_t>(ring) % 8 != 0 || reinterpret_cast<uintptr_t>(head) % 8 != 0) return ARC_E_ALIGN;
     CommitArgs a{tokens, B, V, next_ids, positions, max_position, owners, ring, capacity, head, fault_word};
     commit_kernel<<<1, kCommitThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return cudaGetLastError() == cudaSuccess ? ARC_OK : ARC_E_CUDA;
@@ -65,28 +65,33 @@ int64_t arc_ring_drain(const arc_commit_record* ring, uint32_t capacity, uint64_
     if (capacity == 0 || count < 0) return ARC_E_SHAPE;
     for (int64_t i = 0; i < count; ++i) {
         const uint64_t idx = first + static_cast<uint64_t>(i);
-        const arc_commit_record* rec = ring + (idx % capacity);
+        const uint64_t* w = reinterpret_cast<const uint64_t*>(ring + (idx % capacity));
         const uint32_t want = static_cast<uint32_t>(idx + 1);
         uint64_t spins = 0;
-        uint32_t stamp;
+        uint64_t v[3];
         while (true) {
-            stamp = __atomic_load_n(&rec->stamp, __ATOMIC_ACQUIRE);
-            if (stamp == want) break;
-            // a stamp ahead of the wanted one (modulo 2^32) is a later lap of
-            // the ring: the wanted record was overwritten
-            const uint32_t ahead = stamp - want;
-            if (stamp != 0 && ahead != 0 && ahead < 0x80000000u) return ARC_E_RING_OVERRUN;
+            // each word is one device store; all three with the wanted stamp
+            // are one record
+            bool all = true, overrun = false;
+            for (int k = 0; k < 3; ++k) {
+                v[k] = __atomic_load_n(w + k, __ATOMIC_ACQUIRE);
+                const uint32_t stamp = static_cast<uint32_t>(v[k] >> 32);
+                all = all && stamp == want;
+                // a stamp ahead of the wanted one (modulo 2^32) is a later lap
+                // of the ring: the wanted record was (or is being) overwritten
+                const uint32_t ahead = stamp - want;
+                overrun = overrun || (stamp != 0 && ahead != 0 && ahead < 0x80000000u);
+            }
+            if (all) break;
+            if (overrun) return ARC_E_RING_OVERRUN;
             if (++spins > max_spins) return i;
         }
-        out[i].token = __atomic_load_n(&rec->token, __ATOMIC_RELAXED);
-        out[i].position = __atomic_load_n(&rec->position, __ATOMIC_RELAXED);
-        out[i].owner = __atomic_load_n(&rec->owner, __ATOMIC_RELAXED);
-        out[i].stamp = stamp;
-        // the slot may be rewritten by a later lap while being read: a writer
-        // replaces the stamp before it touches the fields (see commit_kernel),
-        // so the stamp read again after the fields confirms the copy
-        std::atomic_thread_fence(std::memory_order_acquire);
-        if (__atomic_load_n(&rec->stamp, __ATOMIC_RELAXED) != want) return ARC_E_RING_OVERRUN;
+        out[i].token = static_cast<int32_t>(static_cast<uint32_t>(v[0]));
+        out[i].stamp = want;
+        out[i].position = static_cast<int32_t>(static_cast<uint32_t>(v[1]));
+        out[i].stamp_pos = want;
+        out[i].owner = static_cast<uint32_t>(v[2]);
+        out[i].stamp_owner = want;
     }
     return count;
 }

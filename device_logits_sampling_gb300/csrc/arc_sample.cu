@@ -396,7 +396,8 @@ int arc_sample_batch_commit(const void* logits, int64_t B, int64_t V, int64_t ld
     if (commit == nullptr || commit->next_ids == nullptr || commit->positions == nullptr ||
         commit->ring == nullptr || commit->head == nullptr)
         return ARC_E_NULL;
-    if (reinterpret_cast<uintptr_t>(commit->head) % 8 != 0) return ARC_E_ALIGN;
+    if (reinterpret_cast<uintptr_t>(commit->head) % 8 != 0 || reinterpret_cast<uintptr_t>(commit->ring) % 8 != 0)
+        return ARC_E_ALIGN;
     if (commit->max_position <= 0 || commit->capacity == 0 || commit->capacity > ARC_RING_MAX_CAPACITY ||
         B > static_cast<int64_t>(commit->capacity))
         return ARC_E_SHAPE;

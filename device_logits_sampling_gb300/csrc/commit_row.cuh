@@ -15,25 +15,18 @@
 
 namespace arc {
 
-// System-scope release store of a record's stamp: the record's other fields,
-// stored before it by this thread, are visible to a host that reads the
-// stamp with acquire semantics.
-__device__ __forceinline__ void store_release_sys(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// One 8-byte word of a record, (value, stamp), by one system-scope store: a
+// host read of the aligned word sees all of it or none of it.
+__device__ __forceinline__ void store_word_sys(void* p, uint32_t value, uint32_t stamp) {
+    const unsigned long long w = (static_cast<unsigned long long>(stamp) << 32) | value;
+    asm volatile("st.relaxed.sys.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
-__device__ __forceinline__ void store_relaxed_sys(uint32_t* p, uint32_t v) {
-    asm volatile("st.relaxed.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Orders this thread's earlier stores before its later ones for every
-// observer, the host included.
-__device__ __forceinline__ void fence_acq_rel_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
 
 // Row r's commit as record number idx: checks token and position before any
 // write, then (when both pass) next_ids[r] = tok and positions[r] += 1, then
-// the record.  Returns the row's ARC_COMMIT_* bits.  A slot being rewritten
-// first carries a "writing" stamp two laps behind the new record (it matches
-// no record a reader waits for and reads as behind, not as an overrun), so a
-// host copy taken while the fields change fails its second stamp read.
+// the record's three words, each carrying the stamp idx + 1.  Returns the
+// row's ARC_COMMIT_* bits.  No fence: a host accepts the slot only once all
+// three words show the same stamp, so their order does not matter.
 __device__ __forceinline__ uint32_t commit_row(int32_t tok, int64_t r, uint64_t idx, int32_t V, int32_t* next_ids,
                                                int32_t* positions, int32_t max_position, const uint32_t* owners,
                                                arc_commit_record* ring, uint32_t capacity) {
@@ -46,12 +39,10 @@ __device__ __forceinline__ uint32_t commit_row(int32_t tok, int64_t r, uint64_t 
         positions[r] = pos + 1;
     }
     arc_commit_record* rec = ring + (idx % capacity);
-    store_relaxed_sys(&rec->stamp, static_cast<uint32_t>(idx + 1 - 2 * static_cast<uint64_t>(capacity)));
-    fence_acq_rel_sys();
-    rec->token = bad ? -1 : tok;
-    rec->position = pos;
-    rec->owner = owners ? owners[r] : 0u;
-    store_release_sys(&rec->stamp, static_cast<uint32_t>(idx + 1));
+    const uint32_t stamp = static_cast<uint32_t>(idx + 1);
+    store_word_sys(&rec->token, static_cast<uint32_t>(bad ? -1 : tok), stamp);
+    store_word_sys(&rec->position, static_cast<uint32_t>(pos), stamp);
+    store_word_sys(&rec->owner, owners ? owners[r] : 0u, stamp);
     return bad;
 }
 

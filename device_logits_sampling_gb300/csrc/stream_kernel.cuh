@@ -112,6 +112,7 @@ struct FinishScratch {
     float bf[8];
     uint32_t ccount;  // candidates gathered
     uint32_t nwhole;  // chunks listed for a whole read
+    unsigned long long chead;  // decode-loop commit: the ring head this call read
     uint32_t fc[2][kWarps][4];  // floor search partial counts
     double bd[2];
 };
@@ -1365,24 +1366,29 @@ __device__ __forceinline__ void sorted_select(const FinishArgs& a, const arc_row
 // runs after the summaries have been copied on chip (every thread of the CTA
 // calls both).
 // The decode-loop commit of this CTA's row as record head[0] + row (the
-// commit of arc_decode.h, one row per CTA).  Every CTA reads head[0] before
-// its acquire-release arrival on head[1]; the CTA that arrives last has seen
-// every other arrival, so its advance of head[0] by B follows every read of
-// it, and it leaves head[1] at 0 for the next call.
-__device__ __forceinline__ void commit_own_row(const FinishArgs& a, int row, int32_t tok) {
-    const arc_commit_target& c = a.commit;
-    unsigned long long* head = reinterpret_cast<unsigned long long*>(c.head);
+// commit of arc_decode.h, one row per CTA), in two parts.  commit_arrive, in
+// the prologue: read head[0], then arrive on head[1] with an acquire-release
+// atomic; the CTA that arrives last has seen every other arrival, hence every
+// read of head[0], so it advances head[0] by B and leaves head[1] at 0 for the
+// next call.  commit_publish, after the token: the row's checks, writes and
+// record (no fence, no atomic but the fault bits).
+__device__ __forceinline__ unsigned long long commit_arrive(const FinishArgs& a) {
+    unsigned long long* head = reinterpret_cast<unsigned long long*>(a.commit.head);
     unsigned long long h, n;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(h) : "l"(head) : "memory");
-    const uint32_t bad = commit_row(tok, row, h + static_cast<unsigned long long>(row), a.V, c.next_ids, c.positions,
-                                    c.max_position, c.owners, c.ring, c.capacity);
-    if (bad != 0 && c.fault_word != nullptr) atomicOr(c.fault_word, bad);
     asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(n) : "l"(head + 1) : "memory");
     if (n == static_cast<unsigned long long>(a.B) - 1ull) {
         asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" ::"l"(head + 1) : "memory");
         asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(head), "l"(h + static_cast<unsigned long long>(a.B))
                      : "memory");
     }
+    return h;
+}
+__device__ __forceinline__ void commit_publish(const FinishArgs& a, int row, int32_t tok, unsigned long long h) {
+    const arc_commit_target& c = a.commit;
+    const uint32_t bad = commit_row(tok, row, h + static_cast<unsigned long long>(row), a.V, c.next_ids, c.positions,
+                                    c.max_position, c.owners, c.ring, c.capacity);
+    if (bad != 0 && c.fault_word != nullptr) atomicOr(c.fault_word, bad);
 }
 
 template <int DT, bool HIST, class SumAt, class Wait, class Loaded>
@@ -1422,6 +1428,9 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
     // a top-k row with a large k: the wide entries too
     const bool want_wide = want_mv && a.cwide_off >= 0 && RowMode(P, a.V).filtered && P.top_k > kWideK &&
                            P.top_k < a.V;
+    // the decode-loop commit's ring index: read (and the head advanced) while
+    // the scan still runs; the head is no kernel's but the commit's
+    if (a.commit.ring != nullptr && tid == 0) SS.chead = commit_arrive(a);
     // the summaries are complete and visible after this (the parameters and
     // history above are not written by the scan)
     wait();
@@ -2001,7 +2010,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
             dbg.target = st.target;
         }
         if (a.flags & ARC_OPT_STEP_AUTOINC) a.params[row].step = P.step + 1;
-        if (a.commit.ring != nullptr) commit_own_row(a, row, st.token);
+        if (a.commit.ring != nullptr) commit_publish(a, row, st.token, SS.chead);
     }
 }
 

@@ -1,8 +1,8 @@
 """Binding of arc_decode.h: the decode-loop commit after on-device sampling.
 
 Argument marshalling only: the commit is a kernel of libarcsample.so, the
-ring drain its host function.  Record layout (16 bytes): token, position,
-owner, stamp.
+ring drain its host function.  Record layout (24 bytes, three 8-byte words):
+(token, stamp), (position, stamp), (owner, stamp).
 """
 from __future__ import annotations
 
@@ -12,7 +12,8 @@ import numpy as np
 
 from . import sampler
 
-RECORD_DTYPE = np.dtype([("token", "<i4"), ("position", "<i4"), ("owner", "<u4"), ("stamp", "<u4")])
+RECORD_DTYPE = np.dtype([("token", "<i4"), ("stamp", "<u4"), ("position", "<i4"), ("stamp_pos", "<u4"),
+                         ("owner", "<u4"), ("stamp_owner", "<u4")])
 ARC_COMMIT_BAD_TOKEN = 0x1
 ARC_COMMIT_BAD_POSITION = 0x2
 ARC_E_RING_OVERRUN = -9

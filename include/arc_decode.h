@@ -24,16 +24,17 @@
  * (arc_decode_commit) or inside the sampler's per-row finish
  * (arc_sample_batch_commit), with the same checks, record and ordering.
  *
- * Ordering: arc_decode_commit is one kernel on the caller's stream.  A slot
- * is rewritten as a sequence lock: its stamp first becomes a "writing" value
- * (the new record's stamp minus twice the capacity, which no reader waits
- * for), a system-scope fence follows, then the fields, and last the new
- * stamp with system-scope release semantics.  A host that reads the stamp
- * with acquire semantics (arc_ring_drain does) and finds it matching sees
- * the whole record, and a copy taken while the slot was being rewritten
- * fails its second stamp read.  Every argument is a pointer or a size and the ring index lives in
- * device memory (*head), so a commit captured into a CUDA graph publishes
- * fresh records on every replay.
+ * Publication: a record is three 8-byte words -- (token, stamp), (position,
+ * stamp), (owner, stamp) -- each written with one system-scope 64-bit store,
+ * and a host read of an aligned 8-byte word sees one store or another, never
+ * a mix.  The host accepts a slot as record i only when all three words carry
+ * stamp i + 1: a slot caught while a later lap rewrites it shows a later
+ * stamp in some word (an overrun), a slot not yet written an earlier one (not
+ * yet), so no copy mixes two records and the writer needs no fence.  Every
+ * argument is a pointer or a size and the ring index lives in device memory
+ * (*head), so a commit captured into a CUDA graph publishes fresh records on
+ * every replay.  Stamps are 32-bit: a host that falls 2^32 records behind a
+ * slot could take a record 2^32 laps old for the one it waits for.
  */
 #ifndef ARC_DECODE_H
 #define ARC_DECODE_H
@@ -47,12 +48,15 @@
 extern "C" {
 #endif
 
-/* One published row-step.  16 bytes. */
+/* One published row-step: three 8-byte words, each with the record's stamp
+ * (record index + 1) mod 2^32 in its high half.  24 bytes. */
 typedef struct arc_commit_record {
-    int32_t token;     /* the committed id, or -1 when the row was refused */
-    int32_t position;  /* the row's position before this commit */
-    uint32_t owner;    /* owners[row] when the commit ran (0 when owners is NULL) */
-    uint32_t stamp;    /* (record index + 1) mod 2^32, stored last */
+    int32_t token;        /* the committed id, or -1 when the row was refused */
+    uint32_t stamp;
+    int32_t position;     /* the row's position before this commit */
+    uint32_t stamp_pos;   /* == stamp in a complete record */
+    uint32_t owner;       /* owners[row] when the commit ran (0 when owners is NULL) */
+    uint32_t stamp_owner; /* == stamp in a complete record */
 } arc_commit_record;
 
 /* fault bits ORed into *fault_word (sticky: the library never clears it) */
@@ -62,7 +66,7 @@ typedef struct arc_commit_record {
 /* return codes of the calls below besides the ARC_E_* codes of arc_sample.h */
 #define ARC_E_RING_OVERRUN (-9) /* the ring was overwritten before it was drained */
 
-/* the largest ring: a slot's "writing" stamp, two laps behind, stays unambiguous */
+/* the largest ring (records) */
 #define ARC_RING_MAX_CAPACITY (1u << 30)
 
 /*
@@ -76,7 +80,8 @@ typedef struct arc_commit_record {
  *   max_position  > 0
  *   owners        device [B] or NULL: owner tags copied into the records
  *   ring          device-visible address of `capacity` records in pinned,
- *                 mapped host memory (arc_ring_alloc gives both addresses)
+ *                 mapped host memory, 8-byte aligned (arc_ring_alloc gives
+ *                 both addresses)
  *   capacity      records in the ring, >= B and <= 2^30
  *   head          device uint64: records published by all earlier commits;
  *                 this call publishes records *head .. *head + B - 1, record
@@ -85,7 +90,8 @@ typedef struct arc_commit_record {
  *   stream        cudaStream_t
  * A refused row writes nothing but its record (token -1) and its fault bit.
  * Returns ARC_OK after enqueueing, or a negative ARC_E_* code (arc_sample.h)
- * with nothing enqueued; host checks run before any CUDA call.
+ * with nothing enqueued (ARC_E_ALIGN: ring or head not 8-byte aligned); host
+ * checks run before any CUDA call.
  */
 int arc_decode_commit(const int32_t* tokens, int64_t B, int32_t V, int32_t* next_ids,
                       int32_t* positions, int32_t max_position, const uint32_t* owners,
@@ -110,15 +116,15 @@ typedef struct arc_commit_target {
 /*
  * arc_sample_batch followed by arc_decode_commit, without the commit's own
  * launch: the CTA that finishes row r commits row r right after it writes
- * out[r] (same checks, same record, same sequence-locked publication), and
- * the last row to commit advances head[0] by B.  Sampling arguments, results
+ * out[r] (same checks, same record, same publication); head[0] is read by
+ * every row early in the call and advanced by B once all have read it.  Sampling arguments, results
  * and return codes are arc_sample_batch's; tokens = out, B and V are the
  * sampler's.  Afterwards out, next_ids, positions, the ring, head[0] and the
  * fault word hold exactly what arc_sample_batch then arc_decode_commit on the
  * same stream would leave.  Calls that share a head must not overlap (as for
  * arc_decode_commit).  Extra host checks, before any CUDA call: commit,
- * next_ids, positions, ring and head non-NULL (ARC_E_NULL), head 8-byte
- * aligned (ARC_E_ALIGN), max_position > 0 and B <= capacity <=
+ * next_ids, positions, ring and head non-NULL (ARC_E_NULL), ring and head
+ * 8-byte aligned (ARC_E_ALIGN), max_position > 0 and B <= capacity <=
  * ARC_RING_MAX_CAPACITY (ARC_E_SHAPE).
  */
 int arc_sample_batch_commit(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype,
@@ -129,10 +135,10 @@ int arc_sample_batch_commit(const void* logits, int64_t B, int64_t V, int64_t ld
 /*
  * Host only, no CUDA call: copy records first .. first + count - 1 of `ring`
  * (the host address of the pinned array) to out[0 .. count), in order, each
- * once its stamp is (index + 1) mod 2^32.  Polls a missing record at most
+ * once all three of its stamps are (index + 1) mod 2^32.  Polls a missing record at most
  * max_spins times before giving up.  Returns how many records were copied
  * (fewer than count when one did not land in time), or ARC_E_RING_OVERRUN
- * when a slot already holds a later record, or ARC_E_NULL / ARC_E_SHAPE for
+ * when a slot holds (part of) a later record, or ARC_E_NULL / ARC_E_SHAPE for
  * bad arguments.
  */
 int64_t arc_ring_drain(const arc_commit_record* ring, uint32_t capacity, uint64_t first, int64_t count,

@@ -66,7 +66,9 @@
 extern "C" {
 #endif
 
-#define ARC_SAMPLE_ABI_VERSION 2
+/* 3: arc_commit_record (arc_decode.h) stamps each of its three words;
+ *    arc_sample_batch_commit */
+#define ARC_SAMPLE_ABI_VERSION 3
 
 /* logits element types */
 #define ARC_F32 0

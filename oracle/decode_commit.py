@@ -50,5 +50,8 @@ def empty_ring(capacity: int):
 
 
 def as_records(ring) -> np.ndarray:
-    dt = np.dtype([("token", "<i4"), ("position", "<i4"), ("owner", "<u4"), ("stamp", "<u4")])
-    return np.array([tuple(r) for r in ring], dtype=dt)
+    """The ring as the library lays it out in memory: each record as three
+    8-byte words (token, stamp), (position, stamp), (owner, stamp)."""
+    dt = np.dtype([("token", "<i4"), ("stamp", "<u4"), ("position", "<i4"), ("stamp_pos", "<u4"),
+                   ("owner", "<u4"), ("stamp_owner", "<u4")])
+    return np.array([(t, st, p, st, o, st) for (t, p, o, st) in ring], dtype=dt)

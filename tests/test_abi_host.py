@@ -50,7 +50,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.arc_sample_abi_version() == 2
+    assert lib.arc_sample_abi_version() == 3
     assert sampler.strerror(0) == "ok"
     for rc in range(-1, -9, -1):
         assert len(sampler.strerror(rc)) > 10 and "unknown" not in sampler.strerror(rc)
@@ -111,7 +111,7 @@ def test_bad_arguments_fail_before_any_cuda_call(lib):
     assert call_batch(lib, opts=sampler.Options(0, 0, 0, -1, None, FAKE)) == sampler.ARC_E_OPTION
     assert call_batch(lib, opts=sampler.Options(0, 0, 0, 65, None, FAKE)) == sampler.ARC_E_OPTION
     assert sampler.ARC_MAX_TOP_N == 64 and sampler.TOP_LOGPROB_DTYPE.itemsize == 8
-    assert lib.arc_sample_abi_version() == 2
+    assert lib.arc_sample_abi_version() == 3
     g = lib.arc_sample_greedy
     assert g(None, 2, 8, 8, 1, FAKE, None, None) == sampler.ARC_E_NULL
     assert g(FAKE, 2, 8, 4, 1, FAKE, None, None) == sampler.ARC_E_SHAPE

@@ -89,61 +89,84 @@ def test_drain_across_the_stamp_wrap(lib):
     assert got["stamp"].tolist() == [(1 << 32) - 1, 0, 1] and got["token"].tolist() == [1, 2, 3]
 
 
+def _words(ring):
+    """The ring's 8-byte words, [capacity, 3]: (value, stamp) each."""
+    return ring.view(np.uint64).reshape(len(ring), 3)
+
+
+def _put(ring, slot, values, stamp, words=(0, 1, 2)):
+    """Store words of one slot the way the device does: one 8-byte store per
+    word, the stamp in the high half."""
+    w = _words(ring)
+    for k in words:
+        w[slot, k] = np.uint64((int(stamp) << 32) | (int(values[k]) & 0xFFFFFFFF))
+
+
+def test_record_layout_is_three_stamped_words():
+    assert decode.RECORD_DTYPE.itemsize == 24
+    ring = np.zeros(1, dtype=decode.RECORD_DTYPE)
+    _put(ring, 0, (-1, 7, 9), 5)
+    r = ring[0]
+    assert (int(r["token"]), int(r["position"]), int(r["owner"])) == (-1, 7, 9)
+    assert int(r["stamp"]) == int(r["stamp_pos"]) == int(r["stamp_owner"]) == 5
+
+
 def test_drain_never_confirms_a_slot_that_is_being_rewritten(lib):
-    """A slot in the middle of a rewrite (the "writing" stamp, two laps behind
-    the new record, with the new lap's fields already stored) is not a record
-    of either lap: the drain returns short instead of a mixed record."""
+    """A slot in the middle of a rewrite (some words of the new lap stored,
+    the others still of the old one) is not a record of either lap: the old
+    record reads as overrun, the new one as not yet published."""
     cap = 4
     ring = np.zeros(cap, dtype=decode.RECORD_DTYPE)
     for i in range(cap):  # lap 0 published
-        ring[i] = (10 + i, i, 7, i + 1)
-    new = cap + 1  # record 5 is being written into slot 1
-    ring[1]["token"], ring[1]["position"], ring[1]["owner"] = 99, 5, 8
-    ring[1]["stamp"] = (new + 1 - 2 * cap) % (1 << 32)
-    got = decode.ring_drain(ring.ctypes.data, cap, 0, cap, max_spins=50)
-    assert got["token"].tolist() == [10]  # record 1 is neither confirmed nor mixed
-    assert len(decode.ring_drain(ring.ctypes.data, cap, new, 1, max_spins=50)) == 0
-    ring[1]["stamp"] = new + 1  # the rewrite completes: record 1 is overrun, record 5 is readable
+        _put(ring, i, (10 + i, i, 7), i + 1)
+    new = cap + 1  # record 5 is being written into slot 1: its token word first
+    _put(ring, 1, (99, 5, 8), new + 1, words=(0,))
+    assert decode.ring_drain(ring.ctypes.data, cap, 0, 1, max_spins=50)["token"].tolist() == [10]
     with pytest.raises(sampler.ArcError) as e:
         decode.ring_drain(ring.ctypes.data, cap, 1, 1, max_spins=50)
     assert e.value.rc == decode.ARC_E_RING_OVERRUN
-    assert decode.ring_drain(ring.ctypes.data, cap, new, 1)[0].tolist() == (99, 5, 8, new + 1)
+    assert len(decode.ring_drain(ring.ctypes.data, cap, new, 1, max_spins=50)) == 0
+    _put(ring, 1, (99, 5, 8), new + 1, words=(2,))  # the owner word: still not whole
+    assert len(decode.ring_drain(ring.ctypes.data, cap, new, 1, max_spins=50)) == 0
+    _put(ring, 1, (99, 5, 8), new + 1, words=(1,))  # the rewrite completes
+    got = decode.ring_drain(ring.ctypes.data, cap, new, 1)
+    assert (int(got[0]["token"]), int(got[0]["position"]), int(got[0]["owner"]), int(got[0]["stamp"])) == \
+        (99, 5, 8, new + 1)
 
 
 def test_drain_against_a_writer_that_laps_it(lib):
-    """A writer thread rewrites slots as the commit kernel does (writing stamp,
-    fields, new stamp) and laps the reader at will: every record the drain
-    returns is whole (its fields agree with its stamp); a lapped read is an
-    overrun, never a mixed record."""
+    """A writer thread rewrites slots word by word as the commit does (one
+    8-byte store per word, in a varying order) and laps the reader at will:
+    every record the drain returns is whole (its fields agree with its
+    stamp); a lapped read is an overrun, never a mixed record."""
     import threading
 
     cap, n = 8, 4000
     ring = np.zeros(cap, dtype=decode.RECORD_DTYPE)
     done = []
+    orders = [(0, 1, 2), (2, 1, 0), (1, 0, 2)]
 
     def writer():
         for i in range(n):
-            slot = i % cap
-            ring["stamp"][slot] = (i + 1 - 2 * cap) % (1 << 32)
-            ring["token"][slot], ring["position"][slot], ring["owner"][slot] = 3 * i, i, i % 1000
-            ring["stamp"][slot] = i + 1
+            for k in orders[i % 3]:
+                _put(ring, i % cap, (3 * i, i, i % 1000), i + 1, words=(k,))
         done.append(True)
 
     t = threading.Thread(target=writer)
     t.start()
-    seen = overruns = 0
+    seen = 0
     first = 0
     while not done or first < n:
         try:
             got = decode.ring_drain(ring.ctypes.data, cap, first, 4, max_spins=200)
         except sampler.ArcError as e:
             assert e.rc == decode.ARC_E_RING_OVERRUN
-            overruns += 1
             first = max(first + 1, int(ring["stamp"].max()) - cap)  # skip ahead of the writer
             continue
         for r in got:
             i = int(r["stamp"]) - 1
             assert (int(r["token"]), int(r["position"]), int(r["owner"])) == (3 * i, i, i % 1000)
+            assert int(r["stamp_pos"]) == int(r["stamp_owner"]) == i + 1
         seen += len(got)
         first += len(got)
         if done and len(got) == 0:
@@ -153,8 +176,8 @@ def test_drain_against_a_writer_that_laps_it(lib):
 
 
 def test_drain_waits_for_records_published_concurrently(lib):
-    """A writer thread publishes records (fields first, stamp last) while the
-    C drain, which runs without the interpreter lock, polls for them."""
+    """A writer thread publishes records word by word while the C drain,
+    which runs without the interpreter lock, polls for them."""
     import threading
     import time
 
@@ -166,11 +189,10 @@ def test_drain_waits_for_records_published_concurrently(lib):
         for i in range(n):
             while len(drained) + cap <= i:  # never lap the reader
                 time.sleep(0)
-            slot = ring[i % cap]
-            slot["token"], slot["position"], slot["owner"] = i * 3, i, 5
-            ring["stamp"][i % cap] = i + 1
-            if i % 7 == 0:
-                time.sleep(0.0005)
+            for k in (2, 0, 1):
+                _put(ring, i % cap, (i * 3, i, 5), i + 1, words=(k,))
+                if i % 7 == 0:
+                    time.sleep(0.0002)
 
     t = threading.Thread(target=writer)
     t.start()
@@ -193,6 +215,8 @@ def test_commit_rejects_bad_arguments_before_any_cuda_call(lib):
     assert c(F, 9, 10, F, F, 5, None, F, 8, F, None, None) == -2     # capacity < B
     assert c(F, 2, 10, F, F, 5, None, None, 8, F, None, None) == -1  # ring NULL
     assert c(F, 2, 10, F, F, 5, None, F, 8, None, None, None) == -1  # head NULL
+    assert c(F, 2, 10, F, F, 5, None, F + 4, 8, F, None, None) == -4  # ring not 8-byte aligned
+    assert c(F, 2, 10, F, F, 5, None, F, 8, F + 4, None, None) == -4  # head not 8-byte aligned
     assert lib.arc_ring_drain(None, 4, 0, 1, None, 1) == -1
 
 
@@ -213,6 +237,7 @@ def test_sample_and_commit_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _commit_call(lib, T(F, F, None, None, F, None, 5, 8)) == -1     # ring NULL
     assert _commit_call(lib, T(F, F, None, F, None, None, 5, 8)) == -1     # head NULL
     assert _commit_call(lib, T(F, F, None, F, F + 4, None, 5, 8)) == -4    # head not 8-byte aligned
+    assert _commit_call(lib, T(F, F, None, F + 4, F, None, 5, 8)) == -4    # ring not 8-byte aligned
     assert _commit_call(lib, T(F, F, None, F, F, None, 0, 8)) == -2        # max_position <= 0
     assert _commit_call(lib, T(F, F, None, F, F, None, 5, 1)) == -2        # capacity < B
     assert _commit_call(lib, T(F, F, None, F, F, None, 5, (1 << 30) + 1)) == -2  # capacity too large
