@@ -43,6 +43,7 @@ struct Plan {
     int fb_patch_off = 0;
     int fb_rounds = 0;
     int fin_smem = 0;
+    int fin_g = 1;          // finish CTAs per row (a cluster when > 1)
     int64_t slices = 0;
     int F = 0;
     size_t ws_bytes = 0;
@@ -87,6 +88,8 @@ int check_options(const arc_sample_options* o) {
 // all resident at once (two per SM), takes the one-launch cluster kernel when
 // `allow_cluster`; an explicit ctas_per_row always takes the two kernels.
 constexpr int kClusterMax = 16;
+constexpr int kFinishClusterMax = 8;
+constexpr int64_t kSmemPerSM = 233472;  // shared memory of an SM (228 KB)
 
 int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_options* o, int num_sms,
               Plan& p, bool allow_cluster = true) {
@@ -143,11 +146,17 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     // the chunk max vectors of a filtered row, when they fit in 16 KB (else
     // the finish reads them from the logits)
     const int64_t cmv_raw = s * kChunks * 16;
-    const int64_t cmv_bytes = cmv_raw <= 16384 ? r128(cmv_raw) : 0;
+    // two finish CTAs per SM when their shared memory allows it (227 KB of the
+    // SM's 228 KB usable, 1 KB reserved per CTA)
+    const int64_t per_cta_extra = static_cast<int64_t>(sizeof(KernelShared)) + 1024;
+    auto fits_two = [&](int64_t dyn) { return 2 * (dyn + per_cta_extra) <= kSmemPerSM; };
+    const int64_t fin_base = cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch;
+    int64_t cmv_bytes = cmv_raw <= 16384 ? r128(cmv_raw) : 0;
+    // (not at the price of the second CTA per SM)
+    if (fits_two(fin_base) && !fits_two(fin_base + 2 * cmv_bytes)) cmv_bytes = 0;
     // and the wide entries of top-k rows with a large k, under the same bound
     const int64_t cwide_bytes = cmv_bytes;
-    const int64_t fin_smem =
-        cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch + cmv_bytes + cwide_bytes;
+    const int64_t fin_smem = fin_base + cmv_bytes + cwide_bytes;
     int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
     if (cluster) limit -= kSummaryBytes + static_cast<int64_t>(sizeof(ScanShared));
     if (fin_smem > limit || scan_smem > limit) {
@@ -176,6 +185,18 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
                           p.fb_wsum_off, p.fb_patch_off, p.cmv_off, p.cwide_off})
         if (off >= 0 && off % 16 != 0) return ARC_E_UNSUPPORTED;
     p.fin_smem = static_cast<int>(fin_smem);
+    // finish CTAs per row: while the batch leaves finish slots idle (one or
+    // two CTAs per SM, by shared memory), rows of at least 2,048 vectors per
+    // CTA get a cluster of up to 8, which splits the threshold bisection of a
+    // row over the cluster
+    p.fin_g = 1;
+    if (!cluster) {
+        const int64_t nv_row = (V + vec - 1) / vec;
+        const int64_t per_sm = fits_two(fin_smem) ? 2 : 1;
+        while (p.fin_g < kFinishClusterMax && B * 2 * p.fin_g <= per_sm * num_sms &&
+               nv_row >= int64_t{2} * p.fin_g * 2048)
+            p.fin_g *= 2;
+    }
     p.slices = B * s;
     p.F = 62 - ceil_log2(V);
     p.ws_bytes = cluster ? 0 : static_cast<size_t>(B * s) * kSummaryBytes;
@@ -241,6 +262,8 @@ int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history, co
     geom->frac_bits = p.F;
     geom->launches = p.cluster ? 1 : 2;
     geom->workspace_bytes = static_cast<int64_t>(p.ws_bytes);
+    geom->finish_ctas = p.cluster ? 1 : p.fin_g;
+    geom->reserved = 0;
     return ARC_OK;
 }
 
@@ -306,6 +329,17 @@ int sample_impl(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dt
         }
     }
     if (workspace_bytes < p.ws_bytes) return ARC_E_WORKSPACE;
+    if (!p.cluster && p.fin_g > 1) {
+        // a split finish only when the device can schedule its clusters
+        bool ok;
+        if (dtype == ARC_BF16)
+            ok = has_hist ? KernelSet<ARC_BF16, true>::finish_cluster_ok(p.fin_g, p.fin_smem, dev)
+                          : KernelSet<ARC_BF16, false>::finish_cluster_ok(p.fin_g, p.fin_smem, dev);
+        else
+            ok = has_hist ? KernelSet<ARC_F32, true>::finish_cluster_ok(p.fin_g, p.fin_smem, dev)
+                          : KernelSet<ARC_F32, false>::finish_cluster_ok(p.fin_g, p.fin_smem, dev);
+        if (!ok) p.fin_g = 1;
+    }
 
     const int es = elem_bytes(dtype);
     const int aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((ld * es) % 16 == 0);
@@ -356,6 +390,7 @@ int sample_impl(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dt
     fa.fb_patch_off = p.fb_patch_off;
     fa.fb_rounds = p.fb_rounds;
     fa.commit = commit ? *commit : arc_commit_target{};
+    fa.fin_g = p.fin_g;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;

@@ -14,11 +14,14 @@ namespace arc {
 
 template <int DT, bool HIST>
 struct KernelSet {
-    // scan_kernel over B rows of s slices, then finish_kernel (one CTA per
-    // row) behind it under programmatic dependent launch; sets the kernels'
-    // attributes on the first call on a device
+    // scan_kernel over B rows of s slices, then finish_kernel (fa.fin_g CTAs
+    // per row, a cluster) behind it under programmatic dependent launch; sets
+    // the kernels' attributes on the first call on a device
     static cudaError_t launch_two(const ScanArgs& sa, const FinishArgs& fa, int s, int64_t B, int scan_smem,
                                   int fin_smem, int dev, cudaStream_t st);
+    // whether finish_kernel with clusters of g CTAs per row and `smem` bytes
+    // of dynamic shared memory can run on the device (attributes set, cached)
+    static bool finish_cluster_ok(int g, int smem, int dev);
     // whether cluster_kernel with clusters of s CTAs and `dyn` bytes of
     // dynamic shared memory can run on the device (attributes set, cached)
     static bool cluster_ok(int s, int dyn, int dev);

@@ -34,8 +34,15 @@ cudaError_t KernelSet<DT, HIST>::launch_two(const ScanArgs& sa, const FinishArgs
     const unsigned gz = static_cast<unsigned>((B + gy - 1) / gy);
     scan_kernel<DT, HIST><<<dim3(static_cast<unsigned>(s), gy, gz), kThreads, scan_smem, st>>>(sa);
     err = cudaGetLastError();
-    if (err == cudaSuccess) err = launch_cluster(finish_kernel<DT, HIST>, B, 1, fin_smem, st, fa, /*early=*/true);
+    if (err == cudaSuccess)
+        err = launch_cluster(finish_kernel<DT, HIST>, B * fa.fin_g, fa.fin_g, fin_smem, st, fa, /*early=*/true);
     return err;
+}
+
+template <int DT, bool HIST>
+bool KernelSet<DT, HIST>::finish_cluster_ok(int g, int smem, int dev) {
+    return prepare(finish_kernel<DT, HIST>, dev, KernelPrep<DT, HIST>::fin, 100) == cudaSuccess &&
+           cluster_fits(finish_kernel<DT, HIST>, dev, DT + 2, HIST, g, smem);
 }
 
 template <int DT, bool HIST>

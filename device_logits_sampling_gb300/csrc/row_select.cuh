@@ -14,8 +14,10 @@
 // gather are resolved by an id-order count walk.
 //
 // The helpers are written for a thread-block cluster of s CTAs sharing one
-// row (partials exchanged through distributed shared memory, decisions taken
-// identically by every CTA); the finish kernel uses them with s = 1.
+// row, each with a contiguous part of it (partials exchanged through
+// distributed shared memory, decisions taken identically by every CTA): the
+// finish kernel uses them with its cluster of CTAs per row (s = 1 for large
+// batches, up to 8 when the batch leaves SMs idle).
 //
 // Masses are fixed-point integers (units of 2^-F of the max weight), so sums
 // are exact, associative and identical in every pass.
@@ -79,6 +81,7 @@ struct RowCtx {
     cg::cluster_group cl;
     int s, rank, row, tid, lane, warp;
     int a0, a1, n, nv, nvf, rounds;
+    int v0;                     // the row's vector index of this CTA's first vector (a0 / VEC)
     const unsigned char* data;  // the slice: shared memory, or global memory when src_global
     bool src_global;
     bool src_aligned;
@@ -106,7 +109,7 @@ struct RowCtx {
     // ---------------------------------------------------------------- loads
     __device__ __forceinline__ bool vec_patched(int v) const {
         if (!(HIST && has_patch)) return false;
-        const int l0 = v * VEC;
+        const int l0 = (v0 + v) * VEC;
         return ((bm[l0 >> 5] >> (l0 & 31)) & ((1u << VEC) - 1u)) != 0;
     }
 
@@ -117,8 +120,9 @@ struct RowCtx {
     __device__ __forceinline__ bool may_hold(int v, float thr) const {
         if (vmax == nullptr) return true;
         if (vps == 0) return vmax[v] >= thr;
-        const int c = v / vps;
-        return vmax[c * cps + ((v - c * vps) >> 5)] >= thr;
+        const int gv = v0 + v;  // the table is the whole row's
+        const int c = gv / vps;
+        return vmax[c * cps + ((gv - c * vps) >> 5)] >= thr;
     }
 
     __device__ __forceinline__ void load(int v, float (&z)[VEC]) const { unpack_patched(v, raw_vec(v), z); }
@@ -127,7 +131,7 @@ struct RowCtx {
     __device__ __forceinline__ void unpack_patched(int v, const uint4& raw, float (&z)[VEC]) const {
         E::unpack(raw, z);
         if (HIST && has_patch) {
-            const int l0 = v * VEC;
+            const int l0 = (v0 + v) * VEC;  // the patch tables are the whole row's
             const uint32_t word = bm[l0 >> 5];
             const uint32_t bits = (word >> (l0 & 31)) & ((1u << VEC) - 1u);
             if (bits) {

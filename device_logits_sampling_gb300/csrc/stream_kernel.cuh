@@ -91,6 +91,7 @@ struct FinishArgs {
     int fb_wsum_off;   //   per-(round, warp) masses,
     int fb_patch_off;  //   row patch tables
     int fb_rounds;     // rounds of a whole row
+    int fin_g;         // finish CTAs per row (a cluster when > 1)
     arc_commit_target commit;  // decode-loop commit of each row after its token (ring NULL: none)
 };
 
@@ -913,21 +914,30 @@ template <int DT, bool HIST>
 __device__ __forceinline__ void setup_row_ctx(RowCtx<DT, HIST>& X, const FinishArgs& a, int row, const char* rowp,
                                               float* cm, const uint32_t* pbm, const uint32_t* pwp, const float* ppat,
                                               bool has_patch, bool row_nan, float m, float c, float scale, bool infm,
-                                              unsigned char* dyn) {
+                                              unsigned char* dyn, int g = 1, int rank = 0) {
     constexpr int VEC = Elem<DT>::kVec;
-    X.s = 1;
-    X.rank = 0;
+    // a cluster of g CTAs splits the row into g parts of whole 32-vector runs
+    const int nv_row = (a.V + VEC - 1) / VEC;
+    int v0 = 0, v1 = nv_row;
+    if (g > 1) {
+        const int per = ((nv_row + g - 1) / g + 31) & ~31;
+        v0 = min(nv_row, rank * per);
+        v1 = min(nv_row, v0 + per);
+    }
+    X.s = g;
+    X.rank = rank;
     X.row = row;
     X.tid = threadIdx.x;
     X.lane = threadIdx.x & 31;
     X.warp = threadIdx.x >> 5;
-    X.a0 = 0;
-    X.a1 = a.V;
-    X.n = a.V;
-    X.nv = (a.V + VEC - 1) / VEC;
-    X.nvf = a.V / VEC;
+    X.v0 = v0;
+    X.a0 = v0 * VEC;
+    X.a1 = min(a.V, v1 * VEC);
+    X.n = max(0, X.a1 - X.a0);
+    X.nv = v1 - v0;
+    X.nvf = X.n / VEC;
     X.rounds = (X.nv + kThreads - 1) / kThreads;
-    X.data = reinterpret_cast<const unsigned char*>(rowp);
+    X.data = reinterpret_cast<const unsigned char*>(rowp) + static_cast<int64_t>(X.a0) * Elem<DT>::kBytes;
     X.src_global = true;
     X.src_aligned = a.aligned != 0;
     X.vmax = cm;
@@ -959,7 +969,7 @@ template <int DT, bool HIST>
 __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_row_params& P, const RowMode& md, int row,
                                             const char* rowp, float* cm, const uint32_t* pbm, const uint32_t* pwp,
                                             const float* ppat, bool has_patch, KernelShared& KS, unsigned char* dyn,
-                                            RowState& st) {
+                                            RowState& st, int g, int rank) {
     using E = Elem<DT>;
     using Ctx = RowCtx<DT, HIST>;
     constexpr int VEC = E::kVec;
@@ -971,13 +981,15 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     cg::cluster_group cl = cg::this_cluster();
     Ctx X(KS.fb, cl);
     setup_row_ctx<DT, HIST>(X, a, row, rowp, cm, pbm, pwp, ppat, has_patch, st.row_nan, m, st.cT, st.scale, st.infm,
-                            dyn);
+                            dyn, g, rank);
     for (int b = tid; b < kBins; b += kThreads) KS.fb.ghist[b] = 0;
     if (tid == 0) {
         KS.fb.ccount = 0;
         KS.fb.flags = 0;
     }
-    __syncthreads();
+    // every CTA of the row has cleared what the others add into (a cluster
+    // barrier when the row is split)
+    X.xsync();
     const uint32_t Km = fkey(m);
     uint32_t err = st.err;
     Surv K{-INFINITY, INT_MAX};
@@ -1065,10 +1077,21 @@ __device__ __forceinline__ void finish_general(const FinishArgs& a, const arc_ro
     X.xsync();
     st.mass_r = X.xscan(0, ~0ull).total;
     st.target = scale_by_u(st.rbits, st.mass_r);
+    // the CTA whose part holds the target walks it; the others learn the token
+    const typename Ctx::Scan sc = X.xscan(0, st.target);
     X.xnext();
-    int tok = X.walk(
-        st.target, [&](const float(&z)[VEC], int g0) { return X.vec_mass(mr, z, g0, R); },
-        [&](const float(&z)[VEC], int g0, uint64_t tt) { return X.vec_mass_walk(mr, z, g0, R, tt); });
+    int tok = -1;
+    if (sc.first == X.rank)
+        tok = X.walk(
+            st.target - sc.before_me, [&](const float(&z)[VEC], int g0) { return X.vec_mass(mr, z, g0, R); },
+            [&](const float(&z)[VEC], int g0, uint64_t tt) { return X.vec_mass_walk(mr, z, g0, R, tt); });
+    if (X.s > 1) {
+        if (tid == 0) X.S.slot[X.par][0] = static_cast<uint64_t>(static_cast<uint32_t>(tok));
+        X.xsync();
+        tok = sc.first >= 0 ? static_cast<int>(static_cast<uint32_t>(X.xread(sc.first, 0))) : -1;
+        X.xnext();
+        X.xsync();  // no CTA leaves while another may still read its shared memory
+    }
     if (tok < 0) {
         tok = st.am != kAmUnknown ? st.am : first_max_id<DT>(a, rowp, cm, a.s * kChunks, m);
         err |= kErrInternal;
@@ -1393,7 +1416,7 @@ __device__ __forceinline__ void commit_publish(const FinishArgs& a, int row, int
 
 template <int DT, bool HIST, class SumAt, class Wait, class Loaded>
 __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelShared& KS, unsigned char* dyn,
-                                           SumAt sum_at, Wait wait, Loaded loaded) {
+                                           SumAt sum_at, Wait wait, Loaded loaded, int g, int rank) {
     using E = Elem<DT>;
     using Ctx = RowCtx<DT, HIST>;
     constexpr int VEC = E::kVec;
@@ -1430,7 +1453,8 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                            P.top_k < a.V;
     // the decode-loop commit's ring index: read (and the head advanced) while
     // the scan still runs; the head is no kernel's but the commit's
-    if (a.commit.ring != nullptr && tid == 0) SS.chead = commit_arrive(a);
+    const bool leader = rank == 0;  // the CTA that writes the row's results
+    if (a.commit.ring != nullptr && leader && tid == 0) SS.chead = commit_arrive(a);
     // the summaries are complete and visible after this (the parameters and
     // history above are not written by the scan)
     wait();
@@ -1980,11 +2004,12 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                     st.err |= kErrInternal;
                 }
             } else {
-                finish_general<DT, HIST>(a, P, md, row, rowp, cm, pbm, pwp, ppat, has_patch, KS, dyn, st);
+                finish_general<DT, HIST>(a, P, md, row, rowp, cm, pbm, pwp, ppat, has_patch, KS, dyn, st, g, rank);
             }
         }
     }
 
+    if (!leader) return;  // a helper CTA of a split row: its part is done
     if (a.top_n > 0)
         top_n_row<DT, HIST>(a, row, P, mode >= 0, rowp, m, st.row_nan, cT, st.scale, want_mv, hbeg, hn, KS, dyn);
 
@@ -2014,15 +2039,21 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
     }
 }
 
-// One CTA per row, launched behind scan_kernel (programmatic dependent launch).
+// One CTA per row, launched behind scan_kernel (programmatic dependent launch);
+// when the batch leaves SMs idle, a cluster of a.fin_g CTAs per row: every CTA
+// takes the row's decisions from the same summaries, a row that needs the
+// threshold bisection splits its passes over the cluster, and CTA 0 writes
+// the results.
 template <int DT, bool HIST>
 __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_constant__ FinishArgs a) {
     extern __shared__ __align__(128) unsigned char dyn[];
     __shared__ KernelShared KS;
-    const int row = blockIdx.x;
+    const int g = a.fin_g;
+    const int row = static_cast<int>(blockIdx.x) / g;
+    const int rank = static_cast<int>(blockIdx.x) - row * g;  // the CTA's rank in its cluster
     finish_row<DT, HIST>(
         a, row, KS, dyn, [&](int c) { return summary_at(a.summaries, a.s, row, c); },
-        [] { asm volatile("griddepcontrol.wait;" ::: "memory"); }, [] {});
+        [] { asm volatile("griddepcontrol.wait;" ::: "memory"); }, [] {}, g, rank);
 }
 
 struct FusedArgs {
@@ -2056,7 +2087,7 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(const __grid_const
     // (the scan's shared memory is dead here: the finish reuses dyn)
     finish_row<DT, HIST>(
         f.fin, row, KS, dyn, [&](int c) { return static_cast<const unsigned char*>(cl.map_shared_rank(mysum, c)); },
-        [&] { cl.sync(); }, [&] { cl.sync(); });
+        [&] { cl.sync(); }, [&] { cl.sync(); }, 1, 0);
 }
 
 }  // namespace arc

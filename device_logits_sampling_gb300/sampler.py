@@ -78,6 +78,8 @@ class Geometry(ctypes.Structure):
         ("frac_bits", ctypes.c_int32),
         ("launches", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
+        ("finish_ctas", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 

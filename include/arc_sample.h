@@ -67,7 +67,7 @@ extern "C" {
 #endif
 
 /* 3: arc_commit_record (arc_decode.h) stamps each of its three words;
- *    arc_sample_batch_commit */
+ *    arc_sample_batch_commit; arc_sample_geometry.finish_ctas */
 #define ARC_SAMPLE_ABI_VERSION 3
 
 /* logits element types */
@@ -241,6 +241,10 @@ typedef struct arc_sample_geometry {
                                 ctas_per_row CTAs per row, summaries combined in
                                 distributed shared memory); 2: scan + finish */
     int64_t workspace_bytes; /* workspace this geometry uses (0 with one launch) */
+    int32_t finish_ctas;     /* two launches: finish CTAs per row (a cluster
+                                when > 1: small batches split a row's
+                                threshold bisection over it); 1 otherwise */
+    int32_t reserved;        /* 0 */
 } arc_sample_geometry;
 
 int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history,

@@ -62,7 +62,7 @@ def test_struct_layouts_match_header():
     assert sampler.ROW_DEBUG_DTYPE.itemsize == 72
     assert ctypes.sizeof(sampler.Options) == 32
     assert sampler.TOP_LOGPROB_DTYPE.itemsize == 8
-    assert ctypes.sizeof(sampler.Geometry) == 40
+    assert ctypes.sizeof(sampler.Geometry) == 48
     assert ctypes.sizeof(sampler.CommitTarget) == 56
     # field offsets of arc_row_params as laid out in the header
     off = {n: workloads.ROW_PARAMS_DTYPE.fields[n][1] for n in workloads.ROW_PARAMS_DTYPE.names}
@@ -138,6 +138,16 @@ def test_plan_geometry(lib):
     assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_F32).launches == 2
     # fp32 slices hold half as many logits
     assert sampler.plan(64, workloads.VOCAB_V4, workloads.DTYPE_F32).ctas_per_row == 32
+    # finish CTAs per row: one while the batch fills the SMs (two finish CTAs
+    # per SM), else a cluster of up to 8 while each keeps >= 2,048 vectors
+    assert g.finish_ctas == 1 and g1.finish_ctas == 1
+    assert sampler.plan(64, workloads.VOCAB_V4, workloads.DTYPE_F32).finish_ctas == 4
+    assert sampler.plan(152, workloads.VOCAB_V4, workloads.DTYPE_F32).finish_ctas == 2
+    assert sampler.plan(153, workloads.VOCAB_V4, workloads.DTYPE_F32).finish_ctas == 1
+    assert sampler.plan(20, workloads.VOCAB_V4, workloads.DTYPE_BF16).finish_ctas == 4
+    assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_F32).finish_ctas == 8
+    assert sampler.plan(2, 5_000, workloads.DTYPE_F32, ctas_per_row=4).finish_ctas == 1
+    assert sampler.plan(2, 20_000, workloads.DTYPE_F32, ctas_per_row=8).finish_ctas == 2
     # small vocabularies stay on one CTA (which scans and finishes its row)
     g4 = sampler.plan(4, 1024, workloads.DTYPE_F32)
     assert (g4.ctas_per_row, g4.launches) == (1, 1)

@@ -249,7 +249,9 @@ def test_sample_and_commit_rejects_bad_arguments_before_any_cuda_call(lib):
 
 # ---------------------------------------------------------------- GPU
 def _run_oracle(tokens, V, ids, pos, maxp, owners, head, cap, ring_recs, fault):
-    return oc.commit(tokens, V, ids, pos, maxp, owners, head, cap, [tuple(int(x) for x in r) for r in ring_recs], fault)
+    # the library's records as the oracle's (token, position, owner, stamp)
+    ring = [(int(r["token"]), int(r["position"]), int(r["owner"]), int(r["stamp"])) for r in ring_recs]
+    return oc.commit(tokens, V, ids, pos, maxp, owners, head, cap, ring, fault)
 
 
 @pytest.mark.gpu

@@ -330,6 +330,45 @@ def test_enumeration_and_bisection_agree(cuda_lib, name):
           f"bisection {int(filtered.sum()) - direct}")
 
 
+def _rows(w, B, reps=1):
+    """A workload of w's first B rows, repeated reps times (history included)."""
+    import dataclasses
+
+    idx = np.tile(np.arange(B), reps)
+    ho, hi = None, None
+    if w.hist_offsets is not None:
+        lens = np.diff(w.hist_offsets)[idx]
+        ho = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        hi = np.concatenate([w.hist_ids[w.hist_offsets[r]:w.hist_offsets[r + 1]] for r in idx]).astype(np.int32)
+    return dataclasses.replace(w, logits=w.logits[idx].copy(), params=w.params[idx].copy(), hist_offsets=ho,
+                               hist_ids=hi)
+
+
+@pytest.mark.parametrize("name,B,force", [("adversarial_ties", 64, False), ("mixed_quarters", 16, True),
+                                          ("penalized", 24, True), ("adversarial_ties", 8, False)])
+def test_split_finish_matches_one_cta_per_row(cuda_lib, name, B, force):
+    """A small batch finishes each row on a cluster of CTAs that splits the
+    threshold bisection; the same rows at the head of a batch too large for
+    that (one finish CTA per row, same slices) give identical tokens and
+    debug records, and the split rows match the oracle."""
+    S = cuda_lib
+    w, _ = named(name)
+    small, big = _rows(w, B), _rows(w, B, reps=(320 + B - 1) // B)
+    mhl = 256 if w.hist_offsets is not None else 0
+    s = 16 if w.dtype == wl.DTYPE_BF16 else 32  # the fewest slices a 129,280-id row allows
+    assert S.plan(small.B, w.V, w.dtype, ctas_per_row=s).finish_ctas > 1
+    assert S.plan(big.B, w.V, w.dtype, ctas_per_row=s).finish_ctas == 1
+    t1, d1, e1 = run(S, small, ctas_per_row=s, max_hist_len=mhl, force_bisection=force)
+    t2, d2, e2 = run(S, big, ctas_per_row=s, max_hist_len=mhl, force_bisection=force)
+    assert np.array_equal(t1, t2[:B])
+    assert np.array_equal(d1, d2[:B])
+    filtered = d1["mode"] == 2
+    assert (d1["passes"][filtered] >= 2).any()  # the bisection ran on split rows
+    res = oracle.sample_batch(small.logits_f32(), small.params, small.hist_offsets, small.hist_ids)
+    rep = parity.check_batch(small, t1, d1, results=res)
+    assert rep.set_exempt + rep.token_exempt <= max(2, B // 50)
+
+
 def test_graph_replay_reads_step_from_device(cuda_lib):
     """A captured launch replayed 64 times draws 64 different steps (generator state on device)."""
     import torch
