@@ -212,4 +212,13 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     }
 }
 
+// The patch-table position of a patched id at bit li of the bitmap: patches
+// before its word (kept per even word), before it in its word.
+__device__ __forceinline__ int patch_word_base(const uint32_t* bm, const uint32_t* wp, int w) {
+    return static_cast<int>(wp[w >> 1] + ((w & 1) ? __popc(bm[w - 1]) : 0u));
+}
+__device__ __forceinline__ int patch_rank(const uint32_t* bm, const uint32_t* wp, int li) {
+    return patch_word_base(bm, wp, li >> 5) + __popc(bm[li >> 5] & ((1u << (li & 31)) - 1u));
+}
+
 }  // namespace arc

@@ -127,21 +127,21 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     int64_t scan_smem = 0;
     if (has_hist) {
         const int64_t nwords = (int64_t{kVpt} * kThreads * vec + 31) / 32;
-        scan_smem = 2 * nwords * 4 + 2 * int64_t{cap} * 4;
+        scan_smem = nwords * 4 + (nwords + 1) / 2 * 4 + 2 * int64_t{cap} * 4;
     }
     auto r128 = [](int64_t x) { return ((x + 127) / 128) * 128; };
     const int64_t cmax_bytes = r128(s * kChunks * 4);
     const int64_t cs_bytes = 3 * cmax_bytes;  // masses, max ids, second largest logits
     const int64_t clist_bytes = r128((s * kChunks + kWarps) * 4);
-    const int64_t cand_bytes = r128(int64_t{kCandCap} * 16);
-    const int64_t stage_bytes = cand_bytes;  // the candidates in rank order
+    const int64_t cand_bytes = r128(int64_t{kCandCap} * 8);     // (key, id) as one 64-bit value
+    const int64_t stage_bytes = r128(int64_t{kCandCap} * 16);   // in rank order: key, id, mass
     const int64_t nv_row = (V + vec - 1) / vec;
     const int64_t fb_rounds = (nv_row + kThreads - 1) / kThreads;
     const int64_t fb_wsum = r128(fb_rounds * kWarps * 8);
     int64_t fb_patch = 0;
     if (has_hist) {
         const int64_t nwords = (fb_rounds * kThreads * vec + 31) / 32;
-        fb_patch = r128(2 * nwords * 4 + 2 * int64_t{cap} * 4);
+        fb_patch = r128(nwords * 4 + (nwords + 1) / 2 * 4 + 2 * int64_t{cap} * 4);
     }
     // the chunk max vectors of a filtered row, when they fit in 16 KB (else
     // the finish reads them from the logits)
@@ -152,10 +152,12 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     auto fits_two = [&](int64_t dyn) { return 2 * (dyn + per_cta_extra) <= kSmemPerSM; };
     const int64_t fin_base = cmax_bytes + cs_bytes + clist_bytes + cand_bytes + stage_bytes + fb_wsum + fb_patch;
     int64_t cmv_bytes = cmv_raw <= 16384 ? r128(cmv_raw) : 0;
-    // (not at the price of the second CTA per SM)
-    if (fits_two(fin_base) && !fits_two(fin_base + 2 * cmv_bytes)) cmv_bytes = 0;
+    // the wide entries of large-k rows stay (they give those rows a floor);
+    // the max vectors (which only save a re-read) not at the price of the
+    // second CTA per SM
+    if (fits_two(fin_base + cmv_bytes) && !fits_two(fin_base + 2 * cmv_bytes)) cmv_bytes = 0;
     // and the wide entries of top-k rows with a large k, under the same bound
-    const int64_t cwide_bytes = cmv_bytes;
+    const int64_t cwide_bytes = cmv_raw <= 16384 ? r128(cmv_raw) : 0;
     const int64_t fin_smem = fin_base + cmv_bytes + cwide_bytes;
     int64_t limit = kSmemPerBlock - static_cast<int64_t>(sizeof(KernelShared)) - 1024;
     if (cluster) limit -= kSummaryBytes + static_cast<int64_t>(sizeof(ScanShared));

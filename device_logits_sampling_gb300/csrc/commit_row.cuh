@@ -22,15 +22,16 @@ __device__ __forceinline__ void store_word_sys(void* p, uint32_t value, uint32_t
     asm volatile("st.relaxed.sys.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
 
-// Row r's commit as record number idx: checks token and position before any
-// write, then (when both pass) next_ids[r] = tok and positions[r] += 1, then
-// the record's three words, each carrying the stamp idx + 1.  Returns the
-// row's ARC_COMMIT_* bits.  No fence: a host accepts the slot only once all
-// three words show the same stamp, so their order does not matter.
-__device__ __forceinline__ uint32_t commit_row(int32_t tok, int64_t r, uint64_t idx, int32_t V, int32_t* next_ids,
-                                               int32_t* positions, int32_t max_position, const uint32_t* owners,
-                                               arc_commit_record* ring, uint32_t capacity) {
-    const int32_t pos = positions[r];
+// Row r's commit as record number idx, its position `pos` and owner tag
+// already read: checks token and position before any write, then (when both
+// pass) next_ids[r] = tok and positions[r] = pos + 1, then the record's three
+// words, each carrying the stamp idx + 1.  Returns the row's ARC_COMMIT_*
+// bits.  No fence: a host accepts the slot only once all three words show the
+// same stamp, so their order does not matter.
+__device__ __forceinline__ uint32_t commit_row_read(int32_t tok, int32_t pos, uint32_t owner, int64_t r, uint64_t idx,
+                                                    int32_t V, int32_t* next_ids, int32_t* positions,
+                                                    int32_t max_position, arc_commit_record* ring,
+                                                    uint32_t capacity) {
     uint32_t bad = 0;
     if (tok < 0 || tok >= V) bad |= ARC_COMMIT_BAD_TOKEN;
     if (pos < 0 || pos >= max_position) bad |= ARC_COMMIT_BAD_POSITION;
@@ -42,8 +43,16 @@ __device__ __forceinline__ uint32_t commit_row(int32_t tok, int64_t r, uint64_t 
     const uint32_t stamp = static_cast<uint32_t>(idx + 1);
     store_word_sys(&rec->token, static_cast<uint32_t>(bad ? -1 : tok), stamp);
     store_word_sys(&rec->position, static_cast<uint32_t>(pos), stamp);
-    store_word_sys(&rec->owner, owners ? owners[r] : 0u, stamp);
+    store_word_sys(&rec->owner, owner, stamp);
     return bad;
+}
+
+// The same, reading the row's position and owner tag first.
+__device__ __forceinline__ uint32_t commit_row(int32_t tok, int64_t r, uint64_t idx, int32_t V, int32_t* next_ids,
+                                               int32_t* positions, int32_t max_position, const uint32_t* owners,
+                                               arc_commit_record* ring, uint32_t capacity) {
+    return commit_row_read(tok, positions[r], owners ? owners[r] : 0u, r, idx, V, next_ids, positions, max_position,
+                           ring, capacity);
 }
 
 }  // namespace arc

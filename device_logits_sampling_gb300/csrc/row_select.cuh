@@ -135,7 +135,7 @@ struct RowCtx {
             const uint32_t word = bm[l0 >> 5];
             const uint32_t bits = (word >> (l0 & 31)) & ((1u << VEC) - 1u);
             if (bits) {
-                const int base = static_cast<int>(wp[l0 >> 5]);
+                const int base = patch_word_base(bm, wp, l0 >> 5);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     const int li = l0 + e;

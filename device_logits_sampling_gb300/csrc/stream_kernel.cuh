@@ -113,7 +113,9 @@ struct FinishScratch {
     float bf[8];
     uint32_t ccount;  // candidates gathered
     uint32_t nwhole;  // chunks listed for a whole read
-    unsigned long long chead;  // decode-loop commit: the ring head this call read
+    unsigned long long chead;  // decode-loop commit: the ring head this call read,
+    int32_t cpos;              //   the row's position
+    uint32_t cown;             //   and owner tag
     uint32_t fc[2][kWarps][4];  // floor search partial counts
     double bd[2];
 };
@@ -227,16 +229,16 @@ __device__ int build_patches(const char* rowp, int V, int a0, int n, int nvec, c
         if (w < warp) wbase += red32[w];
         distinct += red32[w];
     }
+    // the rank of word w's first bit is kept for even w only (half the
+    // table): an odd word adds its even neighbour's bit count
     uint32_t run = wbase + inc - mine;
     for (int w = w0; w < w1; ++w) {
-        wp[w] = run;
+        if (!(w & 1)) wp[w >> 1] = run;
         run += __popc(bm[w]);
     }
     for (int q = tid; q < static_cast<int>(distinct); q += kThreads) cnt[q] = 0;
     __syncthreads();
-    auto rank_of = [&](int li) {
-        return static_cast<int>(wp[li >> 5] + __popc(bm[li >> 5] & ((1u << (li & 31)) - 1u)));
-    };
+    auto rank_of = [&](int li) { return patch_rank(bm, wp, li); };
     for (int e = tid; e < hn; e += kThreads) {
         const int id = ids[e];
         if (id >= a0 && id < a1) atomicAdd(&cnt[rank_of(id - a0)], 1u);
@@ -265,7 +267,7 @@ __device__ __forceinline__ void apply_patches(const uint32_t* bm, const uint32_t
     const uint32_t word = bm[l0 >> 5];
     const uint32_t bits = (word >> (l0 & 31)) & ((1u << VEC) - 1u);
     if (bits) {
-        const int base = static_cast<int>(wp[l0 >> 5]);
+        const int base = patch_word_base(bm, wp, l0 >> 5);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
             const int li = l0 + e;
@@ -503,7 +505,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         const int nwords_max = (kVpt * kThreads * VEC + 31) / 32;
         uint32_t* bm = reinterpret_cast<uint32_t*>(patch_mem);
         uint32_t* wp = bm + nwords_max;
-        uint32_t* cnt = wp + nwords_max;
+        uint32_t* cnt = wp + (nwords_max + 1) / 2;
         float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
         const int distinct = build_patches<DT>(rowp, a.V, a0, n, nv, R.P, a.hist_ids + R.hbeg, R.hn, bm, wp, cnt,
                                                pat, sh.red32, &sh.sflags);
@@ -1154,7 +1156,7 @@ __device__ __noinline__ void top_n_row(const FinishArgs& a, int row, const arc_r
         const int nwords_max = (a.fb_rounds * kThreads * VEC + 31) / 32;
         uint32_t* bm = reinterpret_cast<uint32_t*>(dyn + a.fb_patch_off);
         uint32_t* wp = bm + nwords_max;
-        uint32_t* cnt = wp + nwords_max;
+        uint32_t* cnt = wp + (nwords_max + 1) / 2;
         float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
         __syncthreads();
         if (tid == 0) SS.bi[7] = 0;
@@ -1390,14 +1392,19 @@ __device__ __forceinline__ void sorted_select(const FinishArgs& a, const arc_row
 // calls both).
 // The decode-loop commit of this CTA's row as record head[0] + row (the
 // commit of arc_decode.h, one row per CTA), in two parts.  commit_arrive, in
-// the prologue: read head[0], then arrive on head[1] with an acquire-release
+// the prologue: read head[0] (and the row's position and owner), then arrive
+// on head[1] with an acquire-release
 // atomic; the CTA that arrives last has seen every other arrival, hence every
 // read of head[0], so it advances head[0] by B and leaves head[1] at 0 for the
 // next call.  commit_publish, after the token: the row's checks, writes and
 // record (no fence, no atomic but the fault bits).
-__device__ __forceinline__ unsigned long long commit_arrive(const FinishArgs& a) {
+__device__ __forceinline__ void commit_arrive(const FinishArgs& a, int row, FinishScratch& SS) {
     unsigned long long* head = reinterpret_cast<unsigned long long*>(a.commit.head);
     unsigned long long h, n;
+    // the row's position and owner tag load with the head (no kernel of the
+    // call writes them before the commit)
+    SS.cpos = a.commit.positions[row];
+    SS.cown = a.commit.owners ? a.commit.owners[row] : 0u;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(h) : "l"(head) : "memory");
     asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(n) : "l"(head + 1) : "memory");
     if (n == static_cast<unsigned long long>(a.B) - 1ull) {
@@ -1405,12 +1412,12 @@ __device__ __forceinline__ unsigned long long commit_arrive(const FinishArgs& a)
         asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(head), "l"(h + static_cast<unsigned long long>(a.B))
                      : "memory");
     }
-    return h;
+    SS.chead = h;
 }
-__device__ __forceinline__ void commit_publish(const FinishArgs& a, int row, int32_t tok, unsigned long long h) {
+__device__ __forceinline__ void commit_publish(const FinishArgs& a, int row, int32_t tok, const FinishScratch& SS) {
     const arc_commit_target& c = a.commit;
-    const uint32_t bad = commit_row(tok, row, h + static_cast<unsigned long long>(row), a.V, c.next_ids, c.positions,
-                                    c.max_position, c.owners, c.ring, c.capacity);
+    const uint32_t bad = commit_row_read(tok, SS.cpos, SS.cown, row, SS.chead + static_cast<unsigned long long>(row),
+                                         a.V, c.next_ids, c.positions, c.max_position, c.ring, c.capacity);
     if (bad != 0 && c.fault_word != nullptr) atomicOr(c.fault_word, bad);
 }
 
@@ -1454,7 +1461,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
     // the decode-loop commit's ring index: read (and the head advanced) while
     // the scan still runs; the head is no kernel's but the commit's
     const bool leader = rank == 0;  // the CTA that writes the row's results
-    if (a.commit.ring != nullptr && leader && tid == 0) SS.chead = commit_arrive(a);
+    if (a.commit.ring != nullptr && leader && tid == 0) commit_arrive(a, row, SS);
     // the summaries are complete and visible after this (the parameters and
     // history above are not written by the scan)
     wait();
@@ -1715,7 +1722,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                 const int nwords_max = (a.fb_rounds * kThreads * VEC + 31) / 32;
                 uint32_t* bm = reinterpret_cast<uint32_t*>(dyn + a.fb_patch_off);
                 uint32_t* wp = bm + nwords_max;
-                uint32_t* cnt = wp + nwords_max;
+                uint32_t* cnt = wp + (nwords_max + 1) / 2;
                 float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
                 __syncthreads();
                 if (tid == 0) SS.bi[7] = 0;
@@ -2035,7 +2042,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
             dbg.target = st.target;
         }
         if (a.flags & ARC_OPT_STEP_AUTOINC) a.params[row].step = P.step + 1;
-        if (a.commit.ring != nullptr) commit_publish(a, row, st.token, SS.chead);
+        if (a.commit.ring != nullptr) commit_publish(a, row, st.token, SS);
     }
 }
 
