@@ -1456,8 +1456,8 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
     // the finish needs the chunk max vectors (filtered rows)
     const bool want_mv = a.cmv_off >= 0 && param_errors(P) == 0 && (RowMode(P, a.V).filtered || a.top_n > 0);
     // a top-k row with a large k: the wide entries too
-    const bool want_wide = want_mv && a.cwide_off >= 0 && RowMode(P, a.V).filtered && P.top_k > kWideK &&
-                           P.top_k < a.V;
+    const bool want_wide = a.cwide_off >= 0 && param_errors(P) == 0 && RowMode(P, a.V).filtered &&
+                           P.top_k > kWideK && P.top_k < a.V;
     // the decode-loop commit's ring index: read (and the head advanced) while
     // the scan still runs; the head is no kernel's but the commit's
     const bool leader = rank == 0;  // the CTA that writes the row's results

@@ -328,6 +328,8 @@ def test_enumeration_and_bisection_agree(cuda_lib, name):
     direct = int((d1["passes"][filtered] == 1).sum())
     print(f"{name}: filtered rows {int(filtered.sum())}, direct selection {direct}, "
           f"bisection {int(filtered.sum()) - direct}")
+    if name != "adversarial_ties":  # (whose tied nucleus holds tens of thousands of ids)
+        assert direct >= 0.9 * int(filtered.sum())
 
 
 def _rows(w, B, reps=1):
