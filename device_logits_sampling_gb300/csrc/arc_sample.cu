@@ -127,7 +127,7 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     int64_t scan_smem = 0;
     if (has_hist) {
         const int64_t nwords = (int64_t{kVpt} * kThreads * vec + 31) / 32;
-        scan_smem = nwords * 4 + (nwords + 1) / 2 * 4 + int64_t{cap} * 4;  // bitmap, word ranks, counts
+        scan_smem = nwords * 4 + (nwords + 1) / 2 * 4 + 2 * int64_t{cap} * 4;
     }
     auto r128 = [](int64_t x) { return ((x + 127) / 128) * 128; };
     const int64_t cmax_bytes = r128(s * kChunks * 4);

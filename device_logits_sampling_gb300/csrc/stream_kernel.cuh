@@ -193,16 +193,7 @@ struct RowMode {
 // history: a bitmap of those ids, per-word prefix popcounts (rank of an id),
 // and per-rank counts and penalised logits.  Returns the number of distinct
 // ids; sets ARC_ERR_HIST_ID in *bad for ids outside [0, V).
-// The penalised logit of an id seen c > 0 times in the row's history:
-// repetition (divide a positive logit, multiply a negative one), then
-// frequency (c times) and presence, each an fp32 round-to-nearest operation.
-__device__ __forceinline__ float penalise(float z, uint32_t c, float rep, float fr, float pr) {
-    z = (z > 0.0f) ? __fdiv_rn(z, rep) : __fmul_rn(z, rep);
-    z = __fsub_rn(z, __fmul_rn(static_cast<float>(c), fr));
-    return __fsub_rn(z, pr);
-}
-
-template <int DT, bool VALUES = true>
+template <int DT>
 __device__ int build_patches(const char* rowp, int V, int a0, int n, int nvec, const arc_row_params& P,
                              const int32_t* ids, int hn, uint32_t* bm, uint32_t* wp, uint32_t* cnt, float* pat,
                              uint32_t* red32, uint32_t* bad) {
@@ -211,13 +202,10 @@ __device__ int build_patches(const char* rowp, int V, int a0, int n, int nvec, c
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int a1 = a0 + n;
     const int nwords = (nvec * VEC + 31) / 32;
-    // the thread's first history id stays in a register for the passes below
-    const int id_first = tid < hn ? ids[tid] : -1;
-    auto id_at = [&](int e) { return e == tid ? id_first : ids[e]; };
     for (int w = tid; w < nwords; w += kThreads) bm[w] = 0;
     __syncthreads();
     for (int e = tid; e < hn; e += kThreads) {
-        const int id = id_at(e);
+        const int id = ids[e];
         if (id < 0 || id >= V)
             atomicOr(bad, ARC_ERR_HIST_ID);
         else if (id >= a0 && id < a1)
@@ -252,23 +240,23 @@ __device__ int build_patches(const char* rowp, int V, int a0, int n, int nvec, c
     __syncthreads();
     auto rank_of = [&](int li) { return patch_rank(bm, wp, li); };
     for (int e = tid; e < hn; e += kThreads) {
-        const int id = id_at(e);
+        const int id = ids[e];
         if (id >= a0 && id < a1) atomicAdd(&cnt[rank_of(id - a0)], 1u);
     }
     __syncthreads();
-    if (VALUES) {
-        // the penalised values themselves (readers without the raw logits at
-        // hand); without VALUES the reader penalises its own copy from cnt
-        const float rep = P.repetition_penalty, fr = P.frequency_penalty, pr = P.presence_penalty;
-        for (int e = tid; e < hn; e += kThreads) {
-            const int id = id_at(e);
-            if (id >= a0 && id < a1) {
-                const int q = rank_of(id - a0);
-                pat[q] = penalise(E::load_scalar(rowp, id), cnt[q], rep, fr, pr);  // duplicates store the same value
-            }
+    const float rep = P.repetition_penalty, fr = P.frequency_penalty, pr = P.presence_penalty;
+    for (int e = tid; e < hn; e += kThreads) {
+        const int id = ids[e];
+        if (id >= a0 && id < a1) {
+            const int q = rank_of(id - a0);
+            float z = E::load_scalar(rowp, id);
+            z = (z > 0.0f) ? __fdiv_rn(z, rep) : __fmul_rn(z, rep);
+            z = __fsub_rn(z, __fmul_rn(static_cast<float>(cnt[q]), fr));
+            z = __fsub_rn(z, pr);
+            pat[q] = z;  // duplicates of an id store the same value
         }
-        __syncthreads();
     }
+    __syncthreads();
     return static_cast<int>(distinct);
 }
 
@@ -284,24 +272,6 @@ __device__ __forceinline__ void apply_patches(const uint32_t* bm, const uint32_t
         for (int e = 0; e < VEC; ++e) {
             const int li = l0 + e;
             if ((bits >> e) & 1u) z[e] = pat[base + __popc(word & ((1u << (li & 31)) - 1u))];
-        }
-    }
-}
-
-// apply_patches for a reader holding the raw logits: the patched ids of
-// vector v penalised from their history counts.
-template <int VEC>
-__device__ __forceinline__ void apply_counts(const uint32_t* bm, const uint32_t* wp, const uint32_t* cnt, float rep,
-                                             float fr, float pr, int v, float (&z)[VEC]) {
-    const int l0 = v * VEC;
-    const uint32_t word = bm[l0 >> 5];
-    const uint32_t bits = (word >> (l0 & 31)) & ((1u << VEC) - 1u);
-    if (bits) {
-        const int base = patch_word_base(bm, wp, l0 >> 5);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            const int li = l0 + e;
-            if ((bits >> e) & 1u) z[e] = penalise(z[e], cnt[base + __popc(word & ((1u << (li & 31)) - 1u))], rep, fr, pr);
         }
     }
 }
@@ -526,7 +496,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
 
     const uint32_t* pbm = nullptr;
     const uint32_t* pwp = nullptr;
-    const uint32_t* pcnt = nullptr;
+    const float* ppat = nullptr;
     bool has_patch = false;
     if (HIST && rerr == 0 && R.hn > 0) {
         if (threadIdx.x == 0) sh.sflags = 0;
@@ -536,20 +506,18 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
         uint32_t* bm = reinterpret_cast<uint32_t*>(patch_mem);
         uint32_t* wp = bm + nwords_max;
         uint32_t* cnt = wp + (nwords_max + 1) / 2;
-        const int distinct = build_patches<DT, false>(rowp, a.V, a0, n, nv, R.P, a.hist_ids + R.hbeg, R.hn, bm, wp,
-                                                      cnt, nullptr, sh.red32, &sh.sflags);
+        float* pat = reinterpret_cast<float*>(cnt + a.hist_cap);
+        const int distinct = build_patches<DT>(rowp, a.V, a0, n, nv, R.P, a.hist_ids + R.hbeg, R.hn, bm, wp, cnt,
+                                               pat, sh.red32, &sh.sflags);
         rerr |= sh.sflags & ARC_ERR_HIST_ID;
         pbm = bm;
         pwp = wp;
-        pcnt = cnt;
+        ppat = pat;
         has_patch = distinct > 0;
     }
-    // the slice's logits are in registers: patched ids are penalised from
-    // their counts
-    const float rep = R.P.repetition_penalty, fr = R.P.frequency_penalty, pr = R.P.presence_penalty;
     auto vals = [&](int j, float (&z)[VEC]) {
         E::unpack(d[j], z);
-        if (HIST && has_patch) apply_counts<VEC>(pbm, pwp, pcnt, rep, fr, pr, j * kThreads + tid, z);
+        if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, j * kThreads + tid, z);
     };
     auto patched = [&](int j) {
         if (!(HIST && has_patch)) return false;
@@ -710,7 +678,7 @@ __device__ __forceinline__ void scan_slice(const ScanArgs& a, const uint4 (&d)[k
                 const uint4 dv = pick(d, jw);
                 float z[VEC];
                 E::unpack(dv, z);
-                if (HIST && has_patch) apply_counts<VEC>(pbm, pwp, pcnt, rep, fr, pr, jw * kThreads + tid, z);
+                if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, jw * kThreads + tid, z);
                 int e0 = VEC - 1;
 #pragma unroll
                 for (int e = VEC - 1; e >= 0; --e)
