@@ -113,6 +113,9 @@ struct FinishScratch {
     float bf[8];
     uint32_t ccount;  // candidates gathered
     uint32_t nwhole;  // chunks listed for a whole read
+    int draw_bin;              // draw over many survivors: the id range holding the target,
+    uint32_t draw_n;           //   its survivors,
+    uint64_t draw_base;        //   the mass of the ranges before it
     unsigned long long chead;  // decode-loop commit: the ring head this call read,
     int32_t cpos;              //   the row's position
     uint32_t cown;             //   and owner tag
@@ -1285,7 +1288,8 @@ __device__ __noinline__ void top_n_row(const FinishArgs& a, int row, const arc_r
 template <int POS>
 __device__ __forceinline__ void sorted_select(const FinishArgs& a, const arc_row_params& P, const RowMode& md,
                                               RowState& st, FinishScratch& SS, const uint32_t* sk, const int* sid,
-                                              const uint64_t* sm, int nk, float zm, const Surv& K) {
+                                              const uint64_t* sm, int nk, float zm, const Surv& K, uint32_t* bins,
+                                              uint32_t* scratch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
         // thread t holds sorted positions [POS t, POS t + POS), read once as
         // 16-byte vectors (kCandCap = POS kThreads: always inside the arrays)
@@ -1374,14 +1378,62 @@ __device__ __forceinline__ void sorted_select(const FinishArgs& a, const arc_row
             st.mass_r = mr;
         }
         st.target = scale_by_u(st.rbits, st.mass_r);
-        // the draw in id order: each survivor sums the survivors with smaller ids
-        for (int pp = tid; pp < nsv; pp += kThreads) {
-            const int ip = sid[pp];
-            const uint64_t mp = sm[pp];
-            uint64_t before = 0;
+        if (nsv <= kRankMax) {
+            // the draw in id order: each survivor sums the survivors with smaller ids
+            for (int pp = tid; pp < nsv; pp += kThreads) {
+                const int ip = sid[pp];
+                const uint64_t mp = sm[pp];
+                uint64_t before = 0;
 #pragma unroll 8
-            for (int qq = 0; qq < nsv; ++qq) before += (sid[qq] < ip) ? sm[qq] : 0u;
-            if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
+                for (int qq = 0; qq < nsv; ++qq) before += (sid[qq] < ip) ? sm[qq] : 0u;
+                if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
+            }
+        } else {
+            // many survivors: their masses by id range (kThreads ranges in id
+            // order, each bin's 64-bit sum as two 32-bit words with exact
+            // carry), the range holding the target, then that range's
+            // survivors in id order
+            auto range_of = [&](int id) {
+                return static_cast<int>((static_cast<uint64_t>(id) * kThreads) / static_cast<uint64_t>(a.V));
+            };
+            bins[2 * tid] = 0u;
+            bins[2 * tid + 1] = 0u;
+            if (tid == 0) SS.draw_n = 0;
+            __syncthreads();
+            for (int pp = tid; pp < nsv; pp += kThreads) {
+                const uint64_t mp = sm[pp];
+                uint32_t* h = &bins[2 * range_of(sid[pp])];
+                const uint32_t lo = static_cast<uint32_t>(mp), hi = static_cast<uint32_t>(mp >> 32);
+                const uint32_t old = atomicAdd(h, lo);
+                const uint32_t carry = (old + lo < old) ? 1u : 0u;
+                if (hi + carry) atomicAdd(h + 1, hi + carry);
+            }
+            __syncthreads();
+            const uint64_t mine = (static_cast<uint64_t>(bins[2 * tid + 1]) << 32) | bins[2 * tid];
+            uint64_t tot_r;
+            const uint64_t inc = block_scan_u64(mine, SS.redu, tot_r);
+            if (tid == 0) SS.draw_bin = -1;
+            __syncthreads();
+            if (mine != 0 && inc - mine <= st.target && st.target < inc) {
+                SS.draw_bin = tid;
+                SS.draw_base = inc - mine;
+            }
+            __syncthreads();
+            const int rb = SS.draw_bin;
+            const uint64_t base = SS.draw_base;
+            // the range's survivors by sorted position (at most nsv <= 2,048)
+            for (int pp = tid; pp < nsv; pp += kThreads) {
+                if (range_of(sid[pp]) == rb) scratch[atomicAdd(&SS.draw_n, 1u)] = static_cast<uint32_t>(pp);
+            }
+            __syncthreads();
+            const int nr = static_cast<int>(SS.draw_n);
+            for (int i = tid; i < nr; i += kThreads) {
+                const int ip = sid[scratch[i]];
+                const uint64_t mp = sm[scratch[i]];
+                uint64_t before = base;
+                for (int j = 0; j < nr; ++j) before += (sid[scratch[j]] < ip) ? sm[scratch[j]] : 0u;
+                if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
+            }
         }
 }
 
@@ -1899,11 +1951,37 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                         }
 #pragma unroll
                         for (int u = 0; u < kU; ++u) {
+                            float z[VEC];
+                            int cnt = 0;
                             if (vr[u] >= 0) {
-                                float z[VEC];
                                 E::unpack(raw[u], z);
                                 if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, vr[u], z);
-                                emit(z, vr[u]);
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
+                            }
+                            // the warp's slots from one shared atomic (a listed
+                            // chunk often holds many ids at or above the floor)
+                            if (__ballot_sync(0xFFFFFFFFu, cnt > 0) == 0u) continue;
+                            int inc = cnt;
+#pragma unroll
+                            for (int dd = 1; dd < 32; dd <<= 1) {
+                                const int o = __shfl_up_sync(0xFFFFFFFFu, inc, dd);
+                                if (lane >= dd) inc += o;
+                            }
+                            uint32_t base = 0;
+                            if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(inc));
+                            base = __shfl_sync(0xFFFFFFFFu, base, 31);
+                            uint32_t pos = base + static_cast<uint32_t>(inc - cnt);
+                            if (cnt > 0) {
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e) {
+                                    if (z[e] >= zf) {
+                                        if (pos < static_cast<uint32_t>(kCandCap))
+                                            cc[pos] = (static_cast<uint64_t>(fkey(z[e])) << 32) |
+                                                      (0xFFFFFFFFu - static_cast<uint32_t>(vr[u] * VEC + e));
+                                        ++pos;
+                                    }
+                                }
                             }
                         }
                     }
@@ -1941,9 +2019,10 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                     for (int i = nc + tid; i < n2; i += kThreads) cc[i] = 0;
                     __syncthreads();
                     for (int size = 2; size <= n2; size <<= 1) {
-                        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                        for (int ls = __ffs(size) - 2; ls >= 0; --ls) {  // stride 2^ls
+                            const int stride = 1 << ls;
                             for (int i = tid; i < (n2 >> 1); i += kThreads) {
-                                const int lo = (i / stride) * 2 * stride + (i % stride), hi = lo + stride;
+                                const int lo = ((i >> ls) << (ls + 1)) | (i & (stride - 1)), hi = lo + stride;
                                 const uint64_t x = cc[lo], y = cc[hi];
                                 if ((x < y) == ((lo & size) == 0)) {  // descending where lo & size == 0
                                     cc[lo] = y;
@@ -2000,9 +2079,11 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                     }
                 } else {
                     if (nc <= 4 * kThreads)
-                        sorted_select<4>(a, P, md, st, SS, sk, sid, sm, nk, zm, K);
+                        sorted_select<4>(a, P, md, st, SS, sk, sid, sm, nk, zm, K,
+                                         reinterpret_cast<uint32_t*>(KS.fb.lhist), reinterpret_cast<uint32_t*>(cc));
                     else
-                        sorted_select<8>(a, P, md, st, SS, sk, sid, sm, nk, zm, K);
+                        sorted_select<8>(a, P, md, st, SS, sk, sid, sm, nk, zm, K,
+                                         reinterpret_cast<uint32_t*>(KS.fb.lhist), reinterpret_cast<uint32_t*>(cc));
                 }
                 __syncthreads();
                 st.token = SS.bi[6];
