@@ -1951,37 +1951,11 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                         }
 #pragma unroll
                         for (int u = 0; u < kU; ++u) {
-                            float z[VEC];
-                            int cnt = 0;
                             if (vr[u] >= 0) {
+                                float z[VEC];
                                 E::unpack(raw[u], z);
                                 if (HIST && has_patch) apply_patches<VEC>(pbm, pwp, ppat, vr[u], z);
-#pragma unroll
-                                for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
-                            }
-                            // the warp's slots from one shared atomic (a listed
-                            // chunk often holds many ids at or above the floor)
-                            if (__ballot_sync(0xFFFFFFFFu, cnt > 0) == 0u) continue;
-                            int inc = cnt;
-#pragma unroll
-                            for (int dd = 1; dd < 32; dd <<= 1) {
-                                const int o = __shfl_up_sync(0xFFFFFFFFu, inc, dd);
-                                if (lane >= dd) inc += o;
-                            }
-                            uint32_t base = 0;
-                            if (lane == 31) base = atomicAdd(&SS.ccount, static_cast<uint32_t>(inc));
-                            base = __shfl_sync(0xFFFFFFFFu, base, 31);
-                            uint32_t pos = base + static_cast<uint32_t>(inc - cnt);
-                            if (cnt > 0) {
-#pragma unroll
-                                for (int e = 0; e < VEC; ++e) {
-                                    if (z[e] >= zf) {
-                                        if (pos < static_cast<uint32_t>(kCandCap))
-                                            cc[pos] = (static_cast<uint64_t>(fkey(z[e])) << 32) |
-                                                      (0xFFFFFFFFu - static_cast<uint32_t>(vr[u] * VEC + e));
-                                        ++pos;
-                                    }
-                                }
+                                emit(z, vr[u]);
                             }
                         }
                     }
