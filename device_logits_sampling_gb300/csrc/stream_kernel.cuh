@@ -1285,11 +1285,86 @@ __device__ __noinline__ void top_n_row(const FinishArgs& a, int row, const arc_r
 // cutoff, min-p, the survivors' mass and the draw in id order.  Thread t holds
 // sorted positions [POS t, POS t + POS): POS = 4 covers 1,024 candidates, 8
 // covers 2,048 (kept apart, so that the common case carries no extra work).
+// Bitonic sort of v[0, n2) (n2 a power of two), descending, by the whole
+// CTA, v[nc, n2) padded with zeros first.  Out of line: the counting rank of
+// few candidates keeps its registers.
+static __device__ __noinline__ void bitonic_desc(uint64_t* v, int nc, int n2) {
+    const int tid = threadIdx.x;
+    for (int i = nc + tid; i < n2; i += kThreads) v[i] = 0;
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int ls = __ffs(size) - 2; ls >= 0; --ls) {  // stride 2^ls
+            const int stride = 1 << ls;
+            for (int i = tid; i < (n2 >> 1); i += kThreads) {
+                const int lo = ((i >> ls) << (ls + 1)) | (i & (stride - 1)), hi = lo + stride;
+                const uint64_t x = v[lo], y = v[hi];
+                if ((x < y) == ((lo & size) == 0)) {  // descending where lo & size == 0
+                    v[lo] = y;
+                    v[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// The draw over many survivors in id order (sorted_select): their masses by
+// id range (kThreads ranges in id order, each bin's 64-bit sum as two 32-bit
+// words with exact carry), the range holding the target, then that range's
+// survivors in id order.  Out of line: the common few-survivor draw keeps its
+// registers.
+static __device__ __noinline__ void draw_by_id_range(const FinishArgs& a, uint64_t target, FinishScratch& SS,
+                                                     const int* sid, const uint64_t* sm, int nsv, uint32_t* bins,
+                                                     uint32_t* scratch) {
+    const int tid = threadIdx.x;
+    auto range_of = [&](int id) {
+        return static_cast<int>((static_cast<uint64_t>(id) * kThreads) / static_cast<uint64_t>(a.V));
+    };
+    bins[2 * tid] = 0u;
+    bins[2 * tid + 1] = 0u;
+    if (tid == 0) SS.draw_n = 0;
+    __syncthreads();
+    for (int pp = tid; pp < nsv; pp += kThreads) {
+        const uint64_t mp = sm[pp];
+        uint32_t* h = &bins[2 * range_of(sid[pp])];
+        const uint32_t lo = static_cast<uint32_t>(mp), hi = static_cast<uint32_t>(mp >> 32);
+        const uint32_t old = atomicAdd(h, lo);
+        const uint32_t carry = (old + lo < old) ? 1u : 0u;
+        if (hi + carry) atomicAdd(h + 1, hi + carry);
+    }
+    __syncthreads();
+    const uint64_t mine = (static_cast<uint64_t>(bins[2 * tid + 1]) << 32) | bins[2 * tid];
+    uint64_t tot_r;
+    const uint64_t inc = block_scan_u64(mine, SS.redu, tot_r);
+    if (tid == 0) SS.draw_bin = -1;
+    __syncthreads();
+    if (mine != 0 && inc - mine <= target && target < inc) {
+        SS.draw_bin = tid;
+        SS.draw_base = inc - mine;
+    }
+    __syncthreads();
+    const int rb = SS.draw_bin;
+    const uint64_t base = SS.draw_base;
+    // the range's survivors by sorted position (at most nsv <= 2,048)
+    for (int pp = tid; pp < nsv; pp += kThreads) {
+        if (range_of(sid[pp]) == rb) scratch[atomicAdd(&SS.draw_n, 1u)] = static_cast<uint32_t>(pp);
+    }
+    __syncthreads();
+    const int nr = static_cast<int>(SS.draw_n);
+    for (int i = tid; i < nr; i += kThreads) {
+        const int ip = sid[scratch[i]];
+        const uint64_t mp = sm[scratch[i]];
+        uint64_t before = base;
+        for (int j = 0; j < nr; ++j) before += (sid[scratch[j]] < ip) ? sm[scratch[j]] : 0u;
+        if (mp != 0 && before <= target && target < before + mp) SS.bi[6] = ip;
+    }
+}
+
 template <int POS>
 __device__ __forceinline__ void sorted_select(const FinishArgs& a, const arc_row_params& P, const RowMode& md,
                                               RowState& st, FinishScratch& SS, const uint32_t* sk, const int* sid,
                                               const uint64_t* sm, int nk, float zm, const Surv& K, uint32_t* bins,
-                                              uint32_t* scratch) {
+                                                     uint32_t* scratch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
         // thread t holds sorted positions [POS t, POS t + POS), read once as
         // 16-byte vectors (kCandCap = POS kThreads: always inside the arrays)
@@ -1389,51 +1464,7 @@ __device__ __forceinline__ void sorted_select(const FinishArgs& a, const arc_row
                 if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
             }
         } else {
-            // many survivors: their masses by id range (kThreads ranges in id
-            // order, each bin's 64-bit sum as two 32-bit words with exact
-            // carry), the range holding the target, then that range's
-            // survivors in id order
-            auto range_of = [&](int id) {
-                return static_cast<int>((static_cast<uint64_t>(id) * kThreads) / static_cast<uint64_t>(a.V));
-            };
-            bins[2 * tid] = 0u;
-            bins[2 * tid + 1] = 0u;
-            if (tid == 0) SS.draw_n = 0;
-            __syncthreads();
-            for (int pp = tid; pp < nsv; pp += kThreads) {
-                const uint64_t mp = sm[pp];
-                uint32_t* h = &bins[2 * range_of(sid[pp])];
-                const uint32_t lo = static_cast<uint32_t>(mp), hi = static_cast<uint32_t>(mp >> 32);
-                const uint32_t old = atomicAdd(h, lo);
-                const uint32_t carry = (old + lo < old) ? 1u : 0u;
-                if (hi + carry) atomicAdd(h + 1, hi + carry);
-            }
-            __syncthreads();
-            const uint64_t mine = (static_cast<uint64_t>(bins[2 * tid + 1]) << 32) | bins[2 * tid];
-            uint64_t tot_r;
-            const uint64_t inc = block_scan_u64(mine, SS.redu, tot_r);
-            if (tid == 0) SS.draw_bin = -1;
-            __syncthreads();
-            if (mine != 0 && inc - mine <= st.target && st.target < inc) {
-                SS.draw_bin = tid;
-                SS.draw_base = inc - mine;
-            }
-            __syncthreads();
-            const int rb = SS.draw_bin;
-            const uint64_t base = SS.draw_base;
-            // the range's survivors by sorted position (at most nsv <= 2,048)
-            for (int pp = tid; pp < nsv; pp += kThreads) {
-                if (range_of(sid[pp]) == rb) scratch[atomicAdd(&SS.draw_n, 1u)] = static_cast<uint32_t>(pp);
-            }
-            __syncthreads();
-            const int nr = static_cast<int>(SS.draw_n);
-            for (int i = tid; i < nr; i += kThreads) {
-                const int ip = sid[scratch[i]];
-                const uint64_t mp = sm[scratch[i]];
-                uint64_t before = base;
-                for (int j = 0; j < nr; ++j) before += (sid[scratch[j]] < ip) ? sm[scratch[j]] : 0u;
-                if (mp != 0 && before <= st.target && st.target < before + mp) SS.bi[6] = ip;
-            }
+            draw_by_id_range(a, st.target, SS, sid, sm, nsv, bins, scratch);
         }
 }
 
@@ -1990,22 +2021,7 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                 } else {
                     int n2 = kRankMax;
                     while (n2 < nc) n2 <<= 1;
-                    for (int i = nc + tid; i < n2; i += kThreads) cc[i] = 0;
-                    __syncthreads();
-                    for (int size = 2; size <= n2; size <<= 1) {
-                        for (int ls = __ffs(size) - 2; ls >= 0; --ls) {  // stride 2^ls
-                            const int stride = 1 << ls;
-                            for (int i = tid; i < (n2 >> 1); i += kThreads) {
-                                const int lo = ((i >> ls) << (ls + 1)) | (i & (stride - 1)), hi = lo + stride;
-                                const uint64_t x = cc[lo], y = cc[hi];
-                                if ((x < y) == ((lo & size) == 0)) {  // descending where lo & size == 0
-                                    cc[lo] = y;
-                                    cc[hi] = x;
-                                }
-                            }
-                            __syncthreads();
-                        }
-                    }
+                    bitonic_desc(cc, nc, n2);
                     for (int i = tid; i < nc; i += kThreads) {
                         const uint64_t vi = cc[i];
                         const uint32_t ki = static_cast<uint32_t>(vi >> 32);
