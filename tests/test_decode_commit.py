@@ -378,14 +378,16 @@ def test_captured_sample_and_commit_replay_drained_from_the_host(cuda_lib):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,B", [("mixed_quarters", 256), ("small_fp32", 4), ("single_row_peaked", 1)])
+@pytest.mark.parametrize("name,B", [("mixed_quarters", 256), ("small_fp32", 4), ("single_row_peaked", 1),
+                                    ("adversarial_ties", 8)])
 def test_commit_folded_into_the_sampler_matches_sample_then_commit(cuda_lib, name, B):
     """arc_sample_batch_commit over several steps (step advanced on device, some
     rows running out of positions, one row with invalid parameters) leaves the
     same tokens, next ids, positions, ring, head and fault word as
     arc_sample_batch followed by arc_decode_commit, and both match the oracle
-    commit of the sampled tokens.  The single-row batch takes the one-launch
-    cluster path, the others the two-kernel path."""
+    commit of the sampled tokens.  The single-row and small fp32 batches take
+    the one-launch cluster path, the others the two-kernel path (the tied
+    batch of 8 rows with a cluster of 8 finish CTAs per row, CTA 0 committing)."""
     import torch
     from device_logits_sampling_gb300 import workloads as wl
 
