@@ -21,17 +21,6 @@ constexpr int kCand = 256;                 // crossing-bin candidates gathered p
 constexpr int kMaxCluster = 16;
 
 // ------------------------------------------------------------------ PTX
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// 16-byte asynchronous global -> shared copy (both 16-byte aligned), cached
-// in L2 only; completes at the issuing thread's next cp_async_wait_all.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // IEEE max that propagates NaN (max.NaN, sm_80+).
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float r;
