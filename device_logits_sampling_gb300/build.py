@@ -1,7 +1,7 @@
 """Build the sampling library in-tree for sm_103a (GB300).
 
 Produces device_logits_sampling_gb300/_lib/libarcsample.so from csrc/: one
-nvcc process per translation unit, all at once (the four kernel sets
+nvcc process per translation unit, all at once (the six kernel sets
 dominate the build), then one link.  Runs on any host with nvcc (no GPU
 needed).
 """
@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libarcsample.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("kernels_bf16.cu", "kernels_bf16_hist.cu", "kernels_f32.cu",
-                                            "kernels_f32_hist.cu", "arc_sample.cu", "arc_decode.cu")]
+                                            "kernels_f32_hist.cu", "kernels_f16.cu", "kernels_f16_hist.cu",
+                                            "arc_sample.cu", "arc_decode.cu")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

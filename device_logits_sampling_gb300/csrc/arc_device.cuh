@@ -6,6 +6,7 @@
 #include <cooperative_groups.h>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "arc_sample.h"
@@ -146,6 +147,52 @@ struct Elem<ARC_BF16> {
             const uint32_t lo = (i < n) ? __ldg(p + i) : 0xFF80u;
             const uint32_t hi = (i + 1 < n) ? __ldg(p + i + 1) : 0xFF80u;
             w[h] = lo | (hi << 16);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+template <>
+struct Elem<ARC_F16> {
+    static constexpr int kVec = 8;
+    static constexpr int kBytes = 2;
+    __device__ __forceinline__ static float h(uint32_t bits) {  // exact widening
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+    }
+    __device__ __forceinline__ static void unpack(const uint4& v, float (&z)[8]) {
+        z[0] = h(v.x & 0xFFFFu);
+        z[1] = h(v.x >> 16);
+        z[2] = h(v.y & 0xFFFFu);
+        z[3] = h(v.y >> 16);
+        z[4] = h(v.z & 0xFFFFu);
+        z[5] = h(v.z >> 16);
+        z[6] = h(v.w & 0xFFFFu);
+        z[7] = h(v.w >> 16);
+    }
+    // max of the vector, propagating NaN (packed half2 max, exact)
+    __device__ __forceinline__ static float vmax_nan(const uint4& v) {
+        const __half2 a = *reinterpret_cast<const __half2*>(&v.x);
+        const __half2 b = *reinterpret_cast<const __half2*>(&v.y);
+        const __half2 c = *reinterpret_cast<const __half2*>(&v.z);
+        const __half2 d = *reinterpret_cast<const __half2*>(&v.w);
+        const __half2 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+        return fmax_nan(__low2float(m), __high2float(m));
+    }
+    __device__ __forceinline__ static float load_scalar(const void* row, int64_t i) {
+        return h(__ldg(reinterpret_cast<const unsigned short*>(row) + i));
+    }
+    // vector v of a slice in global memory holding n elements; elements past
+    // n read as -inf; 16-byte load when the slice start is 16-byte aligned
+    __device__ __forceinline__ static uint4 global_vec(const void* base, int v, int n, bool aligned) {
+        if (aligned && (v + 1) * 8 <= n) return ld_nc_v4(static_cast<const char*>(base) + static_cast<size_t>(v) * 16);
+        const unsigned short* p = static_cast<const unsigned short*>(base);
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = v * 8 + 2 * k;
+            const uint32_t lo = (i < n) ? __ldg(p + i) : 0xFC00u;
+            const uint32_t hi = (i + 1 < n) ? __ldg(p + i + 1) : 0xFC00u;
+            w[k] = lo | (hi << 16);
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
     }

@@ -49,7 +49,17 @@ struct Plan {
     size_t ws_bytes = 0;
 };
 
-int elem_bytes(int dtype) { return dtype == ARC_BF16 ? 2 : 4; }
+int elem_bytes(int dtype) { return dtype == ARC_F32 ? 4 : 2; }
+bool known_dtype(int dtype) { return dtype == ARC_F32 || dtype == ARC_BF16 || dtype == ARC_F16; }
+
+// One call of F on the kernel set of (dtype, history): F receives a value of
+// type KernelSet<DT, HIST> (its static members are the calls).
+template <class F>
+auto with_kernel_set(int dtype, bool hist, F f) {
+    if (dtype == ARC_BF16) return hist ? f(KernelSet<ARC_BF16, true>{}) : f(KernelSet<ARC_BF16, false>{});
+    if (dtype == ARC_F16) return hist ? f(KernelSet<ARC_F16, true>{}) : f(KernelSet<ARC_F16, false>{});
+    return hist ? f(KernelSet<ARC_F32, true>{}) : f(KernelSet<ARC_F32, false>{});
+}
 
 int pow2_at_least(int64_t x) {
     int p = 1;
@@ -65,7 +75,7 @@ int ceil_log2(int64_t v) {
 
 int check_common(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dtype, const int32_t* out) {
     if (logits == nullptr || out == nullptr) return ARC_E_NULL;
-    if (dtype != ARC_F32 && dtype != ARC_BF16) return ARC_E_DTYPE;
+    if (!known_dtype(dtype)) return ARC_E_DTYPE;
     if (B <= 0 || V <= 0 || V > INT_MAX || ld < V) return ARC_E_SHAPE;
     if (B > (int64_t{1} << 24)) return ARC_E_SHAPE;
     if (reinterpret_cast<uintptr_t>(logits) % static_cast<uintptr_t>(elem_bytes(dtype)) != 0) return ARC_E_ALIGN;
@@ -216,7 +226,7 @@ int num_sms_of(int dev) {
     return v;
 }
 
-std::atomic<uint64_t> g_prep_argmax[2];
+std::atomic<uint64_t> g_prep_argmax[3];
 
 // Scratch of arc_sample_batch_static, for callers that cannot allocate device
 // memory: one array per device context, created with the module.  Host code
@@ -235,7 +245,7 @@ const char* arc_sample_strerror(int code) {
         case ARC_OK: return "ok";
         case ARC_E_NULL: return "a required pointer is NULL";
         case ARC_E_SHAPE: return "bad shape: need B > 0, 0 < V <= 2^31-1 and ld >= V";
-        case ARC_E_DTYPE: return "dtype must be ARC_F32 or ARC_BF16";
+        case ARC_E_DTYPE: return "dtype must be ARC_F32, ARC_BF16 or ARC_F16";
         case ARC_E_ALIGN: return "logits pointer is not aligned to its element size";
         case ARC_E_UNSUPPORTED: return "the vocabulary needs more CTAs per row than allowed";
         case ARC_E_OPTION: return "bad field in arc_sample_options";
@@ -249,7 +259,7 @@ const char* arc_sample_strerror(int code) {
 int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history, const arc_sample_options* opts,
                     arc_sample_geometry* geom) {
     if (geom == nullptr) return ARC_E_NULL;
-    if (dtype != ARC_F32 && dtype != ARC_BF16) return ARC_E_DTYPE;
+    if (!known_dtype(dtype)) return ARC_E_DTYPE;
     if (B <= 0 || V <= 0 || V > INT_MAX || B > (int64_t{1} << 24)) return ARC_E_SHAPE;
     int rc = check_options(opts);
     if (rc != ARC_OK) return rc;
@@ -271,7 +281,7 @@ int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history, co
 
 size_t arc_sample_workspace_bytes(int64_t B, int64_t V, int32_t dtype, int32_t has_history,
                                   const arc_sample_options* opts) {
-    if (dtype != ARC_F32 && dtype != ARC_BF16) return 0;
+    if (!known_dtype(dtype)) return 0;
     if (B <= 0 || V <= 0 || V > INT_MAX || B > (int64_t{1} << 24)) return 0;
     if (check_options(opts) != ARC_OK) return 0;
     Plan p;
@@ -318,13 +328,7 @@ int sample_impl(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dt
     if (p.cluster) {
         // the one-launch cluster kernel, when the device can schedule its clusters
         const int dyn = std::max(p.scan_smem, p.fin_smem);
-        bool fits;
-        if (dtype == ARC_BF16)
-            fits = has_hist ? KernelSet<ARC_BF16, true>::cluster_ok(p.s, dyn, dev)
-                            : KernelSet<ARC_BF16, false>::cluster_ok(p.s, dyn, dev);
-        else
-            fits = has_hist ? KernelSet<ARC_F32, true>::cluster_ok(p.s, dyn, dev)
-                            : KernelSet<ARC_F32, false>::cluster_ok(p.s, dyn, dev);
+        const bool fits = with_kernel_set(dtype, has_hist, [&](auto k) { return k.cluster_ok(p.s, dyn, dev); });
         if (!fits) {
             rc = make_plan(B, V, dtype, has_hist, opts, num_sms_of(dev), p, false);
             if (rc != ARC_OK) return rc;
@@ -333,13 +337,8 @@ int sample_impl(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dt
     if (workspace_bytes < p.ws_bytes) return ARC_E_WORKSPACE;
     if (!p.cluster && p.fin_g > 1) {
         // a split finish only when the device can schedule its clusters
-        bool ok;
-        if (dtype == ARC_BF16)
-            ok = has_hist ? KernelSet<ARC_BF16, true>::finish_cluster_ok(p.fin_g, p.fin_smem, dev)
-                          : KernelSet<ARC_BF16, false>::finish_cluster_ok(p.fin_g, p.fin_smem, dev);
-        else
-            ok = has_hist ? KernelSet<ARC_F32, true>::finish_cluster_ok(p.fin_g, p.fin_smem, dev)
-                          : KernelSet<ARC_F32, false>::finish_cluster_ok(p.fin_g, p.fin_smem, dev);
+        const bool ok =
+            with_kernel_set(dtype, has_hist, [&](auto k) { return k.finish_cluster_ok(p.fin_g, p.fin_smem, dev); });
         if (!ok) p.fin_g = 1;
     }
 
@@ -399,18 +398,10 @@ int sample_impl(const void* logits, int64_t B, int64_t V, int64_t ld, int32_t dt
     if (p.cluster) {
         const FusedArgs fu{sa, fa};
         const int dyn = std::max(p.scan_smem, p.fin_smem);
-        if (dtype == ARC_BF16)
-            e = has_hist ? KernelSet<ARC_BF16, true>::launch_fused(fu, B, p.s, dyn, st)
-                         : KernelSet<ARC_BF16, false>::launch_fused(fu, B, p.s, dyn, st);
-        else
-            e = has_hist ? KernelSet<ARC_F32, true>::launch_fused(fu, B, p.s, dyn, st)
-                         : KernelSet<ARC_F32, false>::launch_fused(fu, B, p.s, dyn, st);
-    } else if (dtype == ARC_BF16) {
-        e = has_hist ? KernelSet<ARC_BF16, true>::launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st)
-                     : KernelSet<ARC_BF16, false>::launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st);
+        e = with_kernel_set(dtype, has_hist, [&](auto k) { return k.launch_fused(fu, B, p.s, dyn, st); });
     } else {
-        e = has_hist ? KernelSet<ARC_F32, true>::launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st)
-                     : KernelSet<ARC_F32, false>::launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st);
+        e = with_kernel_set(dtype, has_hist,
+                            [&](auto k) { return k.launch_two(sa, fa, p.s, B, p.scan_smem, p.fin_smem, dev, st); });
     }
     return e == cudaSuccess ? ARC_OK : ARC_E_CUDA;
 }
@@ -491,6 +482,9 @@ int arc_sample_greedy(const void* logits, int64_t B, int64_t V, int64_t ld, int3
     if (dtype == ARC_BF16) {
         e = prepare(argmax_kernel<ARC_BF16>, dev, g_prep_argmax[1], 0);
         if (e == cudaSuccess) e = launch_cluster(argmax_kernel<ARC_BF16>, B * s, s, 0, st, a);
+    } else if (dtype == ARC_F16) {
+        e = prepare(argmax_kernel<ARC_F16>, dev, g_prep_argmax[2], 0);
+        if (e == cudaSuccess) e = launch_cluster(argmax_kernel<ARC_F16>, B * s, s, 0, st, a);
     } else {
         e = prepare(argmax_kernel<ARC_F32>, dev, g_prep_argmax[0], 0);
         if (e == cudaSuccess) e = launch_cluster(argmax_kernel<ARC_F32>, B * s, s, 0, st, a);

@@ -720,8 +720,9 @@ __device__ __forceinline__ void scan_cta(const ScanArgs& a, int row, int cidx, S
     const int nv = (n + VEC - 1) / VEC;
     const char* sp = static_cast<const char*>(a.logits) +
                      (static_cast<int64_t>(row) * a.ld + static_cast<int64_t>(a0)) * E::kBytes;
-    const uint4 ninf = (DT == ARC_BF16) ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
-                                        : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+    const uint4 ninf = (DT == ARC_BF16)  ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                       : (DT == ARC_F16) ? make_uint4(0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u)
+                                         : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
     uint64_t pw[6];
     params_words_nc<HIST>(a.params + row, pw);
     uint4 d[kVpt];

@@ -12,7 +12,7 @@ import os
 
 import numpy as np
 
-from .workloads import DTYPE_BF16, DTYPE_F32, ROW_PARAMS_DTYPE
+from .workloads import DTYPE_BF16, DTYPE_F16, DTYPE_F32, ROW_PARAMS_DTYPE
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libarcsample.so")
@@ -178,7 +178,9 @@ def _dtype_code(t) -> int:
         return DTYPE_BF16
     if t.dtype == torch.float32:
         return DTYPE_F32
-    raise TypeError(f"logits must be bfloat16 or float32, not {t.dtype}")
+    if t.dtype == torch.float16:
+        return DTYPE_F16
+    raise TypeError(f"logits must be bfloat16, float16 or float32, not {t.dtype}")
 
 
 def _stream(stream) -> int:
@@ -311,6 +313,8 @@ def logits_tensor(wl, device="cuda", ld: int | None = None):
 
     if wl.dtype == DTYPE_BF16:
         host = torch.from_numpy(np.ascontiguousarray(wl.logits).view(np.int16)).view(torch.bfloat16)
+    elif wl.dtype == DTYPE_F16:
+        host = torch.from_numpy(np.ascontiguousarray(wl.logits).view(np.int16)).view(torch.float16)
     else:
         host = torch.from_numpy(np.ascontiguousarray(wl.logits, dtype=np.float32))
     if ld is None or ld == wl.V:

@@ -25,6 +25,7 @@ VOCAB_V4 = 129_280
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+DTYPE_F16 = 2
 
 # Layout of one per-row parameter record, identical to `arc_row_params` in
 # include/arc_sample.h (48 bytes, little endian).
@@ -63,6 +64,26 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to IEEE half (numpy's round to nearest, ties to even);
+    return uint16 bits."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen IEEE half bit patterns to fp32 values (exact)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def as_f16(w: "Workload") -> "Workload":
+    """The same rows as fp16 logits, rounded to nearest (exact for every value
+    in fp16's normal range, 2^-14 .. 65,504 in magnitude, with at most 11
+    significant bits: bf16 values there included)."""
+    import dataclasses
+
+    return dataclasses.replace(w, name=w.name + "_as_f16", dtype=DTYPE_F16, logits=f32_to_f16_bits(w.logits_f32()))
+
+
 def make_params(B: int) -> np.ndarray:
     """B parameter records with every filter disabled and T = 1."""
     p = np.zeros(B, dtype=ROW_PARAMS_DTYPE)
@@ -78,8 +99,8 @@ def make_params(B: int) -> np.ndarray:
 class Workload:
     """One batch of sampler inputs.
 
-    logits: [B, V] array.  For dtype == DTYPE_BF16 it holds uint16 bf16 bit
-    patterns, for DTYPE_F32 float32 values.
+    logits: [B, V] array.  For dtype == DTYPE_BF16 (DTYPE_F16) it holds uint16
+    bf16 (IEEE half) bit patterns, for DTYPE_F32 float32 values.
     hist_offsets / hist_ids: CSR token history (None when no row has one).
     """
 
@@ -101,12 +122,14 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 2 if self.dtype == DTYPE_BF16 else 4
+        return 4 if self.dtype == DTYPE_F32 else 2
 
     def logits_f32(self) -> np.ndarray:
         """The logits as fp32 values (exact widening for bf16)."""
         if self.dtype == DTYPE_BF16:
             return bf16_bits_to_f32(self.logits)
+        if self.dtype == DTYPE_F16:
+            return f16_bits_to_f32(self.logits)
         return np.asarray(self.logits, dtype=np.float32)
 
     def history(self, row: int) -> np.ndarray:
@@ -241,7 +264,7 @@ def random_case(seed: int, B: int, V: int, dtype: int, *, ties: bool = False,
     if ties:
         x = np.round(x * 2.0) / 2.0
     x = x.astype(np.float32)
-    logits = f32_to_bf16_bits(x) if dtype == DTYPE_BF16 else x
+    logits = f32_to_bf16_bits(x) if dtype == DTYPE_BF16 else (f32_to_f16_bits(x) if dtype == DTYPE_F16 else x)
     p = make_params(B)
     for r in range(B):
         kind = r % 6 if param_mix == "all" else int(param_mix)

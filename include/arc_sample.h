@@ -67,18 +67,19 @@ extern "C" {
 #endif
 
 /* 3: arc_commit_record (arc_decode.h) stamps each of its three words;
- *    arc_sample_batch_commit; arc_sample_geometry.finish_ctas */
+ *    arc_sample_batch_commit; arc_sample_geometry.finish_ctas; ARC_F16 */
 #define ARC_SAMPLE_ABI_VERSION 3
 
 /* logits element types */
 #define ARC_F32 0
 #define ARC_BF16 1
+#define ARC_F16 2
 
 /* host-side return codes: nothing was enqueued when a call returns < 0 */
 #define ARC_OK 0
 #define ARC_E_NULL (-1)        /* a required pointer is NULL */
 #define ARC_E_SHAPE (-2)       /* B <= 0, V <= 0, V > 2^31-1 or ld < V */
-#define ARC_E_DTYPE (-3)       /* dtype is not ARC_F32 / ARC_BF16 */
+#define ARC_E_DTYPE (-3)       /* dtype is not ARC_F32 / ARC_BF16 / ARC_F16 */
 #define ARC_E_ALIGN (-4)       /* logits not aligned to the element size */
 #define ARC_E_UNSUPPORTED (-5) /* a row does not fit on chip (see arc_sample_plan) */
 #define ARC_E_OPTION (-6)      /* bad field in arc_sample_options */
@@ -187,7 +188,7 @@ typedef struct arc_sample_options {
 
 /*
  * Sample one token per row.
- *   logits        device, [B rows][ld elements], ARC_F32 or ARC_BF16, aligned
+ *   logits        device, [B rows][ld elements], ARC_F32, ARC_BF16 or ARC_F16, aligned
  *                 to its element size (16-byte aligned rows use 16-byte loads)
  *   B, V, ld      rows, vocabulary, row stride in elements (ld >= V)
  *   params        device [B]; written only under ARC_OPT_STEP_AUTOINC

@@ -89,10 +89,11 @@ def test_bad_arguments_fail_before_any_cuda_call(lib):
     assert call_batch(lib, V=0) == sampler.ARC_E_SHAPE
     assert call_batch(lib, V=2**31) == sampler.ARC_E_SHAPE
     assert call_batch(lib, ld=7) == sampler.ARC_E_SHAPE
-    assert call_batch(lib, dtype=2) == sampler.ARC_E_DTYPE
+    assert call_batch(lib, dtype=3) == sampler.ARC_E_DTYPE
     assert call_batch(lib, dtype=-1) == sampler.ARC_E_DTYPE
     assert call_batch(lib, logits=FAKE + 1) == sampler.ARC_E_ALIGN
     assert call_batch(lib, logits=FAKE + 2, dtype=0) == sampler.ARC_E_ALIGN
+    assert call_batch(lib, logits=FAKE + 1, dtype=2) == sampler.ARC_E_ALIGN  # fp16: 2-byte elements
     assert call_batch(lib, params=FAKE + 4) == sampler.ARC_E_ALIGN
     assert call_batch(lib, opts=sampler.Options(0, 129, 0, 0, None)) == sampler.ARC_E_OPTION
     assert call_batch(lib, opts=sampler.Options(0, -1, 0, 0, None)) == sampler.ARC_E_OPTION
@@ -136,6 +137,9 @@ def test_plan_geometry(lib):
     assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16, ctas_per_row=32).launches == 2
     # fp32 rows of 129,280 need 32 slices: more than a cluster holds
     assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_F32).launches == 2
+    # fp16 rows slice like bf16 rows (8 logits per 16-byte vector)
+    g16 = sampler.plan(256, workloads.VOCAB_V4, workloads.DTYPE_F16)
+    assert (g16.ctas_per_row, g16.slice_elems, g16.grid_ctas) == (16, 8080, 4096)
     # fp32 slices hold half as many logits
     assert sampler.plan(64, workloads.VOCAB_V4, workloads.DTYPE_F32).ctas_per_row == 32
     # finish CTAs per row: one while the batch fills the SMs (two finish CTAs

@@ -120,12 +120,33 @@ def test_greedy_kernel_is_exact_argmax(cuda_lib, name):
     (1, 1, 0, 3), (5, 0, 0, 4), (8, 1, 0, 5), (9, 1, 0, 6), (1000, 0, 0, 12), (4097, 1, 0, 12),
     (12345, 1, 0, 12), (12345, 0, 3, 12), (4097, 1, 8, 12), (33333, 1, 1, 12), (200_000, 1, 0, 6),
     (129_280, 0, 4, 6),
+    # fp16 logits
+    (7, 2, 0, 4), (4097, 2, 3, 12), (33333, 2, 0, 12), (129_280, 2, 0, 40), (200_000, 2, 8, 6),
 ])
 def test_ragged_and_strided_rows(cuda_lib, V, dtype, ld_pad, B):
     w = wl.random_case(seed=V * 7 + dtype + ld_pad, B=B, V=V, dtype=dtype, ties=(V % 2 == 1))
     tokens, dbg, err = run(cuda_lib, w, ld=V + ld_pad if ld_pad else None)
     rep = parity.check_batch(w, tokens, dbg)
     assert rep.rows == B
+
+
+@pytest.mark.parametrize("name", ["small_fp32", "mixed_quarters", "penalized", "adversarial_ties"])
+def test_fp16_logits_parity(cuda_lib, name):
+    """The named workloads as fp16 logits: the oracle on the fp16 values, the
+    same rules; greedy rows also through arc_sample_greedy."""
+    import torch
+
+    w = wl.as_f16(wl.NAMED[name]())
+    res = oracle.sample_batch(w.logits_f32(), w.params, w.hist_offsets, w.hist_ids)
+    tokens, dbg, err = run(cuda_lib, w, max_hist_len=256 if w.hist_offsets is not None else 0)
+    rep = parity.check_batch(w, tokens, dbg, results=res)
+    assert rep.rows == w.B
+    assert err & ~parity.GPU_ERR_NAN == 0, hex(err)
+    assert rep.set_exempt + rep.token_exempt <= max(2, w.B // 50)
+    out = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    cuda_lib.sample_greedy(cuda_lib.logits_tensor(w), out)
+    torch.cuda.synchronize()
+    assert out.cpu().numpy().tolist() == np.argmax(w.logits_f32(), axis=1).tolist()
 
 
 @pytest.mark.parametrize("hist_len", [1, 64, 700])
