@@ -289,7 +289,10 @@ def bench_config(sampler, workloads, name, peak, steps, repeats):
     import numpy as np
     import torch
 
-    w = getattr(workloads, name[0])(**name[1])
+    kw = {k: v for k, v in name[1].items() if k != "f16"}
+    w = getattr(workloads, name[0])(**kw)
+    if name[1].get("f16"):
+        w = workloads.as_f16(w)
     B, V = w.B, w.V
     nbuf = max(2, min(NBUF, int(3 * 129e6 // (B * V * w.elem_bytes)) + 1))
     bufs = [sampler.logits_tensor(w) for _ in range(nbuf)]
@@ -316,7 +319,8 @@ def bench_config(sampler, workloads, name, peak, steps, repeats):
     med, mn = statistics.median(ts), min(ts)
     alg = B * V * w.elem_bytes + B * 48 + B * 4 + (4 * int(w.hist_ids.size) + 4 * (B + 1) if hoff is not None else 0)
     filt = d["mode"] == 2
-    rec = {"B": B, "V": V, "logits_dtype": "bf16" if w.dtype == workloads.DTYPE_BF16 else "f32",
+    rec = {"B": B, "V": V, "logits_dtype": {workloads.DTYPE_F32: "f32", workloads.DTYPE_BF16: "bf16",
+                                            workloads.DTYPE_F16: "f16"}[w.dtype],
            "us_per_step_median": med, "us_per_step_min": mn, "rows_per_s": B / (med * 1e-6),
            "achieved_gbs": alg / (med * 1e-6) / 1e9, "frac_of_measured_peak": alg / (med * 1e-6) / 1e9 / peak,
            "alg_bytes": alg, "steps": steps, "repeats": repeats, "input_copies": nbuf,
@@ -335,6 +339,7 @@ CONFIGS = [  # the five synthetic workloads, in the order of the configuration l
     ("mixed_batch", {}),
     ("penalized_batch", {}),
     ("adversarial_ties", {}),
+    ("mixed_batch", {"f16": True}),  # the mixed batch's values as fp16 logits
 ]
 
 
@@ -350,6 +355,8 @@ def bench_only_config(args) -> None:
     peak = measured_peaks().get("hbm_gbs") or 6800.0
     kw = {"greedy": True} if args.only_config == "single_row_peaked_greedy" else {}
     name = "single_row_peaked" if args.only_config.startswith("single_row_peaked") else args.only_config
+    if name.endswith("_f16"):  # e.g. mixed_batch_f16: the workload's values as fp16 logits
+        name, kw = name[: -len("_f16")], {**kw, "f16": True}
     key, rec = bench_config(sampler, workloads, (name, kw), peak, max(1, args.steps), max(1, args.repeats))
     print(json.dumps({"workload": key, **rec}))
 
@@ -612,7 +619,7 @@ def main():
     ap.add_argument("--repeats", type=int, default=5, help="timed regions of K steps (median and min reported)")
     ap.add_argument("--only-config", default=None,
                     help="time one synthetic workload only (small_fp32, single_row_peaked[_greedy], mixed_batch, "
-                         "penalized_batch, adversarial_ties) and print its record")
+                         "penalized_batch, adversarial_ties; a _f16 suffix: as fp16 logits) and print its record")
     ap.add_argument("--decode-loop", action="store_true", help="time the decode-loop commit (separate JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
