@@ -1893,35 +1893,20 @@ __device__ __forceinline__ void finish_row(const FinishArgs& a, int row, KernelS
                 const int Lv = a.L / VEC;
                 int* whole = reinterpret_cast<int*>(dyn + a.clist_off);  // listed chunks
                 // the ids of a vector >= zf take slots from one shared counter
-                // the lanes that emit together take their slots with one
-                // shared atomic: each lane's offset is the sum of the counts
-                // of the active lanes below it, bit by bit from ballots
                 auto emit = [&](const float (&z)[VEC], int vrow) {
-                    uint32_t cnt = 0;
+                    int cnt = 0;
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1u : 0u;
-                    const unsigned am = __activemask();
-                    __syncwarp(am);
-                    const unsigned below = am & ((1u << lane) - 1u);
-                    uint32_t pre = 0, tot = 0;
+                    for (int e = 0; e < VEC; ++e) cnt += (z[e] >= zf) ? 1 : 0;
+                    if (cnt > 0) {
+                        uint32_t pos = atomicAdd(&SS.ccount, static_cast<uint32_t>(cnt));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {  // cnt <= VEC <= 8
-                        const unsigned b = __ballot_sync(am, (cnt >> k) & 1u);
-                        pre += static_cast<uint32_t>(__popc(b & below)) << k;
-                        tot += static_cast<uint32_t>(__popc(b)) << k;
-                    }
-                    if (tot == 0) return;
-                    const int leader = __ffs(am) - 1;
-                    uint32_t base = 0;
-                    if (lane == leader) base = atomicAdd(&SS.ccount, tot);
-                    uint32_t pos = __shfl_sync(am, base, leader) + pre;
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        if (z[e] >= zf) {
-                            if (pos < static_cast<uint32_t>(kCandCap))
-                                cc[pos] = (static_cast<uint64_t>(fkey(z[e])) << 32) |
-                                          (0xFFFFFFFFu - static_cast<uint32_t>(vrow * VEC + e));
-                            ++pos;
+                        for (int e = 0; e < VEC; ++e) {
+                            if (z[e] >= zf) {
+                                if (pos < static_cast<uint32_t>(kCandCap))
+                                    cc[pos] = (static_cast<uint64_t>(fkey(z[e])) << 32) |
+                                              (0xFFFFFFFFu - static_cast<uint32_t>(vrow * VEC + e));
+                                ++pos;
+                            }
                         }
                     }
                 };
