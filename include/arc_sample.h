@@ -272,8 +272,8 @@ int arc_sample_plan(int64_t B, int64_t V, int32_t dtype, int32_t has_history,
  * Limit: a shape whose workspace on this device (arc_sample_plan
  * workspace_bytes = B x slices-per-row x 1,664 bytes) exceeds
  * ARC_STATIC_WORKSPACE_BYTES returns ARC_E_WORKSPACE with nothing enqueued.
- * At V = 129,280 a row has 16 slices in bf16 and 32 in fp32, so B up to 630
- * (bf16) or 315 (fp32) is accepted.  Nothing in the array needs to start at
+ * At V = 129,280 a row has 16 slices in bf16 or fp16 and 32 in fp32, so B up
+ * to 630 (bf16, fp16) or 315 (fp32) is accepted.  Nothing in the array needs to start at
  * zero: each call writes every byte it later uses.  Every call on a device
  * shares the one array, so calls that may overlap on the GPU (different
  * streams without an ordering between them, or concurrent host threads)

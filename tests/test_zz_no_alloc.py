@@ -68,6 +68,7 @@ def test_static_limits_are_the_documented_ones():
     S = sampler
     S.load()
     assert _largest_accepted(S, 129_280, workloads.DTYPE_BF16) == 630
+    assert _largest_accepted(S, 129_280, workloads.DTYPE_F16) == 630
     assert _largest_accepted(S, 129_280, workloads.DTYPE_F32) == 315
 
 
