@@ -529,6 +529,48 @@ def bench_gpu(args) -> None:
         torch.distributed.destroy_process_group()
 
 
+def bench_small_batches(args) -> None:
+    """--small-batches: per-step latency of small batches of the mixed rows
+    (V = 129,280 bf16) on the one-launch cluster path and on the two-kernel
+    path (forced by an explicit slice count), and the path the library picks,
+    so that the choice per B can be checked against both."""
+    import torch
+
+    from device_logits_sampling_gb300 import sampler, workloads
+
+    torch.cuda.set_device(0)
+    sampler.load()
+    n = max(1, args.steps)
+    rows = []
+    for B in (1, 2, 4, 8, 16, 19, 20, 32, 64):
+        w = workloads.mixed_batch(B=B)
+        nbuf = max(2, min(NBUF, int(3 * 129e6 // (B * w.V * w.elem_bytes)) + 1))
+        bufs = [sampler.logits_tensor(w) for _ in range(nbuf)]
+        prm = sampler.params_tensor(w.params)
+        out = torch.zeros(B, dtype=torch.int32, device="cuda")
+        st = torch.cuda.Stream()
+        rec = {"B": B, "chosen_launches": sampler.plan(B, w.V, w.dtype).launches}
+        for label, cpr in (("auto_us", 0), ("two_kernel_us", 16)):
+            ws = sampler.workspace_tensor(B, w.V, w.dtype, ctas_per_row=cpr)
+
+            def call(x, ws=ws, cpr=cpr):
+                sampler.sample_batch(x, prm, out, workspace=ws, ctas_per_row=cpr, stream=st)
+
+            with torch.cuda.stream(st):
+                call(bufs[0])
+            st.synchronize()
+            g = graph_steps(sampler, st, bufs, call, n)
+            g.replay()
+            st.synchronize()
+            rec[label] = statistics.median(time_steps(st, [(g, n)], max(1, args.repeats)))
+        rows.append(rec)
+        del bufs
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "small-batch step latency, mixed rows, V=129,280 bf16: the library's choice "
+                                "(one cluster launch when B x 16 CTAs fit two per SM) against two kernels",
+                      "unit": "us", "higher_is_better": False, "steps": n, "rows": rows}))
+
+
 def bench_decode_loop(args) -> None:
     """--decode-loop: the decode step after sampling (arc_decode_commit into a
     pinned host ring).  Times, with CUDA events over graph replays on the
@@ -621,11 +663,15 @@ def main():
                     help="time one synthetic workload only (small_fp32, single_row_peaked[_greedy], mixed_batch, "
                          "penalized_batch, adversarial_ties; a _f16 suffix: as fp16 logits) and print its record")
     ap.add_argument("--decode-loop", action="store_true", help="time the decode-loop commit (separate JSON line)")
+    ap.add_argument("--small-batches", action="store_true",
+                    help="small-batch latency: cluster path against two kernels (separate JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.only_config:
         bench_only_config(args)
+    elif args.small_batches:
+        bench_small_batches(args)
     elif args.decode_loop:
         bench_decode_loop(args)
     elif args.impl == "reference":
