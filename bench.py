@@ -567,7 +567,7 @@ def bench_small_batches(args) -> None:
         del bufs
         torch.cuda.empty_cache()
     print(json.dumps({"metric": "small-batch step latency, mixed rows, V=129,280 bf16: the library's choice "
-                                "(one cluster launch when B x 16 CTAs fit two per SM) against two kernels",
+                                "(one cluster launch for B <= 8) against two kernels with 16 slices per row",
                       "unit": "us", "higher_is_better": False, "steps": n, "rows": rows}))
 
 

@@ -93,11 +93,16 @@ int check_options(const arc_sample_options* o) {
 }
 
 // Geometry: a row is cut into s slices of at most kVpt * kThreads 16-byte
-// vectors (one scan CTA each); small batches use more, smaller slices so that
-// every SM gets work.  A batch whose rows fit in clusters of at most 16 CTAs,
-// all resident at once (two per SM), takes the one-launch cluster kernel when
-// `allow_cluster`; an explicit ctas_per_row always takes the two kernels.
+// vectors (one scan CTA each), as few as the row allows: every slice adds 32
+// chunk entries to the row's finish, and on the mixed rows at V = 129,280
+// more, smaller slices were slower at every batch size measured (20 rows:
+// 19.0 us with 61 slices against 11.3 us with 16).  A batch of at most 8 rows
+// whose rows fit in clusters of at most 16 CTAs, all resident at once (two
+// per SM), takes the one-launch cluster kernel when `allow_cluster` (at 16
+// rows and more the two kernels were faster); an explicit ctas_per_row always
+// takes the two kernels.
 constexpr int kClusterMax = 16;
+constexpr int kClusterMaxRows = 8;
 constexpr int kFinishClusterMax = 8;
 constexpr int64_t kSmemPerSM = 233472;  // shared memory of an SM (228 KB)
 
@@ -109,7 +114,7 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     int64_t s;
     const bool automatic = o == nullptr || o->ctas_per_row == 0;
     bool cluster = false;
-    if (automatic && allow_cluster) {
+    if (automatic && allow_cluster && B <= kClusterMaxRows) {
         const int64_t s_min = (V + slice_max - 1) / slice_max;
         const int64_t s_cap = std::max<int64_t>(1, V / 1024);
         const int64_t fs =
@@ -123,11 +128,7 @@ int make_plan(int64_t B, int64_t V, int dtype, bool has_hist, const arc_sample_o
     } else if (!automatic) {
         s = o->ctas_per_row;
     } else {
-        const int64_t s_min = (V + slice_max - 1) / slice_max;
-        const int64_t s_want = (8 * int64_t{num_sms} + B - 1) / B;
-        const int64_t s_cap = std::max<int64_t>(1, V / 1024);
-        s = std::max<int64_t>(s_min, std::min<int64_t>(s_want, s_cap));
-        s = std::min<int64_t>(s, kMaxRowCtas);
+        s = std::min<int64_t>((V + slice_max - 1) / slice_max, kMaxRowCtas);
     }
     if (s * slice_max < V || s > kMaxRowCtas) return ARC_E_UNSUPPORTED;
     const int64_t per = (V + s - 1) / s;

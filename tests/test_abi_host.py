@@ -129,10 +129,15 @@ def test_plan_geometry(lib):
     # summaries combined in distributed shared memory, no workspace)
     g1 = sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16)
     assert (g1.launches, g1.ctas_per_row, g1.grid_ctas, g1.workspace_bytes) == (1, 16, 16, 0)
-    # up to 19 such rows fit the GPU at once (16 CTAs each, two per SM); 20 take two launches
-    assert sampler.plan(19, workloads.VOCAB_V4, workloads.DTYPE_BF16).launches == 1
+    # up to 8 such rows take the cluster kernel; more take two launches with
+    # the fewest slices a row allows (16 for bf16 at V = 129,280)
+    assert sampler.plan(8, workloads.VOCAB_V4, workloads.DTYPE_BF16).launches == 1
+    g9 = sampler.plan(9, workloads.VOCAB_V4, workloads.DTYPE_BF16)
+    assert g9.launches == 2 and g9.ctas_per_row == 16
     g20 = sampler.plan(20, workloads.VOCAB_V4, workloads.DTYPE_BF16)
-    assert g20.launches == 2 and g20.ctas_per_row >= 16
+    assert g20.launches == 2 and g20.ctas_per_row == 16
+    # small vocabularies too take the fewest slices (one here)
+    assert sampler.plan(64, 20_000, workloads.DTYPE_BF16).ctas_per_row == 3
     # an explicit slice count always takes the two kernels
     assert sampler.plan(1, workloads.VOCAB_V4, workloads.DTYPE_BF16, ctas_per_row=32).launches == 2
     # fp32 rows of 129,280 need 32 slices: more than a cluster holds
